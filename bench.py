@@ -1,0 +1,455 @@
+"""Benchmark of the binned-summation hot path on GB300.
+
+One step = one pass of every hot-path row over its full-size synthetic input:
+  binned sum, K=3:            float32 N(0,1) 100M; float64 wide-range 100M
+  binned cumulative sum, K=3: the same two arrays (out of place)
+  segmented binned sum, K=3:  [4096, 4096] float32 rows
+  float32 variance kernel:    [4096, 4096] float32, axis 1, ddof 1
+The value is elements processed per second over the whole step
+(GElements/s); per-row device times, the roofline of the dominant kernel, an
+end-to-end run through the C ABI with host buffers, comparison baselines and
+the CPU oracle's rate are reported on the same JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+N_SUM = 100_000_000
+ROWS = COLS = 4096
+METRIC = "GElements/s and % HBM roofline: ADN sum/cumsum 100M fp32/fp64 K=3; var [4096²]"
+WORKLOAD = ("adn sum+cumsum 1e8 f32 N(0,1) & 1e8 f64 wide-range (K=3) + segmented sum and "
+            "stable_var_f32 [4096,4096] axis1 ddof1")
+# algorithmic bytes per element of each row (input read once, output written once)
+ROWS_SPEC = [
+    # name, elements, bytes/element
+    ("var_f32_4096x4096", ROWS * COLS, 4),
+    ("sum_f32_1e8", N_SUM, 4),
+    ("segsum_f32_4096x4096", ROWS * COLS, 4),
+    ("cumsum_f32_1e8", N_SUM, 8),
+    ("sum_f64_1e8", N_SUM, 8),
+    ("cumsum_f64_1e8", N_SUM, 16),
+]
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ ours
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from compensated_bit_reproducible_gb300 import api, inputs
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    api.lib()
+    api.validate_environment()
+    seed_off = 100 * rank
+    h32 = inputs.normal_f32(N_SUM, seed=1 + seed_off)
+    h64 = inputs.wide_f64(N_SUM, seed=2 + seed_off)
+    hA = inputs.offset_rows(ROWS, COLS, seed=3 + seed_off)
+    x32 = torch.from_numpy(h32).to(dev)
+    x64 = torch.from_numpy(h64).to(dev)
+    A = torch.from_numpy(hA).to(dev)
+    c32 = torch.empty_like(x32)
+    c64 = torch.empty_like(x64)
+    s32 = torch.empty(1, dtype=torch.float32, device=dev)
+    s64 = torch.empty(1, dtype=torch.float64, device=dev)
+    vout = torch.empty(ROWS, dtype=torch.float32, device=dev)
+    vmean = torch.empty(ROWS, dtype=torch.float32, device=dev)
+    segout = torch.empty(ROWS, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    calls = {
+        "var_f32_4096x4096": lambda: api.stable_var(A, axis=1, ddof=1, out=vout, mean_out=vmean),
+        "sum_f32_1e8": lambda: api.repro_sum_async(x32, s32, 3),
+        "segsum_f32_4096x4096": lambda: api.repro_segsum(A, axis=1, K=3, out=segout),
+        "cumsum_f32_1e8": lambda: api.repro_cumsum(x32, out=c32, K=3),
+        "sum_f64_1e8": lambda: api.repro_sum_async(x64, s64, 3),
+        "cumsum_f64_1e8": lambda: api.repro_cumsum(x64, out=c64, K=3),
+    }
+    launches_per_row = {"var_f32_4096x4096": 1, "sum_f32_1e8": 1, "segsum_f32_4096x4096": 1,
+                        "cumsum_f32_1e8": 3, "sum_f64_1e8": 1, "cumsum_f64_1e8": 3}
+
+    def step(evs=None):
+        for name, _, _ in ROWS_SPEC:
+            if evs is not None:
+                evs[name][0].append(torch.cuda.Event(enable_timing=True))
+                evs[name][0][-1].record(stream)
+            calls[name]()
+            if evs is not None:
+                evs[name][1].append(torch.cuda.Event(enable_timing=True))
+                evs[name][1][-1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(ws)
+    clocks = ClockSampler(local)
+    clocks.start()
+    evs = {name: ([], []) for name, _, _ in ROWS_SPEC}
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(evs)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    clk = clocks.stop()
+    ms_total = t0.elapsed_time(t1)
+    ms_total = max_over_ranks(ms_total, ws)
+    ms_step = ms_total / args.steps
+    elems_step = sum(n for _, n, _ in ROWS_SPEC)
+    value = elems_step * ws / (ms_step * 1e-3) / 1e9
+    hbm, peak_kind = load_peaks()
+    rows = {}
+    for name, n, bpe in ROWS_SPEC:
+        durs = [a.elapsed_time(b) for a, b in zip(*evs[name])]
+        ms = sum(durs) / len(durs)
+        rows[name] = {"ms": round(ms, 4), "gelem_s": round(n / (ms * 1e-3) / 1e9, 2),
+                      "gb_s": round(n * bpe / (ms * 1e-3) / 1e9, 1),
+                      "hbm_frac": round(n * bpe / (ms * 1e-3) / 1e9 / hbm, 4)}
+    dom = max(rows, key=lambda k: rows[k]["ms"])
+    dom_n, dom_bpe = [(n, b) for nm, n, b in ROWS_SPEC if nm == dom][0]
+    achieved = dom_n * dom_bpe / (rows[dom]["ms"] * 1e-3) / 1e9
+    traffic = load_traffic(dom)
+    # correctness of what was timed: the two 1e8 sums against host checks
+    torch.cuda.synchronize()
+
+    # end to end through the C ABI: pinned host buffers in, results out
+    e2e = run_e2e(args, api, torch, h32, h64, hA, dev, stream)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_seconds)
+    comparisons = run_comparisons(api, torch, x32, x64, A, stream)
+    gpu_launches = args.steps * sum(launches_per_row.values())
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "GElements/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32+f64 inputs, exact int64/int128 binned lanes",
+        "data": "synthetic (seeded numpy generators, shapes and distributions of the pages' workloads)",
+        "config": {"workload": WORKLOAD, "K": 3, "elements_per_step_per_gpu": elems_step,
+                   "l2": "every input is larger than L2 or follows >= 400 MB of other traffic in the step",
+                   "parallelism": "independent replicas" if ws > 1 else "single GPU"},
+        "rows": rows,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": hbm,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                     "traffic": traffic},
+        "e2e": e2e,
+        "gpu_launches": gpu_launches,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+        "comparisons": comparisons,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def load_traffic(kernel_row: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary (profiles/traffic.json), or None when not captured for the
+    current kernel version."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    v = d.get(kernel_row)
+    return v.get("dram_bytes_per_launch") if isinstance(v, dict) and v.get("current") else None
+
+
+def run_e2e(args, api, torch, h32, h64, hA, dev, stream):
+    """Same step through the C ABI from pinned host buffers: every input is
+    copied host->device and every result device->host inside the timed
+    region."""
+    p32 = torch.from_numpy(h32).pin_memory()
+    p64 = torch.from_numpy(h64).pin_memory()
+    pA = torch.from_numpy(hA).pin_memory()
+    oc32 = torch.empty(N_SUM, dtype=torch.float32).pin_memory()
+    oc64 = torch.empty(N_SUM, dtype=torch.float64).pin_memory()
+    ov = torch.empty(ROWS, dtype=torch.float32).pin_memory()
+    om = torch.empty(ROWS, dtype=torch.float32).pin_memory()
+    oseg = torch.empty(ROWS, dtype=torch.float32).pin_memory()
+    d32 = torch.empty(N_SUM, dtype=torch.float32, device=dev)
+    d64 = torch.empty(N_SUM, dtype=torch.float64, device=dev)
+    dA = torch.empty(ROWS, COLS, dtype=torch.float32, device=dev)
+    res = {}
+
+    def one():
+        dA.copy_(pA, non_blocking=True)
+        v, m = api.stable_var(dA, axis=1, ddof=1)
+        ov.copy_(v, non_blocking=True)
+        om.copy_(m, non_blocking=True)
+        res["s32"] = api.repro_sum(p32, 3)            # host pointer: the library copies it
+        oseg.copy_(api.repro_segsum(dA, axis=1, K=3), non_blocking=True)
+        d32.copy_(p32, non_blocking=True)
+        api.repro_cumsum(d32, out=d32, K=3)
+        oc32.copy_(d32, non_blocking=True)
+        res["s64"] = api.repro_sum(p64, 3)
+        d64.copy_(p64, non_blocking=True)
+        api.repro_cumsum(d64, out=d64, K=3)
+        oc64.copy_(d64, non_blocking=True)
+        torch.cuda.synchronize()
+
+    one()
+    n = max(1, args.e2e_steps)
+    t = time.perf_counter()
+    for _ in range(n):
+        one()
+    dt = (time.perf_counter() - t) / n
+    elems = sum(nn for _, nn, _ in ROWS_SPEC)
+    h2d = 4 * N_SUM * 2 + 8 * N_SUM * 2 + 4 * ROWS * COLS
+    d2h = 4 * N_SUM + 8 * N_SUM + 4 + 8 + 3 * 4 * ROWS
+    return {"value": round(elems / dt / 1e9, 3), "unit": "GElements/s", "ms_per_step": round(dt * 1e3, 3),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+def run_comparisons(api, torch, x32, x64, A, stream):
+    """Context only: non-reproducible and comparison reductions on the same
+    inputs (device time per call, CUDA events)."""
+    def timed(fn, reps=5):
+        fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    out = {}
+    for name, fn, n in (
+        ("naive_sum_f32_1e8", lambda: api.compare_sum(x32, "naive"), N_SUM),
+        ("pairwise_sum_f32_1e8", lambda: api.compare_sum(x32, "pairwise"), N_SUM),
+        ("torch_sum_f32_1e8", lambda: torch.sum(x32), N_SUM),
+        ("naive_sum_f64_1e8", lambda: api.compare_sum(x64, "naive"), N_SUM),
+        ("torch_sum_f64_1e8", lambda: torch.sum(x64), N_SUM),
+        ("torch_cumsum_f32_1e8", lambda: torch.cumsum(x32, 0), N_SUM),
+        ("torch_cumsum_f64_1e8", lambda: torch.cumsum(x64, 0), N_SUM),
+        ("twoterm_var_f32_4096x4096", lambda: api.twoterm_var(A, axis=1, ddof=1), ROWS * COLS),
+        ("torch_var_f32_4096x4096", lambda: torch.var(A, dim=1), ROWS * COLS),
+    ):
+        ms = timed(fn)
+        out[name] = {"ms": round(ms, 4), "gelem_s": round(n / (ms * 1e-3) / 1e9, 2)}
+    return out
+
+
+# ------------------------------------------------------------ oracle (CPU)
+def oracle_rates(seconds: float):
+    """Oracle throughput per hot-path row on bounded samples of the workload
+    (single thread).  Returns ({row: elements/s}, description)."""
+    import numpy as np
+
+    import oracle
+    from compensated_bit_reproducible_gb300 import inputs
+
+    oracle.build()
+    budget = max(1.0, seconds / 6.0)
+    rates = {}
+    samples = {}
+
+    def measure(name, fn, unit_elems, max_reps=64):
+        reps, el, t0 = 0, 0, time.perf_counter()
+        while reps < max_reps:
+            fn()
+            reps += 1
+            el += unit_elems
+            if time.perf_counter() - t0 >= budget:
+                break
+        dt = time.perf_counter() - t0
+        rates[name] = el / dt
+        samples[name] = "%d x %d elements" % (reps, unit_elems)
+
+    n = 2_000_000
+    a32 = inputs.normal_f32(N_SUM, seed=1)[:n].copy()
+    a64 = inputs.wide_f64(N_SUM, seed=2)[:n].copy()
+    A = inputs.offset_rows(ROWS, COLS, seed=3)[:128].copy()
+    measure("sum_f32_1e8", lambda: oracle.adn_sum(a32, 3, "fp"), n)
+    measure("sum_f64_1e8", lambda: oracle.adn_sum(a64, 3, "fp"), n)
+    m = 200_000
+    measure("cumsum_f32_1e8", lambda: oracle.adn_cumsum(a32[:m], 3), m)
+    measure("cumsum_f64_1e8", lambda: oracle.adn_cumsum(a64[:m], 3), m)
+    measure("var_f32_4096x4096", lambda: oracle.var_kernel(A, 1, 1), A.size)
+    measure("segsum_f32_4096x4096", lambda: oracle.segsum(A[:32], 1, 3), 32 * COLS)
+    return rates, samples
+
+
+def cpu_baseline(seconds: float):
+    rates, samples = oracle_rates(seconds)
+    t_step = sum(n / rates[name] for name, n, _ in ROWS_SPEC)
+    elems = sum(n for _, n, _ in ROWS_SPEC)
+    return {"value": round(elems / t_step / 1e9, 6), "unit": "GElements/s", "cores": 1, "kind": "oracle",
+            "sample": "per row: " + "; ".join("%s %s" % (k, v) for k, v in samples.items()) +
+                      " (step time extrapolated from each row's rate)",
+            "rows_gelem_s": {k: round(v / 1e9, 6) for k, v in rates.items()}}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    t = []
+    for _ in range(args.warmup):
+        oracle_rates(args.cpu_seconds / 3)
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        rates, samples = oracle_rates(args.cpu_seconds / 3)
+        t.append((rates, samples, time.perf_counter() - t0))
+    # each step: the oracle's rate on bounded samples -> whole-step rate
+    vals = []
+    for rates, _, _ in t:
+        t_step = sum(n / rates[name] for name, n, _ in ROWS_SPEC)
+        vals.append(sum(n for _, n, _ in ROWS_SPEC) / t_step / 1e9)
+    v = statistics.mean(vals)
+    ms = statistics.mean(x[2] for x in t) * 1e3
+    line = {"metric": METRIC, "value": round(v, 6), "unit": "GElements/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 1), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32+f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "K": 3},
+            "cpu_baseline": {"value": round(v, 6), "unit": "GElements/s", "cores": 1, "kind": "oracle",
+                             "sample": "per step, bounded samples of each row: " +
+                                       "; ".join("%s %s" % kv for kv in t[-1][1].items())},
+            "e2e": {"value": round(v, 6), "unit": "GElements/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------ distributed
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, ws: int) -> float:
+    if ws <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def init_dist(ws):
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    ws, _, _ = dist_env()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    init_dist(ws)
+    run_ours(args)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,441 @@
+// Binned cumulative sum (SyclReproSum README, "How It Works", cumsum
+// paragraph): contiguous tiles are reduced to binned totals, the totals are
+// scanned exclusively in binned form, and each tile is replayed from its
+// incoming state, converting every prefix.  Only tile totals and tile
+// prefixes are stored.  Each output uses the index of its own prefix, so
+// every prefix is bit-identical for any launch shape and out[n-1] equals the
+// binned sum.
+#include "accum.cuh"
+#include "launch.h"
+
+namespace repro {
+
+constexpr int CS_BLOCK = 256;
+constexpr int CS_ITEMS = 16;
+constexpr int CS_TILE = CS_BLOCK * CS_ITEMS;
+
+template <int N> struct SState {
+  int I;
+  int flags;
+  W128 F[N];
+};
+
+template <int N>
+__device__ __forceinline__ void sstate_zero(SState<N>& s, int I0) {
+  s.I = I0;
+  s.flags = 0;
+#pragma unroll(N <= 8 ? N : 1)
+  for (int k = 0; k < N; ++k) s.F[k] = W128{0, 0};
+}
+
+// a <- merge(a, b): both re-expressed at the smaller index, folds added.
+template <int N>
+__device__ __forceinline__ void sstate_merge(SState<N>& a, const SState<N>& b, int K) {
+  int I = min(a.I, b.I);
+  int da = a.I - I, db = b.I - I;
+  W128 r[N];
+#pragma unroll(N <= 8 ? N : 1)
+  for (int k = 0; k < N; ++k) r[k] = w_add(fold_at<N, W128>(a.F, K, k - da), fold_at<N, W128>(b.F, K, k - db));
+#pragma unroll(N <= 8 ? N : 1)
+  for (int k = 0; k < N; ++k) a.F[k] = r[k];
+  a.I = I;
+  a.flags |= b.flags;
+}
+
+template <int N>
+__device__ __forceinline__ SState<N> sstate_shfl_up(const SState<N>& s, int d) {
+  SState<N> o;
+  o.I = __shfl_up_sync(0xffffffffu, s.I, d);
+  o.flags = __shfl_up_sync(0xffffffffu, s.flags, d);
+#pragma unroll(N <= 8 ? N : 1)
+  for (int k = 0; k < N; ++k) o.F[k] = shfl_up_w(s.F[k], d);
+  return o;
+}
+
+// Exclusive scan of one state per thread across the block.  Returns the
+// merge of the states of all lower threads (identity for thread 0) and, in
+// *total, the merge of all.  Uses `sm` (one SState per warp).
+template <int N>
+__device__ SState<N> block_exclusive_scan(const SState<N>& mine, int K, int I0, SState<N>* sm,
+                                          SState<N>* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  SState<N> inc = mine;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    SState<N> o = sstate_shfl_up(inc, d);
+    if (lane >= d) {
+      SState<N> t = o;
+      sstate_merge(t, inc, K);
+      inc = t;
+    }
+  }
+  SState<N> exc = sstate_shfl_up(inc, 1);
+  if (lane == 0) sstate_zero(exc, I0);
+  if (lane == 31) sm[warp] = inc;
+  __syncthreads();
+  SState<N> base;
+  sstate_zero(base, I0);
+  for (int w = 0; w < warp; ++w) sstate_merge(base, sm[w], K);
+  if (total) {
+    sstate_zero(*total, I0);
+    for (int w = 0; w < nw; ++w) sstate_merge(*total, sm[w], K);
+  }
+  sstate_merge(base, exc, K);
+  __syncthreads();
+  return base;
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void sstate_deposit(SState<N>& s, T x, int K) {
+  uint64_t a = abs_bits<T>(x);
+  if (a >= (sizeof(T) == 4 ? 0x7F800000ull : 0x7FF0000000000000ull)) {
+    s.flags |= special_flag(x);
+    return;
+  }
+  if (x == (T)0) return;
+  int j = bin_index<T>(x);
+  if (j < s.I) {
+    int d = s.I - j;
+    W128 t[N];
+#pragma unroll(N <= 8 ? N : 1)
+    for (int k = 0; k < N; ++k) t[k] = fold_at<N, W128>(s.F, K, k - d);
+#pragma unroll(N <= 8 ? N : 1)
+    for (int k = 0; k < N; ++k) s.F[k] = t[k];
+    s.I = j;
+  }
+  int64_t dg[N];
+  chain_digits<T>(x, s.I, K, dg);
+#pragma unroll(N <= 8 ? N : 1)
+  for (int k = 0; k < N; ++k)
+    if (k < K) s.F[k] = w_add(s.F[k], w_from(dg[k]));
+}
+
+template <typename T, int N>
+__device__ __forceinline__ T sstate_value(const SState<N>& s, int K) {
+  State<N> st;
+  st.I = s.I;
+  st.flags = s.flags;
+#pragma unroll(N <= 8 ? N : 1)
+  for (int k = 0; k < N; ++k) st.F[k] = s.F[k];
+  return convert_state<T, N>(st, K);
+}
+
+// Tile staging: coalesced copy of the tile into shared memory, thread t then
+// owns elements [t * ITEMS, (t + 1) * ITEMS) of it.
+template <typename T>
+__device__ __forceinline__ int load_tile(const T* __restrict__ in, int64_t n, int64_t tile, T* sm) {
+  int64_t base = tile * CS_TILE;
+  int cnt = (int)min((int64_t)CS_TILE, n - base);
+  for (int i = threadIdx.x; i < cnt; i += blockDim.x) sm[i + i / CS_ITEMS] = in[base + i];
+  __syncthreads();
+  return cnt;
+}
+
+template <typename T, int KT>
+__global__ void __launch_bounds__(CS_BLOCK) cumsum_tile_reduce(const T* __restrict__ in, int64_t n, int K,
+                                                               unsigned char* __restrict__ tstate) {
+  constexpr int N = KArr<T, KT>::N;
+  __shared__ T sm[CS_TILE + CS_TILE / CS_ITEMS];
+  int cnt = load_tile<T>(in, n, blockIdx.x, sm);
+  SState<N> s;
+  sstate_zero(s, Geom<T>::NB - K);
+  int b = threadIdx.x * CS_ITEMS;
+  for (int i = 0; i < CS_ITEMS; ++i)
+    if (b + i < cnt) sstate_deposit<T, N>(s, sm[b + i + b / CS_ITEMS], K);
+  int64_t L[N];
+  // block merge works on int64 lanes; a tile's fold sums fit (4096 * 2^39)
+#pragma unroll(N <= 8 ? N : 1)
+  for (int k = 0; k < N; ++k) L[k] = (int64_t)s.F[k].lo;
+  State<N> st;
+  block_merge<N>(s.I, s.flags, L, K, &st);
+  if (threadIdx.x == 0) store_partial<N>(tstate, blockIdx.x, K, st);
+}
+
+template <int N>
+__device__ __forceinline__ void load_sstate(SState<N>& s, const unsigned char* base, int64_t idx, int K) {
+  const unsigned char* p = base + (size_t)idx * (16 + 16 * (size_t)K);
+  s.I = ((const int*)p)[0];
+  s.flags = ((const int*)p)[1];
+#pragma unroll(N <= 8 ? N : 1)
+  for (int k = 0; k < N; ++k) {
+    const int64_t* q = (const int64_t*)(p + 16) + 2 * k;
+    s.F[k] = (k < K) ? W128{(uint64_t)q[0], q[1]} : W128{0, 0};
+  }
+}
+
+template <int N>
+__device__ __forceinline__ void store_sstate(const SState<N>& s, unsigned char* base, int64_t idx, int K) {
+  unsigned char* p = base + (size_t)idx * (16 + 16 * (size_t)K);
+  ((int*)p)[0] = s.I;
+  ((int*)p)[1] = s.flags;
+  for (int k = 0; k < K; ++k) {
+    int64_t* q = (int64_t*)(p + 16) + 2 * k;
+    q[0] = (int64_t)s.F[k].lo;
+    q[1] = s.F[k].hi;
+  }
+}
+
+// One block: exclusive scan of the tile totals into tile prefixes.
+template <typename T, int KT>
+__global__ void __launch_bounds__(1024) cumsum_tile_scan(const unsigned char* __restrict__ tstate, int64_t ntiles,
+                                                         int K, unsigned char* __restrict__ tpref) {
+  constexpr int N = KArr<T, KT>::N;
+  __shared__ SState<N> sm[32];
+  const int I0 = Geom<T>::NB - K;
+  int64_t per = (ntiles + blockDim.x - 1) / blockDim.x;
+  int64_t b = (int64_t)threadIdx.x * per, e = min(ntiles, b + per);
+  SState<N> agg, x;
+  sstate_zero(agg, I0);
+  for (int64_t t = b; t < e; ++t) {
+    load_sstate(x, tstate, t, K);
+    sstate_merge(agg, x, K);
+  }
+  SState<N> run = block_exclusive_scan<N>(agg, K, I0, sm, nullptr);
+  for (int64_t t = b; t < e; ++t) {
+    store_sstate(run, tpref, t, K);
+    load_sstate(x, tstate, t, K);
+    sstate_merge(run, x, K);
+  }
+}
+
+template <typename T, int KT>
+__global__ void __launch_bounds__(CS_BLOCK) cumsum_replay(const T* in, T* out, int64_t n, int K,
+                                                          const unsigned char* __restrict__ tpref) {
+  constexpr int N = KArr<T, KT>::N;
+  __shared__ T sm[CS_TILE + CS_TILE / CS_ITEMS];
+  __shared__ SState<N> wsm[CS_BLOCK / 32];
+  const int I0 = Geom<T>::NB - K;
+  int cnt = load_tile<T>(in, n, blockIdx.x, sm);
+  int b = threadIdx.x * CS_ITEMS;
+  SState<N> mine;
+  sstate_zero(mine, I0);
+  for (int i = 0; i < CS_ITEMS; ++i)
+    if (b + i < cnt) sstate_deposit<T, N>(mine, sm[b + i + b / CS_ITEMS], K);
+  SState<N> run = block_exclusive_scan<N>(mine, K, I0, wsm, nullptr);
+  SState<N> tp;
+  load_sstate(tp, tpref, blockIdx.x, K);
+  sstate_merge(tp, run, K);
+  for (int i = 0; i < CS_ITEMS; ++i) {
+    if (b + i < cnt) {
+      int si = b + i + b / CS_ITEMS;
+      sstate_deposit<T, N>(tp, sm[si], K);
+      sm[si] = sstate_value<T, N>(tp, K);
+    }
+  }
+  __syncthreads();
+  int64_t base = (int64_t)blockIdx.x * CS_TILE;
+  for (int i = threadIdx.x; i < cnt; i += blockDim.x) out[base + i] = sm[i + i / CS_ITEMS];
+}
+
+// ------------------------------------------------------------------
+// Run-time K (K > 8): a plain design.  Tile totals come from per-thread int64
+// lanes and the exact block merge (as in the sum); the tile scan and the
+// replay run on one thread per block with the binned state in shared memory.
+template <typename T> struct GState {
+  static constexpr int N = KMax<T>::V;
+  int I;
+  int flags;
+  uint64_t lo[N];
+  int64_t hi[N];
+  int64_t dg[N];
+  uint32_t limb[ConvLimbs<T>::N];
+};
+
+template <typename T>
+__device__ void gs_zero(GState<T>* s, int K) {
+  s->I = Geom<T>::NB - K;
+  s->flags = 0;
+  for (int k = 0; k < K; ++k) { s->lo[k] = 0; s->hi[k] = 0; }
+}
+
+template <typename T>
+__device__ void gs_add(GState<T>* s, int k, W128 v) {
+  W128 r = w_add(W128{s->lo[k], s->hi[k]}, v);
+  s->lo[k] = r.lo;
+  s->hi[k] = r.hi;
+}
+
+// Re-express at the coarser index j < s->I (descending, in place: every
+// read index is below the written one).
+template <typename T>
+__device__ void gs_raise(GState<T>* s, int j, int K) {
+  int d = s->I - j;
+  for (int k = K - 1; k >= 0; --k) {
+    if (k >= d) { s->lo[k] = s->lo[k - d]; s->hi[k] = s->hi[k - d]; }
+    else { s->lo[k] = 0; s->hi[k] = 0; }
+  }
+  s->I = j;
+}
+
+// s <- merge(s, state stored at p)
+template <typename T>
+__device__ void gs_merge_stored(GState<T>* s, const unsigned char* p, int K) {
+  int Ib = ((const int*)p)[0];
+  if (Ib < s->I) gs_raise(s, Ib, K);
+  int d = Ib - s->I;
+  s->flags |= ((const int*)p)[1];
+  const int64_t* F = (const int64_t*)(p + 16);
+  for (int k = d; k < K; ++k) gs_add(s, k, W128{(uint64_t)F[2 * (k - d)], F[2 * (k - d) + 1]});
+}
+
+template <typename T>
+__device__ void gs_store(const GState<T>* s, unsigned char* p, int K) {
+  ((int*)p)[0] = s->I;
+  ((int*)p)[1] = s->flags;
+  int64_t* F = (int64_t*)(p + 16);
+  for (int k = 0; k < K; ++k) { F[2 * k] = (int64_t)s->lo[k]; F[2 * k + 1] = s->hi[k]; }
+}
+
+template <typename T>
+__device__ void gs_deposit(GState<T>* s, T x, int K) {
+  uint64_t a = abs_bits<T>(x);
+  if (a >= (sizeof(T) == 4 ? 0x7F800000ull : 0x7FF0000000000000ull)) {
+    s->flags |= special_flag(x);
+    return;
+  }
+  if (x == (T)0) return;
+  int j = bin_index<T>(x);
+  if (j < s->I) gs_raise(s, j, K);
+  chain_digits<T>(x, s->I, K, s->dg);
+  for (int k = 0; k < K; ++k) gs_add(s, k, w_from(s->dg[k]));
+}
+
+// Correct rounding of the state (same arithmetic as convert_state, limbs in
+// the shared state).
+template <typename T>
+__device__ T gs_value(GState<T>* s, int K) {
+  typedef Geom<T> G;
+  if (s->flags) return from_flags<T>(s->flags);
+  constexpr int NLMAX = ConvLimbs<T>::N;
+  int nl = (G::W * (K - 1) + 134) / 32 + 2;
+  if (nl > NLMAX) nl = NLMAX;
+  uint32_t* limb = s->limb;
+  for (int i = 0; i < nl; ++i) limb[i] = 0;
+  for (int k = 0; k < K; ++k) {
+    uint64_t vlo = s->lo[k];
+    int64_t vhi = s->hi[k];
+    if (vlo == 0 && vhi == 0) continue;
+    int off = G::W * (K - 1 - k);
+    int li = off >> 5, sh = off & 31;
+    uint32_t ext = (vhi < 0) ? 0xFFFFFFFFu : 0u;
+    uint32_t src[5] = {(uint32_t)vlo, (uint32_t)(vlo >> 32), (uint32_t)vhi, (uint32_t)((uint64_t)vhi >> 32), ext};
+    uint32_t carry = 0;
+    for (int i = li; i < nl; ++i) {
+      int r = i - li;
+      uint32_t addv;
+      if (r < 5) addv = sh ? ((src[r] << sh) | (r ? (src[r - 1] >> (32 - sh)) : 0u)) : src[r];
+      else addv = ext;
+      uint64_t t = (uint64_t)limb[i] + addv + carry;
+      limb[i] = (uint32_t)t;
+      carry = (uint32_t)(t >> 32);
+    }
+  }
+  bool neg = (limb[nl - 1] >> 31) != 0;
+  if (neg) {
+    uint32_t c = 1;
+    for (int i = 0; i < nl; ++i) {
+      uint64_t t = (uint64_t)(~limb[i]) + c;
+      limb[i] = (uint32_t)t;
+      c = (uint32_t)(t >> 32);
+    }
+  }
+  return round_limbs<T>(neg, limb, nl, beta<T>(s->I + K - 1));
+}
+
+template <typename T>
+__global__ void __launch_bounds__(CS_BLOCK) cumsum_generic_reduce(const T* __restrict__ in, int64_t n, int K,
+                                                                  unsigned char* __restrict__ tstate) {
+  typedef typename AccOf<T, 0>::type Acc;
+  constexpr int N = Acc::N;
+  int64_t base = (int64_t)blockIdx.x * CS_TILE;
+  int64_t cnt = min((int64_t)CS_TILE, n - base);
+  Acc acc;
+  acc.init(K);
+  for (int64_t i = threadIdx.x; i < cnt; i += blockDim.x) {
+    T v[1] = {in[base + i]};
+    acc.template chunk<1>(v);
+  }
+  acc.finish();
+  State<N> st;
+  block_merge<N>(acc.I, acc.flags, acc.L, K, &st);
+  if (threadIdx.x == 0) store_partial<N>(tstate, blockIdx.x, K, st);
+}
+
+template <typename T>
+__global__ void cumsum_generic_scan(const unsigned char* __restrict__ tstate, int64_t ntiles, int K,
+                                    unsigned char* __restrict__ tpref) {
+  __shared__ GState<T> s;
+  if (threadIdx.x != 0) return;
+  const size_t st = 16 + 16 * (size_t)K;
+  gs_zero(&s, K);
+  for (int64_t t = 0; t < ntiles; ++t) {
+    gs_store(&s, tpref + (size_t)t * st, K);
+    gs_merge_stored(&s, tstate + (size_t)t * st, K);
+  }
+}
+
+template <typename T>
+__global__ void cumsum_generic_replay(const T* in, T* out, int64_t n, int K, const unsigned char* __restrict__ tpref) {
+  __shared__ GState<T> s;
+  if (threadIdx.x != 0) return;
+  const size_t st = 16 + 16 * (size_t)K;
+  int64_t base = (int64_t)blockIdx.x * CS_TILE;
+  int64_t cnt = min((int64_t)CS_TILE, n - base);
+  gs_zero(&s, K);
+  gs_merge_stored(&s, tpref + (size_t)blockIdx.x * st, K);
+  for (int64_t i = 0; i < cnt; ++i) {
+    gs_deposit(&s, in[base + i], K);
+    out[base + i] = gs_value(&s, K);
+  }
+}
+
+template <typename T>
+size_t cumsum_workspace_bytes(int64_t n, int K) {
+  int64_t nt = (n + CS_TILE - 1) / CS_TILE;
+  return 2 * (size_t)nt * (16 + 16 * (size_t)K) + 64;
+}
+
+template <typename T, int KT>
+static cudaError_t launch_cumsum_k(const T* in, T* out, int64_t n, int K, unsigned char* ws, cudaStream_t s) {
+  int64_t nt = (n + CS_TILE - 1) / CS_TILE;
+  unsigned char* tstate = ws;
+  unsigned char* tpref = ws + (size_t)nt * (16 + 16 * (size_t)K);
+  cumsum_tile_reduce<T, KT><<<(unsigned)nt, CS_BLOCK, 0, s>>>(in, n, K, tstate);
+  cumsum_tile_scan<T, KT><<<1, 1024, 0, s>>>(tstate, nt, K, tpref);
+  cumsum_replay<T, KT><<<(unsigned)nt, CS_BLOCK, 0, s>>>(in, out, n, K, tpref);
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_cumsum_generic(const T* in, T* out, int64_t n, int K, unsigned char* ws, cudaStream_t s) {
+  int64_t nt = (n + CS_TILE - 1) / CS_TILE;
+  unsigned char* tstate = ws;
+  unsigned char* tpref = ws + (size_t)nt * (16 + 16 * (size_t)K);
+  cumsum_generic_reduce<T><<<(unsigned)nt, CS_BLOCK, 0, s>>>(in, n, K, tstate);
+  cumsum_generic_scan<T><<<1, 32, 0, s>>>(tstate, nt, K, tpref);
+  cumsum_generic_replay<T><<<(unsigned)nt, 32, 0, s>>>(in, out, n, K, tpref);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_cumsum(const T* in, T* out, int64_t n, int K, unsigned char* ws, int block, cudaStream_t s) {
+  (void)block;
+  switch (K) {
+    case 2: return launch_cumsum_k<T, 2>(in, out, n, K, ws, s);
+    case 3: return launch_cumsum_k<T, 3>(in, out, n, K, ws, s);
+    case 4: return launch_cumsum_k<T, 4>(in, out, n, K, ws, s);
+    case 5: return launch_cumsum_k<T, 5>(in, out, n, K, ws, s);
+    case 6: return launch_cumsum_k<T, 6>(in, out, n, K, ws, s);
+    case 7: return launch_cumsum_k<T, 7>(in, out, n, K, ws, s);
+    case 8: return launch_cumsum_k<T, 8>(in, out, n, K, ws, s);
+    default: return launch_cumsum_generic<T>(in, out, n, K, ws, s);
+  }
+}
+
+template size_t cumsum_workspace_bytes<float>(int64_t, int);
+template size_t cumsum_workspace_bytes<double>(int64_t, int);
+template cudaError_t launch_cumsum<float>(const float*, float*, int64_t, int, unsigned char*, int, cudaStream_t);
+template cudaError_t launch_cumsum<double>(const double*, double*, int64_t, int, unsigned char*, int,
+                                           cudaStream_t);
+
+}  // namespace repro

@@ -1,0 +1,237 @@
+// Binned sum: one read of the input, per-thread binned accumulation, exact
+// block merge, and a last-block grid merge + conversion (SyclReproSum README,
+// "How It Works": deposit, renormalize, merge; the sum reads each input
+// element exactly once).  The result bits depend only on the multiset of
+// inputs, never on the grid, block size or scheduling.
+#include "accum.cuh"
+#include "launch.h"
+
+namespace repro {
+
+template <typename T> struct Vec;
+template <> struct Vec<float> { typedef float4 type; static constexpr int W = 4; };
+template <> struct Vec<double> { typedef double2 type; static constexpr int W = 2; };
+
+template <typename T>
+__device__ __forceinline__ void unpack(const typename Vec<T>::type& v, T* out);
+template <> __device__ __forceinline__ void unpack<float>(const float4& v, float* o) {
+  o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+}
+template <> __device__ __forceinline__ void unpack<double>(const double2& v, double* o) {
+  o[0] = v.x; o[1] = v.y;
+}
+
+// Streaming loads that bypass L1 allocation (each byte is used once).
+__device__ __forceinline__ float4 ldg_stream(const float4* p) { return __ldcs(p); }
+__device__ __forceinline__ double2 ldg_stream(const double2* p) { return __ldcs(p); }
+
+// Accumulate x[lo, hi) (any alignment) into acc; thread `t` of `nt`.
+// Vector part: U 16-byte vectors per thread per iteration, interleaved so that
+// each load instruction of a warp covers contiguous memory.
+template <typename T, typename Acc, int U>
+__device__ __forceinline__ void accumulate_range(Acc& acc, const T* __restrict__ x, int64_t n, int64_t t,
+                                                 int64_t nt) {
+  typedef typename Vec<T>::type V;
+  constexpr int VW = Vec<T>::W;
+  int64_t head = (int64_t)(((16 - ((uintptr_t)x & 15)) & 15) / sizeof(T));
+  if (head > n) head = n;
+  const V* xv = (const V*)(x + head);
+  int64_t nv = (n - head) / VW;
+  int64_t i = t;
+  for (; i + (int64_t)(U - 1) * nt < nv; i += (int64_t)U * nt) {
+    V r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) r[u] = ldg_stream(xv + i + (int64_t)u * nt);
+    T v[U * VW];
+#pragma unroll
+    for (int u = 0; u < U; ++u) unpack<T>(r[u], v + u * VW);
+    acc.template chunk<U * VW>(v);
+  }
+  for (; i < nv; i += nt) {
+    T v[VW];
+    unpack<T>(ldg_stream(xv + i), v);
+    acc.template chunk<VW>(v);
+  }
+  // scalar head and tail elements
+  int64_t tail0 = head + nv * VW;
+  int64_t ns = head + (n - tail0);
+  for (int64_t j = t; j < ns; j += nt) {
+    T v[1] = {j < head ? x[j] : x[tail0 + (j - head)]};
+    acc.template chunk<1>(v);
+  }
+}
+
+__device__ __forceinline__ W128 ld_w128_cg(const int64_t* p) {
+  longlong2 v = __ldcg((const longlong2*)p);
+  return W128{(uint64_t)v.x, (int64_t)v.y};
+}
+
+template <int N>
+__device__ void merge_partials_cg(const unsigned char* base, int np, int K, State<N>* out);
+
+// Last-block merge of all partial states.  Loads use the L2-coherent path
+// since the partials were written by other blocks of this launch.
+template <int N>
+__device__ void merge_partials_cg(const unsigned char* base, int np, int K, State<N>* out) {
+  __shared__ int sI[32];
+  __shared__ int sFl[32];
+  __shared__ W128 sF[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const size_t st = 16 + 16 * (size_t)K;
+  int I = 1 << 30, fl = 0;
+  for (int p = threadIdx.x; p < np; p += blockDim.x) {
+    const int* h = (const int*)(base + (size_t)p * st);
+    I = min(I, __ldcg(h));
+    fl |= __ldcg(h + 1);
+  }
+  int wi = __reduce_min_sync(0xffffffffu, I);
+  int wf = (int)__reduce_or_sync(0xffffffffu, (unsigned)fl);
+  if (lane == 0) { sI[warp] = wi; sFl[warp] = wf; }
+  __syncthreads();
+  int Ig = sI[0], fg = 0;
+  for (int w = 0; w < nw; ++w) { Ig = min(Ig, sI[w]); fg |= sFl[w]; }
+  if (threadIdx.x == 0) { out->I = Ig; out->flags = fg; }
+  for (int k = 0; k < K; ++k) {
+    W128 v = W128{0, 0};
+    for (int p = threadIdx.x; p < np; p += blockDim.x) {
+      const unsigned char* q = base + (size_t)p * st;
+      int src = k - (__ldcg((const int*)q) - Ig);
+      if (src >= 0) v = w_add(v, ld_w128_cg((const int64_t*)(q + 16) + 2 * src));
+    }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) v = w_add(v, shfl_xor_w(v, m));
+    __syncthreads();
+    if (lane == 0) sF[warp] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      W128 s = W128{0, 0};
+      for (int w = 0; w < nw; ++w) s = w_add(s, sF[w]);
+      out->F[k] = s;
+    }
+  }
+  __syncthreads();
+}
+
+// Workspace: [0, 256) ticket counter (zero at launch); [256, ...) partials.
+template <typename T, int KT, int U>
+__global__ void __launch_bounds__(1024) adn_sum_kernel(const T* __restrict__ x, int64_t n, int K,
+                                                       unsigned char* __restrict__ ws, T* __restrict__ result) {
+  typedef typename AccOf<T, KT>::type Acc;
+  constexpr int N = Acc::N;
+  Acc acc;
+  acc.init(K);
+  accumulate_range<T, Acc, U>(acc, x, n, (int64_t)blockIdx.x * blockDim.x + threadIdx.x,
+                              (int64_t)gridDim.x * blockDim.x);
+  acc.finish();
+  State<N> st;
+  block_merge<N>(acc.I, acc.flags, acc.L, K, &st);
+  unsigned* ticket = (unsigned*)ws;
+  unsigned char* parts = ws + 256;
+  __shared__ bool last;
+  if (threadIdx.x == 0) {
+    store_partial<N>(parts, blockIdx.x, K, st);
+    __threadfence();
+    unsigned t = atomicAdd(ticket, 1u);
+    last = (t == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  merge_partials_cg<N>(parts, gridDim.x, K, &st);
+  if (threadIdx.x == 0) {
+    *result = convert_state<T, N>(st, K);
+    *ticket = 0u;
+  }
+}
+
+// --------------------------------------------------------- segmented sums
+// One block per row (grid-stride over rows): rows of a row-major [rows, cols]
+// array, any cols.
+template <int KT, int U>
+__global__ void __launch_bounds__(1024) segsum_rows_kernel(const float* __restrict__ x, int64_t rows,
+                                                           int64_t cols, int K, float* __restrict__ out) {
+  typedef AccF<KT> Acc;
+  constexpr int N = Acc::N;
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    Acc acc;
+    acc.init(K);
+    accumulate_range<float, Acc, U>(acc, x + r * cols, cols, threadIdx.x, blockDim.x);
+    acc.finish();
+    State<N> st;
+    block_merge<N>(acc.I, acc.flags, acc.L, K, &st);
+    if (threadIdx.x == 0) out[r] = convert_state<float, N>(st, K);
+    __syncthreads();
+  }
+}
+
+// One thread per column, rows walked in order (coalesced across columns).
+template <int KT>
+__global__ void __launch_bounds__(256) segsum_cols_kernel(const float* __restrict__ x, int64_t rows,
+                                                          int64_t cols, int K, float* __restrict__ out) {
+  typedef AccF<KT> Acc;
+  constexpr int N = Acc::N;
+  int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  Acc acc;
+  acc.init(K);
+  for (int64_t r = 0; r < rows; ++r) {
+    float v[1] = {x[r * cols + c]};
+    acc.template chunk<1>(v);
+  }
+  acc.finish();
+  State<N> st;
+  st.I = acc.I;
+  st.flags = acc.flags;
+  for (int k = 0; k < N; ++k) st.F[k] = w_from((k < K) ? acc.L[k] : 0);
+  out[c] = convert_state<float, N>(st, K);
+}
+
+// ------------------------------------------------------------------ launch
+template <typename T, int KT>
+static cudaError_t launch_sum_k(const T* x, int64_t n, int K, unsigned char* ws, T* result, int grid, int block,
+                                cudaStream_t s) {
+  constexpr int U = 4;
+  adn_sum_kernel<T, KT, U><<<grid, block, 0, s>>>(x, n, K, ws, result);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_sum(const T* x, int64_t n, int K, unsigned char* ws, T* result, int grid, int block,
+                       cudaStream_t s) {
+  switch (K) {
+    case 2: return launch_sum_k<T, 2>(x, n, K, ws, result, grid, block, s);
+    case 3: return launch_sum_k<T, 3>(x, n, K, ws, result, grid, block, s);
+    case 4: return launch_sum_k<T, 4>(x, n, K, ws, result, grid, block, s);
+    case 5: return launch_sum_k<T, 5>(x, n, K, ws, result, grid, block, s);
+    case 6: return launch_sum_k<T, 6>(x, n, K, ws, result, grid, block, s);
+    case 7: return launch_sum_k<T, 7>(x, n, K, ws, result, grid, block, s);
+    case 8: return launch_sum_k<T, 8>(x, n, K, ws, result, grid, block, s);
+    default: return launch_sum_k<T, 0>(x, n, K, ws, result, grid, block, s);
+  }
+}
+
+template cudaError_t launch_sum<float>(const float*, int64_t, int, unsigned char*, float*, int, int, cudaStream_t);
+template cudaError_t launch_sum<double>(const double*, int64_t, int, unsigned char*, double*, int, int,
+                                        cudaStream_t);
+
+size_t sum_workspace_bytes(int K, int grid) { return 256 + (size_t)grid * (16 + 16 * (size_t)K) + 64; }
+
+cudaError_t launch_segsum(const float* x, int64_t rows, int64_t cols, int axis, int K, float* out, int grid,
+                          int block, cudaStream_t s) {
+  if (axis == 1) {
+    switch (K) {
+      case 3: segsum_rows_kernel<3, 4><<<grid, block, 0, s>>>(x, rows, cols, K, out); break;
+      case 2: segsum_rows_kernel<2, 4><<<grid, block, 0, s>>>(x, rows, cols, K, out); break;
+      default: segsum_rows_kernel<0, 1><<<grid, block, 0, s>>>(x, rows, cols, K, out); break;
+    }
+  } else {
+    int g = (int)((cols + 255) / 256);
+    switch (K) {
+      case 3: segsum_cols_kernel<3><<<g, 256, 0, s>>>(x, rows, cols, K, out); break;
+      default: segsum_cols_kernel<0><<<g, 256, 0, s>>>(x, rows, cols, K, out); break;
+    }
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace repro

@@ -1,0 +1,333 @@
+// C-ABI entry points (declared in include/repro.h).  Argument, capacity and
+// overlap checks run before any pointer is touched or memory allocated
+// ("SyclReproSum" README, "Accumulator capacity": the length error comes
+// before the pointer is inspected).  Temporary memory comes from the
+// stream-ordered allocator on the caller's stream.
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include "../../include/repro.h"
+#include "launch.h"
+
+using namespace repro;
+
+namespace {
+
+thread_local int g_last_cuda = 0;
+
+repro_status cuda_fail(cudaError_t e) {
+  g_last_cuda = (int)e;
+  return REPRO_ERR_CUDA;
+}
+#define CK(call)                                  \
+  do {                                            \
+    cudaError_t _e = (call);                      \
+    if (_e != cudaSuccess) return cuda_fail(_e);  \
+  } while (0)
+
+// "Accumulator capacity": (2^(p-1) - 1) carries, one per 2^(p-W-2) deposits.
+constexpr uint64_t MAX_COUNT_F32 = ((1ull << 23) - 1) << 9;
+constexpr uint64_t MAX_COUNT_F64 = ((1ull << 52) - 1) << 11;
+constexpr int MAXK_F32 = 21, MAXK_F64 = 52;
+
+template <typename T> struct Lim;
+template <> struct Lim<float> {
+  static constexpr uint64_t COUNT = MAX_COUNT_F32;
+  static constexpr int MAXK = MAXK_F32;
+};
+template <> struct Lim<double> {
+  static constexpr uint64_t COUNT = MAX_COUNT_F64;
+  static constexpr int MAXK = MAXK_F64;
+};
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (!cached[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = v > 0 ? v : 152;
+  }
+  return cached[dev];
+}
+
+// ------------------------------------------------------------ environment
+std::mutex g_env_mu;
+int g_env_state[64] = {0};   // 0 unknown, 1 ok, 2 failed
+
+repro_status validate_env(cudaStream_t stream) {
+  const char* force = std::getenv("REPRO_FORCE_ENV_FAIL");
+  if (force && force[0] == '1') return REPRO_ERR_ENV;
+  int dev = 0;
+  CK(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return REPRO_ERR_ENV;
+  {
+    std::lock_guard<std::mutex> g(g_env_mu);
+    if (g_env_state[dev] == 1) return REPRO_OK;
+    if (g_env_state[dev] == 2) return REPRO_ERR_ENV;
+  }
+  unsigned* d = nullptr;
+  CK(cudaMallocAsync((void**)&d, sizeof(unsigned), stream));
+  unsigned h = 0xFFFFFFFFu;
+  cudaError_t e = launch_env_probe(d, stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(&h, d, sizeof(unsigned), cudaMemcpyDeviceToHost, stream);
+  cudaError_t e2 = cudaFreeAsync(d, stream);
+  if (e == cudaSuccess) e = e2;
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  std::lock_guard<std::mutex> g(g_env_mu);
+  g_env_state[dev] = (h == 0) ? 1 : 2;
+  return h == 0 ? REPRO_OK : REPRO_ERR_ENV;
+}
+
+// ------------------------------------------------------------- pointers
+bool is_host_only(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return true;
+  }
+  return a.type == cudaMemoryTypeUnregistered;
+}
+
+template <typename T> bool aligned(const T* p) { return ((uintptr_t)p % sizeof(T)) == 0; }
+
+struct Scratch {
+  void* p = nullptr;
+  cudaStream_t s = nullptr;
+  ~Scratch() {
+    if (p) cudaFreeAsync(p, s);
+  }
+};
+
+template <typename T>
+repro_status check_sum_args(const T* x, size_t n, int K) {
+  if (K < 2 || K > Lim<T>::MAXK) return REPRO_ERR_INVALID_ARG;
+  if ((uint64_t)n > Lim<T>::COUNT) return REPRO_ERR_CAPACITY;
+  if (n > 0 && (x == nullptr || !aligned(x))) return REPRO_ERR_INVALID_ARG;
+  return REPRO_OK;
+}
+
+bool launch_ok(const repro_launch* l) {
+  if (!l) return true;
+  if (l->block != 0 && (l->block < 32 || l->block > 1024 || (l->block % 32) != 0)) return false;
+  if (l->grid < 0) return false;
+  return true;
+}
+
+// Grid for the binned sum: enough blocks to fill the GPU, no more than the
+// work needs, and few enough elements per thread that int64 lanes cannot
+// overflow (<= 2^23 deposits per thread).
+int sum_grid(int64_t n, int block, int elems_per_iter, const repro_launch* l) {
+  if (l && l->grid > 0) {
+    int64_t g = l->grid;
+    int64_t need = (n + ((int64_t)block << 23) - 1) / ((int64_t)block << 23);
+    return (int)(g > need ? g : need);
+  }
+  int64_t work = (n + (int64_t)block * elems_per_iter - 1) / ((int64_t)block * elems_per_iter);
+  int64_t cap = (int64_t)sm_count() * (2048 / block);
+  int64_t g = work < cap ? work : cap;
+  if (g < 1) g = 1;
+  return (int)g;
+}
+
+template <typename T>
+repro_status sum_async_impl(const T* x, size_t n, int K, cudaStream_t stream, T* result_dev,
+                            const repro_launch* l) {
+  repro_status st = check_sum_args(x, n, K);
+  if (st != REPRO_OK) return st;
+  if (!result_dev || !aligned(result_dev) || !launch_ok(l)) return REPRO_ERR_INVALID_ARG;
+  st = validate_env(stream);
+  if (st != REPRO_OK) return st;
+  int block = (l && l->block) ? l->block : 256;
+  int grid = sum_grid((int64_t)n, block, 16 * (int)(16 / sizeof(T)) / 4, l);
+  size_t wsb = sum_workspace_bytes(K, grid);
+  Scratch ws;
+  ws.s = stream;
+  CK(cudaMallocAsync(&ws.p, wsb, stream));
+  CK(cudaMemsetAsync(ws.p, 0, 256, stream));
+  CK(launch_sum<T>(x, (int64_t)n, K, (unsigned char*)ws.p, result_dev, grid, block, stream));
+  return REPRO_OK;
+}
+
+template <typename T>
+repro_status sum_sync_impl(const T* x, size_t n, int K, cudaStream_t stream, T* result) {
+  repro_status st = check_sum_args(x, n, K);
+  if (st != REPRO_OK) return st;
+  if (!result) return REPRO_ERR_INVALID_ARG;
+  if (n == 0) {
+    *result = (T)0;
+    return REPRO_OK;
+  }
+  st = validate_env(stream);
+  if (st != REPRO_OK) return st;
+  // plain host memory is copied to the device first
+  Scratch in;
+  in.s = stream;
+  const T* xd = x;
+  if (is_host_only(x)) {
+    CK(cudaMallocAsync(&in.p, n * sizeof(T), stream));
+    CK(cudaMemcpyAsync(in.p, x, n * sizeof(T), cudaMemcpyHostToDevice, stream));
+    xd = (const T*)in.p;
+  }
+  Scratch r;
+  r.s = stream;
+  CK(cudaMallocAsync(&r.p, 16, stream));
+  st = sum_async_impl<T>(xd, n, K, stream, (T*)r.p, nullptr);
+  if (st != REPRO_OK) return st;
+  T h;
+  CK(cudaMemcpyAsync(&h, r.p, sizeof(T), cudaMemcpyDeviceToHost, stream));
+  CK(cudaStreamSynchronize(stream));
+  *result = h;
+  return REPRO_OK;
+}
+
+template <typename T>
+repro_status cumsum_impl(const T* in, T* out, size_t n, int K, cudaStream_t stream, const repro_launch* l) {
+  if (K < 2 || K > Lim<T>::MAXK) return REPRO_ERR_INVALID_ARG;
+  if ((uint64_t)n > Lim<T>::COUNT) return REPRO_ERR_CAPACITY;
+  if (n == 0) return REPRO_OK;
+  if (!in || !out || !aligned(in) || !aligned(out) || !launch_ok(l)) return REPRO_ERR_INVALID_ARG;
+  uintptr_t a0 = (uintptr_t)in, a1 = a0 + n * sizeof(T), b0 = (uintptr_t)out, b1 = b0 + n * sizeof(T);
+  if (in != out && a0 < b1 && b0 < a1) return REPRO_ERR_OVERLAP;
+  repro_status st = validate_env(stream);
+  if (st != REPRO_OK) return st;
+  Scratch ws;
+  ws.s = stream;
+  CK(cudaMallocAsync(&ws.p, cumsum_workspace_bytes<T>((int64_t)n, K), stream));
+  CK(launch_cumsum<T>(in, out, (int64_t)n, K, (unsigned char*)ws.p, l ? l->block : 0, stream));
+  return REPRO_OK;
+}
+
+repro_status var_impl(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out, float* mean,
+                      int twoterm, cudaStream_t stream) {
+  if (axis != 0 && axis != 1) return REPRO_ERR_INVALID_ARG;
+  if (rows <= 0 || cols <= 0) return REPRO_ERR_INVALID_ARG;
+  int64_t n = axis == 1 ? cols : rows;
+  if (ddof < 0 || ddof >= n) return REPRO_ERR_INVALID_ARG;
+  if (n > (1ll << 24)) return REPRO_ERR_INVALID_ARG;   // n must be exact in float32
+  if (!x || !out || !aligned(x) || !aligned(out) || (mean && !aligned(mean))) return REPRO_ERR_INVALID_ARG;
+  CK(launch_var(x, rows, cols, axis, ddof, out, mean, twoterm, nullptr, stream));
+  return REPRO_OK;
+}
+
+template <typename T>
+repro_status compare_impl(const T* x, size_t n, int mode, T* result, cudaStream_t stream) {
+  if ((n > 0 && (!x || !aligned(x))) || !result || !aligned(result)) return REPRO_ERR_INVALID_ARG;
+  if (n > (1ull << 40)) return REPRO_ERR_CAPACITY;
+  Scratch ws;
+  ws.s = stream;
+  CK(cudaMallocAsync(&ws.p, compare_workspace_bytes<T>((int64_t)n, mode), stream));
+  if (mode == 0) CK(cudaMemsetAsync(ws.p, 0, 256, stream));
+  CK(launch_compare<T>(x, (int64_t)n, mode, result, (unsigned char*)ws.p, stream));
+  return REPRO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* repro_strerror(repro_status s) {
+  switch (s) {
+    case REPRO_OK: return "ok";
+    case REPRO_ERR_INVALID_ARG: return "invalid argument";
+    case REPRO_ERR_CAPACITY: return "input count exceeds the reproducible capacity";
+    case REPRO_ERR_OVERLAP: return "input and output overlap (only exact in-place is allowed)";
+    case REPRO_ERR_ENV: return "device floating-point environment failed validation";
+    case REPRO_ERR_CUDA: return "CUDA runtime error";
+    case REPRO_ERR_DEVICE_TIMEOUT: return "device-side wait exceeded its bound";
+  }
+  return "unknown status";
+}
+
+int repro_last_cuda_error(void) { return g_last_cuda; }
+
+uint64_t repro_max_count_f32(void) { return MAX_COUNT_F32; }
+uint64_t repro_max_count_f64(void) { return MAX_COUNT_F64; }
+int repro_max_k_f32(void) { return MAXK_F32; }
+int repro_max_k_f64(void) { return MAXK_F64; }
+
+repro_status repro_validate_environment(cudaStream_t stream) { return validate_env(stream); }
+
+repro_status repro_sum_f32(const float* x, size_t n, int K, cudaStream_t s, float* r) {
+  return sum_sync_impl<float>(x, n, K, s, r);
+}
+repro_status repro_sum_f64(const double* x, size_t n, int K, cudaStream_t s, double* r) {
+  return sum_sync_impl<double>(x, n, K, s, r);
+}
+repro_status repro_sum_f32_async(const float* x, size_t n, int K, cudaStream_t s, float* r,
+                                 const repro_launch* l) {
+  return sum_async_impl<float>(x, n, K, s, r, l);
+}
+repro_status repro_sum_f64_async(const double* x, size_t n, int K, cudaStream_t s, double* r,
+                                 const repro_launch* l) {
+  return sum_async_impl<double>(x, n, K, s, r, l);
+}
+
+repro_status repro_cumsum_f32(const float* in, float* out, size_t n, int K, cudaStream_t s) {
+  return cumsum_impl<float>(in, out, n, K, s, nullptr);
+}
+repro_status repro_cumsum_f64(const double* in, double* out, size_t n, int K, cudaStream_t s) {
+  return cumsum_impl<double>(in, out, n, K, s, nullptr);
+}
+repro_status repro_cumsum_f32_ex(const float* in, float* out, size_t n, int K, cudaStream_t s,
+                                 const repro_launch* l) {
+  return cumsum_impl<float>(in, out, n, K, s, l);
+}
+repro_status repro_cumsum_f64_ex(const double* in, double* out, size_t n, int K, cudaStream_t s,
+                                 const repro_launch* l) {
+  return cumsum_impl<double>(in, out, n, K, s, l);
+}
+
+repro_status repro_segsum_f32(const float* x, int64_t rows, int64_t cols, int axis, int K, float* out,
+                              cudaStream_t s) {
+  if (axis != 0 && axis != 1) return REPRO_ERR_INVALID_ARG;
+  if (K < 2 || K > MAXK_F32 || rows <= 0 || cols <= 0) return REPRO_ERR_INVALID_ARG;
+  if ((uint64_t)(axis == 1 ? cols : rows) > MAX_COUNT_F32) return REPRO_ERR_CAPACITY;
+  if (!x || !out || !aligned(x) || !aligned(out)) return REPRO_ERR_INVALID_ARG;
+  repro_status st = validate_env(s);
+  if (st != REPRO_OK) return st;
+  int64_t grid = rows < 65535 * 16 ? rows : 65535 * 16;
+  CK(launch_segsum(x, rows, cols, axis, K, out, (int)grid, 256, s));
+  return REPRO_OK;
+}
+
+repro_status stable_var_f32(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out,
+                            float* mean_out, cudaStream_t s) {
+  return var_impl(x, rows, cols, axis, ddof, out, mean_out, 0, s);
+}
+repro_status twoterm_var_f32(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out,
+                             cudaStream_t s) {
+  return var_impl(x, rows, cols, axis, ddof, out, nullptr, 1, s);
+}
+
+repro_status repro_sum_naive_f32(const float* x, size_t n, float* r, cudaStream_t s) {
+  return compare_impl<float>(x, n, 0, r, s);
+}
+repro_status repro_sum_naive_f64(const double* x, size_t n, double* r, cudaStream_t s) {
+  return compare_impl<double>(x, n, 0, r, s);
+}
+repro_status repro_sum_pairwise_f32(const float* x, size_t n, float* r, cudaStream_t s) {
+  return compare_impl<float>(x, n, 1, r, s);
+}
+repro_status repro_sum_pairwise_f64(const double* x, size_t n, double* r, cudaStream_t s) {
+  return compare_impl<double>(x, n, 1, r, s);
+}
+repro_status repro_sum_kahan_f32(const float* x, size_t n, float* r, cudaStream_t s) {
+  return compare_impl<float>(x, n, 2, r, s);
+}
+repro_status repro_sum_kahan_f64(const double* x, size_t n, double* r, cudaStream_t s) {
+  return compare_impl<double>(x, n, 2, r, s);
+}
+repro_status repro_sum_neumaier_f32(const float* x, size_t n, float* r, cudaStream_t s) {
+  return compare_impl<float>(x, n, 3, r, s);
+}
+repro_status repro_sum_neumaier_f64(const double* x, size_t n, double* r, cudaStream_t s) {
+  return compare_impl<double>(x, n, 3, r, s);
+}
+int repro_compensated_chunk(void) { return COMPENSATED_CHUNK; }
+
+}  // extern "C"

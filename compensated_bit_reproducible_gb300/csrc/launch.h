@@ -1,0 +1,38 @@
+// Internal launchers (host side), called by the C-ABI layer.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace repro {
+
+// binned sum
+template <typename T>
+cudaError_t launch_sum(const T* x, int64_t n, int K, unsigned char* ws, T* result, int grid, int block,
+                       cudaStream_t s);
+size_t sum_workspace_bytes(int K, int grid);
+cudaError_t launch_segsum(const float* x, int64_t rows, int64_t cols, int axis, int K, float* out, int grid,
+                          int block, cudaStream_t s);
+
+// binned cumulative sum
+template <typename T>
+size_t cumsum_workspace_bytes(int64_t n, int K);
+template <typename T>
+cudaError_t launch_cumsum(const T* in, T* out, int64_t n, int K, unsigned char* ws, int block, cudaStream_t s);
+
+// variance
+cudaError_t launch_var(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out, float* mean,
+                       int twoterm, unsigned char* ws, cudaStream_t s);
+size_t var_workspace_bytes(int64_t rows, int64_t cols, int axis);
+
+// comparison sums: mode 0 naive, 1 pairwise, 2 kahan, 3 neumaier
+template <typename T>
+cudaError_t launch_compare(const T* x, int64_t n, int mode, T* result, unsigned char* ws, cudaStream_t s);
+template <typename T>
+size_t compare_workspace_bytes(int64_t n, int mode);
+constexpr int COMPENSATED_CHUNK = 4096;
+
+// environment probe: writes check bits to *out (device), 0 = all passed
+cudaError_t launch_env_probe(unsigned* out, cudaStream_t s);
+
+}  // namespace repro

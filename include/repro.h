@@ -1,0 +1,162 @@
+/*
+ * repro: order-independent floating-point summation on one NVIDIA GB300.
+ *
+ * C ABI of librepro_gb300.so.  Every call takes plain pointers and sizes and a
+ * CUDA stream; no C++ or framework types cross this boundary.
+ *
+ * Conventions shared by all calls
+ *  - Pointers: inputs and outputs are caller-owned device pointers (also
+ *    managed memory, or host memory as stated per call); the library never
+ *    frees them.  Floating-point pointers must be aligned to their element
+ *    size.  Temporary device memory is taken from the stream-ordered
+ *    allocator (cudaMallocAsync on `stream`) and returned before the call's
+ *    work completes on that stream.
+ *  - Streams: work is enqueued on `stream` (0 = legacy default stream).
+ *    Calls documented "synchronous" wait for their own work; the others
+ *    return once the work is enqueued.
+ *  - Errors: a non-zero repro_status.  Argument and capacity checks happen
+ *    before any pointer is touched or any memory allocated; an error leaves
+ *    outputs unwritten.  repro_strerror() gives a static message.
+ *  - Reproducibility: for the binned (ADN) calls the result bits depend only
+ *    on the input values (for sums: on the multiset; for cumulative sums: on
+ *    the sequence), never on launch configuration, scheduling or stream.
+ *
+ * Sources: "SyclReproSum" README (sections "How It Works", "API Reference",
+ * "Accumulator capacity", "Template Parameters", "Runtime environment
+ * validation"); "Variance in float32 with a first-element shift, a local
+ * centring and a compensated tree sum" (section 2); "Reduction order and
+ * compensation solve related but different problems" and "Kahan's Summation
+ * Formula" (comparison sums).
+ */
+#ifndef REPRO_GB300_H
+#define REPRO_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* cudaStream_t;
+
+typedef enum {
+  REPRO_OK = 0,
+  REPRO_ERR_INVALID_ARG = 1,      /* null pointer with n > 0, K out of range, bad axis/ddof/shape, misaligned */
+  REPRO_ERR_CAPACITY = 2,         /* n above the reproducible capacity */
+  REPRO_ERR_OVERLAP = 3,          /* cumulative sum with partially overlapping input/output */
+  REPRO_ERR_ENV = 4,              /* device floating-point environment failed validation */
+  REPRO_ERR_CUDA = 5,             /* a CUDA runtime call failed (see repro_last_cuda_error) */
+  REPRO_ERR_DEVICE_TIMEOUT = 6    /* a device-side wait exceeded its bound */
+} repro_status;
+
+/* Optional launch shape for the *_ex calls (0 fields = library default).
+   Only the speed changes with it, never the result bits. */
+typedef struct {
+  int block;   /* threads per block: a multiple of 32 in [32, 1024] */
+  int grid;    /* blocks; 0 = sized from n and the SM count */
+} repro_launch;
+
+/* Static description of a status code. */
+const char* repro_strerror(repro_status s);
+/* Last CUDA error code seen by this host thread (cudaError_t value). */
+int repro_last_cuda_error(void);
+
+/* ---- constants ("Accumulator capacity", "Template Parameters") ---------- */
+/* Largest n for which results are reproducible: 4,294,966,784 (float) and
+   9,223,372,036,854,773,760 (double). */
+uint64_t repro_max_count_f32(void);
+uint64_t repro_max_count_f64(void);
+/* Largest fold count K: 21 (float), 52 (double); the smallest is 2. */
+int repro_max_k_f32(void);
+int repro_max_k_f64(void);
+
+/* ---- environment ("Runtime environment validation") --------------------- */
+/* Runs a probe kernel on the current device checking IEEE binary32/64
+   layouts, round-to-nearest-even, unflushed subnormals, signed zero and
+   Inf/NaN arithmetic.  The result is cached per device; every sum and
+   cumulative sum calls it on first use.  Synchronous.  REPRO_ERR_ENV when a
+   check fails. */
+repro_status repro_validate_environment(cudaStream_t stream);
+
+/* ---- binned sums ("How It Works": deposit, renormalize, merge) ---------- */
+/* Reproducible sum of x[0..n) with K folds (2 <= K <= max K).  x may be a
+   device, managed, pinned-host or plain host pointer (host data is copied to
+   the device first).  Synchronous; *result is a host pointer.  n == 0 gives
+   +0.0.  Any NaN, or both +Inf and -Inf, gives the canonical quiet NaN
+   (0x7fc00000 / 0x7ff8000000000000); otherwise an Inf propagates; an exact
+   zero is +0.0.  Result = correct rounding of the exact binned value. */
+repro_status repro_sum_f32(const float* x, size_t n, int K, cudaStream_t stream, float* result);
+repro_status repro_sum_f64(const double* x, size_t n, int K, cudaStream_t stream, double* result);
+/* Same sum, stream-ordered: x is device-accessible, *result_dev is a device
+   pointer written when the work completes; nothing waits on the host. */
+repro_status repro_sum_f32_async(const float* x, size_t n, int K, cudaStream_t stream, float* result_dev,
+                                 const repro_launch* launch);
+repro_status repro_sum_f64_async(const double* x, size_t n, int K, cudaStream_t stream, double* result_dev,
+                                 const repro_launch* launch);
+
+/* ---- binned cumulative sums ("How It Works", cumsum paragraph; "API
+   Reference": cumsum) ------------------------------------------------------ */
+/* out[i] = reproducible sum of in[0..i] (each prefix with its own bin
+   index, so out[n-1] equals repro_sum of the whole input).  in == out (exact
+   in place) is allowed; any other overlap gives REPRO_ERR_OVERLAP.  Device or
+   managed pointers; stream-ordered (returns once enqueued). */
+repro_status repro_cumsum_f32(const float* in, float* out, size_t n, int K, cudaStream_t stream);
+repro_status repro_cumsum_f64(const double* in, double* out, size_t n, int K, cudaStream_t stream);
+repro_status repro_cumsum_f32_ex(const float* in, float* out, size_t n, int K, cudaStream_t stream,
+                                 const repro_launch* launch);
+repro_status repro_cumsum_f64_ex(const double* in, double* out, size_t n, int K, cudaStream_t stream,
+                                 const repro_launch* launch);
+
+/* ---- segmented binned sums --------------------------------------------- */
+/* One reproducible sum per slice of a row-major [rows, cols] float array:
+   axis 1 sums each row (out has rows entries), axis 0 each column (cols
+   entries).  Device pointers; stream-ordered. */
+repro_status repro_segsum_f32(const float* x, int64_t rows, int64_t cols, int axis, int K, float* out,
+                              cudaStream_t stream);
+
+/* ---- float32 variance (variance note, section 2) ------------------------ */
+/* Per-slice variance of a row-major [rows, cols] float array along `axis`
+   (1: each row, 0: each column), entirely in float32:
+     y = x - x[0];  m = sum(y) / n;  d = y - m;
+     s2 = compensated TwoSum tree over d*d (errors carried up a second array,
+          result = final sum + final carry);  s1 = tree sum of d;
+     var = max(s2/n - (s1/n)^2, 0) * n / (n - ddof);  mean = x[0] + m.
+   Trees pair adjacent nodes (2i, 2i+1) level by level; an unpaired last node
+   passes up unchanged.  0 <= ddof < n.  out gets one variance per slice;
+   mean_out (nullable) the means.  Device pointers; stream-ordered. */
+repro_status stable_var_f32(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out,
+                            float* mean_out, cudaStream_t stream);
+
+/* ---- comparison modes (reductions page; Kahan's Summation Formula) ------ */
+/* Formula of reference for the variance (tf.nn.moments, variance note
+   section 1): m = mean(x); d = x - m; var = max(mean(d^2) - mean(d)^2, 0),
+   mean(v) = RN(tree_sum(v) * RN(1/n)), same ddof rescale.  Stream-ordered. */
+repro_status twoterm_var_f32(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out,
+                             cudaStream_t stream);
+/* Non-reproducible comparison sums, result to a device pointer,
+   stream-ordered:
+   naive     - plain parallel float/double reduction (order depends on the
+               launch shape: the usual non-reproducible baseline);
+   pairwise  - the adjacent-pair tree over x[0..n) (deterministic for a given
+               n);
+   kahan     - Kahan's loop (y = x - c; t = s + y; c = (t - s) - y; s = t) over
+               consecutive 4096-element chunks, chunk sums combined by the
+               pairwise tree;
+   neumaier  - Neumaier's loop over the same chunks (result s + c per chunk),
+               combined by the pairwise tree. */
+repro_status repro_sum_naive_f32(const float* x, size_t n, float* result_dev, cudaStream_t stream);
+repro_status repro_sum_naive_f64(const double* x, size_t n, double* result_dev, cudaStream_t stream);
+repro_status repro_sum_pairwise_f32(const float* x, size_t n, float* result_dev, cudaStream_t stream);
+repro_status repro_sum_pairwise_f64(const double* x, size_t n, double* result_dev, cudaStream_t stream);
+repro_status repro_sum_kahan_f32(const float* x, size_t n, float* result_dev, cudaStream_t stream);
+repro_status repro_sum_kahan_f64(const double* x, size_t n, double* result_dev, cudaStream_t stream);
+repro_status repro_sum_neumaier_f32(const float* x, size_t n, float* result_dev, cudaStream_t stream);
+repro_status repro_sum_neumaier_f64(const double* x, size_t n, double* result_dev, cudaStream_t stream);
+/* Chunk length used by the chunked Kahan / Neumaier comparison sums. */
+int repro_compensated_chunk(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* REPRO_GB300_H */

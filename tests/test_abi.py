@@ -1,0 +1,82 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad
+arguments before touching pointers or the GPU (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "repro.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from compensated_bit_reproducible_gb300 import build, api
+    build.build()
+    return api.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    expected = {"repro_strerror", "repro_last_cuda_error", "repro_validate_environment",
+                "repro_compensated_chunk", "stable_var_f32", "twoterm_var_f32", "repro_segsum_f32"}
+    for t in ("f32", "f64"):
+        expected |= {"repro_max_count_" + t, "repro_max_k_" + t, "repro_sum_" + t, "repro_sum_%s_async" % t,
+                     "repro_cumsum_" + t, "repro_cumsum_%s_ex" % t}
+        expected |= {"repro_sum_%s_%s" % (m, t) for m in ("naive", "pairwise", "kahan", "neumaier")}
+    assert expected <= set(names), expected - set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_constants_match_the_pages(L):
+    assert L.repro_max_count_f32() == 4294966784
+    assert L.repro_max_count_f64() == 9223372036854773760
+    assert L.repro_max_k_f32() == 21 and L.repro_max_k_f64() == 52
+    assert L.repro_compensated_chunk() == 4096
+
+
+def test_argument_errors_before_pointer_access(L):
+    P = ctypes.c_void_p
+    out = ctypes.c_float()
+    outd = ctypes.c_double()
+    bogus = P(0x10)   # never dereferenced: every case below fails its checks first
+    # K out of range
+    for K in (1, 22, 0, -3):
+        assert L.repro_sum_f32(bogus, 10, K, None, ctypes.byref(out)) == 1
+    assert L.repro_sum_f64(bogus, 10, 53, None, ctypes.byref(outd)) == 1
+    # capacity, with a null pointer: the length check comes first
+    assert L.repro_sum_f32(None, 4294966785, 3, None, ctypes.byref(out)) == 2
+    assert L.repro_sum_f64(None, 9223372036854773761, 3, None, ctypes.byref(outd)) == 2
+    assert L.repro_cumsum_f32(None, None, 4294966785, 3, None) == 2
+    # null input with n > 0
+    assert L.repro_sum_f32(None, 5, 3, None, ctypes.byref(out)) == 1
+    # misaligned pointers
+    assert L.repro_sum_f32(P(0x1002), 5, 3, None, ctypes.byref(out)) == 1
+    assert L.repro_sum_f64(P(0x1004), 5, 3, None, ctypes.byref(outd)) == 1
+    # overlapping (but not identical) cumsum ranges
+    assert L.repro_cumsum_f32(P(0x100000), P(0x100004), 16, 3, None) == 3
+    assert L.repro_cumsum_f64(P(0x100000), P(0x100040), 16, 3, None) == 3
+    # n == 0 is a no-op / +0.0 without touching anything
+    assert L.repro_cumsum_f32(None, None, 0, 3, None) == 0
+    out.value = 7.0
+    assert L.repro_sum_f32(None, 0, 3, None, ctypes.byref(out)) == 0 and out.value == 0.0
+    # variance shape / ddof / axis checks
+    assert L.stable_var_f32(bogus, 4, 4, 2, 0, bogus, None, None) == 1
+    assert L.stable_var_f32(bogus, 4, 4, 1, 4, bogus, None, None) == 1
+    assert L.stable_var_f32(bogus, 4, 4, 1, -1, bogus, None, None) == 1
+    assert L.stable_var_f32(bogus, 0, 4, 1, 0, bogus, None, None) == 1
+    assert L.repro_segsum_f32(bogus, 4, 4, 1, 22, bogus, None) == 1
+
+
+def test_strerror(L):
+    for s in range(7):
+        assert L.repro_strerror(s)
