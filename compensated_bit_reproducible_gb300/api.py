@@ -54,6 +54,7 @@ def lib():
             "repro_sum_f64": (I, [P, S, I, P, P]),
             "repro_sum_f32_async": (I, [P, S, I, P, P, P]),
             "repro_sum_f64_async": (I, [P, S, I, P, P, P]),
+            "repro_sum_f32_noalloc": (I, [P, S, I, P, P]),
             "repro_cumsum_f32": (I, [P, P, S, I, P]),
             "repro_cumsum_f64": (I, [P, P, S, I, P]),
             "repro_cumsum_f32_ex": (I, [P, P, S, I, P, P]),
@@ -133,6 +134,16 @@ def repro_sum_async(x: torch.Tensor, out: torch.Tensor, K: int = 3, block: int =
     assert x.is_cuda and out.is_cuda and out.dtype == x.dtype and x.is_contiguous()
     _check(getattr(lib(), "repro_sum_%s_async" % sfx)(_ptr(x), x.numel(), K, _stream(stream), _ptr(out),
                                                       _launch(block, grid)), "repro_sum_%s_async" % sfx)
+    return out
+
+
+def repro_sum_noalloc(x: torch.Tensor, out: torch.Tensor, K: int = 3, stream=None) -> torch.Tensor:
+    """Binned float sum whose workspace is a fixed device array inside the
+    library: for callers that cannot allocate device memory (see
+    include/repro.h).  Calls on one device must not overlap on the GPU."""
+    assert x.is_cuda and out.is_cuda and x.dtype == torch.float32 and out.dtype == torch.float32
+    assert x.is_contiguous()
+    _check(lib().repro_sum_f32_noalloc(_ptr(x), x.numel(), K, _stream(stream), _ptr(out)), "repro_sum_f32_noalloc")
     return out
 
 

@@ -95,6 +95,21 @@ repro_status repro_sum_f32_async(const float* x, size_t n, int K, cudaStream_t s
 repro_status repro_sum_f64_async(const double* x, size_t n, int K, cudaStream_t stream, double* result_dev,
                                  const repro_launch* launch);
 
+/* Same binned float sum for callers that cannot allocate device memory (the
+   pages have no counterpart to this call).  Some callers cannot call
+   cudaMalloc: another allocator already holds the GPU's memory, or the call
+   sits where an allocation could synchronize the device or fail.  The
+   workspace is one file-scope device array of 256 KiB inside the library,
+   held by every GPU that loads it until the process exits; nothing is
+   allocated per call.  x is device-accessible, *result_dev a device pointer;
+   stream-ordered.  Limits: K in 2..21, n up to the float capacity
+   (4,294,966,784), else REPRO_ERR_INVALID_ARG / REPRO_ERR_CAPACITY.  All calls
+   share the array (each clears what must start at zero): calls whose work
+   overlaps on the GPU race, so order them on one stream or with events.  The
+   first call on a device sets up (device address of the array, environment
+   probe) and waits for it; make it before any stream capture. */
+repro_status repro_sum_f32_noalloc(const float* x, size_t n, int K, cudaStream_t stream, float* result_dev);
+
 /* ---- binned cumulative sums ("How It Works", cumsum paragraph; "API
    Reference": cumsum) ------------------------------------------------------ */
 /* out[i] = reproducible sum of in[0..i] (each prefix with its own bin
