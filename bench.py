@@ -74,7 +74,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -150,8 +150,10 @@ def run_ours(args):
     launches_per_row = {"var_f32_4096x4096": 1, "sum_f32_1e8": 1, "segsum_f32_4096x4096": 1,
                         "cumsum_f32_1e8": 3, "sum_f64_1e8": 1, "cumsum_f64_1e8": 3}
 
+    active = [r for r in ROWS_SPEC if not args.rows or r[0] in args.rows.split(",")]
+
     def step(evs=None):
-        for name, _, _ in ROWS_SPEC:
+        for name, _, _ in active:
             if evs is not None:
                 evs[name][0].append(torch.cuda.Event(enable_timing=True))
                 evs[name][0][-1].record(stream)
@@ -166,7 +168,7 @@ def run_ours(args):
     barrier(ws)
     clocks = ClockSampler(local)
     clocks.start()
-    evs = {name: ([], []) for name, _, _ in ROWS_SPEC}
+    evs = {name: ([], []) for name, _, _ in active}
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -180,30 +182,31 @@ def run_ours(args):
     ms_total = t0.elapsed_time(t1)
     ms_total = max_over_ranks(ms_total, ws)
     ms_step = ms_total / args.steps
-    elems_step = sum(n for _, n, _ in ROWS_SPEC)
+    elems_step = sum(n for _, n, _ in active)
     value = elems_step * ws / (ms_step * 1e-3) / 1e9
     hbm, peak_kind = load_peaks()
     rows = {}
-    for name, n, bpe in ROWS_SPEC:
+    for name, n, bpe in active:
         durs = [a.elapsed_time(b) for a, b in zip(*evs[name])]
         ms = sum(durs) / len(durs)
         rows[name] = {"ms": round(ms, 4), "gelem_s": round(n / (ms * 1e-3) / 1e9, 2),
                       "gb_s": round(n * bpe / (ms * 1e-3) / 1e9, 1),
                       "hbm_frac": round(n * bpe / (ms * 1e-3) / 1e9 / hbm, 4)}
     dom = max(rows, key=lambda k: rows[k]["ms"])
-    dom_n, dom_bpe = [(n, b) for nm, n, b in ROWS_SPEC if nm == dom][0]
+    dom_n, dom_bpe = [(n, b) for nm, n, b in active if nm == dom][0]
     achieved = dom_n * dom_bpe / (rows[dom]["ms"] * 1e-3) / 1e9
     traffic = load_traffic(dom)
     # correctness of what was timed: the two 1e8 sums against host checks
     torch.cuda.synchronize()
 
     # end to end through the C ABI: pinned host buffers in, results out
-    e2e = run_e2e(args, api, torch, h32, h64, hA, dev, stream)
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(args.cpu_seconds)
-    comparisons = run_comparisons(api, torch, x32, x64, A, stream)
-    gpu_launches = args.steps * sum(launches_per_row.values())
+    e2e = cpu = comparisons = None
+    if not args.skip_extras:
+        e2e = run_e2e(args, api, torch, h32, h64, hA, dev, stream)
+        if rank == 0 and not args.no_cpu_baseline:
+            cpu = cpu_baseline(args.cpu_seconds)
+        comparisons = run_comparisons(api, torch, x32, x64, A, stream)
+    gpu_launches = args.steps * sum(launches_per_row[name] for name, _, _ in active)
     line = {
         "metric": METRIC,
         "value": round(value, 3),
@@ -433,12 +436,15 @@ def init_dist(ws):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", default="", help="comma list of rows to run (profiling); default: all")
+    ap.add_argument("--skip-extras", action="store_true",
+                    help="skip the end-to-end, CPU-baseline and comparison legs (profiling)")
     args = ap.parse_args(argv)
     ws, _, _ = dist_env()
     if args.impl == "reference":

@@ -135,7 +135,7 @@ struct AccF : Lanes<float, KT> {
 
   // A chunk where some value may lie above the current bins or be Inf/NaN.
   template <int U>
-  __device__ __noinline__ void slow_chunk(float* v) {
+  __device__ __forceinline__ void slow_chunk(float* v) {
     int jmin = this->I;
 #pragma unroll
     for (int i = 0; i < U; ++i) {
@@ -186,19 +186,33 @@ struct AccD : Lanes<double, KT> {
   typedef Lanes<double, KT> B;
   static constexpr int N = B::N;
   uint64_t thr;
+  FastD<KT ? KT : 1> fc;
 
   __device__ __forceinline__ void init(int Kr) {
     B::init(Kr);
     thr = index_threshold<double>(this->I);
+    if (KT) fc.set(this->I);
   }
 
   __device__ __forceinline__ void raise(int j) {
     this->raise_lanes(j);
     thr = index_threshold<double>(this->I);
+    if (KT) fc.set(this->I);
+  }
+
+  __device__ __forceinline__ void add_fast(double x) {
+    if constexpr (KT != 0) {
+      int64_t a[KT];
+      fast_digits_f64<KT>(x, fc, a);
+#pragma unroll
+      for (int k = 0; k < KT; ++k) this->L[k] += a[k];
+    } else {
+      this->add_digits(x);
+    }
   }
 
   template <int U>
-  __device__ __noinline__ void slow_chunk(double* v) {
+  __device__ __forceinline__ void slow_chunk(double* v) {
     int jmin = this->I;
 #pragma unroll
     for (int i = 0; i < U; ++i) {
@@ -215,19 +229,19 @@ struct AccD : Lanes<double, KT> {
     }
     if (jmin < this->I) raise(jmin);
 #pragma unroll
-    for (int i = 0; i < U; ++i) this->add_digits(v[i]);
+    for (int i = 0; i < U; ++i) add_fast(v[i]);
   }
 
   template <int U>
   __device__ __forceinline__ void chunk(double* v) {
-    bool out = false;
+    uint32_t m = 0;
 #pragma unroll
-    for (int i = 0; i < U; ++i) out |= abs_bits<double>(v[i]) >= thr;
-    if (out) {
+    for (int i = 0; i < U; ++i) m = max(m, (uint32_t)__double2hiint(v[i]) & 0x7FFFFFFFu);
+    if (m >= (uint32_t)(thr >> 32)) {
       slow_chunk<U>(v);
     } else {
 #pragma unroll
-      for (int i = 0; i < U; ++i) this->add_digits(v[i]);
+      for (int i = 0; i < U; ++i) add_fast(v[i]);
     }
   }
 

@@ -156,6 +156,72 @@ __device__ void chain_digits(T x, int I, int K, int64_t* a) {
   }
 }
 
+// -------------------------------------------------- fast digits (double)
+// Same digits as chain_digits for a double, with a fixed K and index.  With
+// |X| = |x| / 2^(beta_k - 1) written in binary, digit k before tie handling
+// is the signed value of the W bits above the binary point of |x| / 2^beta_k
+// (the bit at beta_k + W - 1 is the sign: it is the rounding bit of fold
+// k - 1) plus the bit just below, beta_k - 1 (round half up).  One shifted
+// copy G of the significand per fold holds both: bits [24, 64) the window,
+// bit 23 the rounding bit.  Round-half-away differs from round-half-up only
+// at an exact tie whose remainder is negative: for |x| that is fold k >= 1
+// when the lowest set bit of |x| is beta_k - 1 and the rounding bit of fold
+// k - 1 is set; then digit k drops by one and digit k + 1 gains 2^W.
+__device__ __forceinline__ uint64_t shl_clamp(uint64_t v, int s) {
+  uint64_t r;
+  asm("shl.b64 %0, %1, %2;" : "=l"(r) : "l"(v), "r"(s));   // s >= 64 (as unsigned) gives 0
+  return r;
+}
+__device__ __forceinline__ uint64_t shr_clamp(uint64_t v, int s) {
+  uint64_t r;
+  asm("shr.b64 %0, %1, %2;" : "=l"(r) : "l"(v), "r"(s));
+  return r;
+}
+
+template <int K>
+struct FastD {
+  int tsh[K];   // shift of the significand for fold k: biased exponent + tsh[k]
+  int tie[K];   // biased exponent + ctz(significand) == tie[k]: tie at fold k
+  __device__ __forceinline__ void set(int I) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      int b = beta<double>(I + k);
+      tsh[k] = 24 - b - 1075;        // e - (beta_k - 1) + 23, e = eb - 1075
+      tie[k] = b - 1 + 1075;
+    }
+  }
+};
+
+// Digits of a finite double x (no Inf/NaN) at the index set in `c`.
+template <int K>
+__device__ __forceinline__ void fast_digits_f64(double x, const FastD<K>& c, int64_t* a) {
+  uint32_t hi = (uint32_t)__double2hiint(x), lo = (uint32_t)__double2loint(x);
+  int eb = (int)((hi >> 20) & 0x7FF);
+  int ee = eb ? eb : 1;
+  uint32_t mh = (hi & 0xFFFFFu) | (eb ? 0x100000u : 0u);
+  uint64_t M = ((uint64_t)mh << 32) | lo;
+  uint64_t G[K];
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    int t = ee + c.tsh[k];
+    G[k] = shl_clamp(M, t) | shr_clamp(M, -t);
+    a[k] = ((int64_t)G[k] >> 24) + (int64_t)((G[k] >> 23) & 1);
+  }
+  // ties with a negative remainder (folds k >= 1)
+  int ctz = lo ? (__ffs((int)lo) - 1) : (32 + __ffs((int)mh) - 1);
+  int lam = ee + ctz;
+#pragma unroll
+  for (int k = 1; k < K; ++k) {
+    bool cfix = (lam == c.tie[k]) && ((int64_t)G[k] < 0);
+    a[k] -= cfix ? 1 : 0;
+    if (k + 1 < K) a[k + 1] += cfix ? ((int64_t)1 << Geom<double>::W) : 0;
+  }
+  if (hi >> 31) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) a[k] = -a[k];
+  }
+}
+
 // ------------------------------------------------------------ 128-bit shuffles
 __device__ __forceinline__ W128 shfl_xor_w(W128 v, int m) {
   uint32_t w0 = (uint32_t)v.lo, w1 = (uint32_t)(v.lo >> 32), w2 = (uint32_t)v.hi, w3 = (uint32_t)((uint64_t)v.hi >> 32);
@@ -321,6 +387,114 @@ __device__ T convert_state(const State<KMAXS>& st, int K) {
     }
   }
   return round_limbs<T>(neg, limb, nl, beta<T>(st.I + K - 1));
+}
+
+// -------------------------------------------- fast conversion (fixed K)
+// Correct rounding of sum_k F_k 2^(beta_{I+k}) with compile-time K, in
+// registers: the folds are added into a little-endian two's-complement
+// integer of NW 32-bit words (bit 0 = the finest grid unit), whose leading
+// 64 bits are then rounded to nearest, ties to even, with a sticky bit.
+template <typename T, int K> struct ConvW {
+  static constexpr int NW = (Geom<T>::W * (K - 1) + 130) / 32 + 1;
+};
+
+// w += v * 2^off (v a sign-extended 128-bit value), static offset.
+template <int NW, int OFF>
+__device__ __forceinline__ void words_add(uint32_t* w, W128 v) {
+  constexpr int li = OFF / 32, sh = OFF % 32;
+  uint32_t ext = (v.hi < 0) ? 0xFFFFFFFFu : 0u;
+  uint32_t s[5] = {(uint32_t)v.lo, (uint32_t)(v.lo >> 32), (uint32_t)v.hi, (uint32_t)((uint64_t)v.hi >> 32), ext};
+  uint32_t carry = 0;
+#pragma unroll
+  for (int i = li; i < NW; ++i) {
+    const int r = i - li;
+    uint32_t a;
+    if (r < 5) a = sh ? ((s[r] << sh) | (r ? (s[r - 1] >> (32 - sh)) : 0u)) : s[r];
+    else a = ext;
+    uint64_t t = (uint64_t)w[i] + a + carry;
+    w[i] = (uint32_t)t;
+    carry = (uint32_t)(t >> 32);
+  }
+}
+
+template <typename T, int K, int k>
+struct FoldAdder {
+  template <int NW>
+  __device__ __forceinline__ static void run(uint32_t* w, const W128* F) {
+    words_add<NW, Geom<T>::W * (K - 1 - k)>(w, F[k]);
+    FoldAdder<T, K, k + 1>::template run<NW>(w, F);
+  }
+};
+template <typename T, int K>
+struct FoldAdder<T, K, K> {
+  template <int NW>
+  __device__ __forceinline__ static void run(uint32_t*, const W128*) {}
+};
+
+template <typename T, int K>
+__device__ __forceinline__ T convert_fast(int I, int flags, const W128* F) {
+  typedef Geom<T> G;
+  constexpr int NW = ConvW<T, K>::NW;
+  if (flags) return from_flags<T>(flags);
+  uint32_t w[NW];
+#pragma unroll
+  for (int i = 0; i < NW; ++i) w[i] = 0;
+  FoldAdder<T, K, 0>::template run<NW>(w, F);
+  bool neg = (w[NW - 1] >> 31) != 0;
+  if (neg) {
+    uint32_t c = 1;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      uint64_t t = (uint64_t)(~w[i]) + c;
+      w[i] = (uint32_t)t;
+      c = (uint32_t)(t >> 32);
+    }
+  }
+  // leading word and the 64 bits from the leading bit down (a, b, c words)
+  int ti = -1;
+#pragma unroll
+  for (int i = 0; i < NW; ++i)
+    if (w[i]) ti = i;
+  if (ti < 0) return (T)0.0;
+  uint32_t a = 0, b = 0, c = 0;
+  bool below = false;   // any set bit in the words under c
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
+    if (i == ti) a = w[i];
+    if (i == ti - 1) b = w[i];
+    if (i == ti - 2) c = w[i];
+    if (i < ti - 2 && w[i]) below = true;
+  }
+  int lz = __clz((int)a);
+  // top 64 bits: a:b:c shifted left by lz
+  uint64_t hi64 = ((uint64_t)a << 32 | b);
+  uint64_t top = lz ? ((hi64 << lz) | ((uint64_t)c >> (32 - lz))) : hi64;
+  bool st0 = lz ? ((c << lz) != 0) : (c != 0);
+  int topbit = 32 * ti + 31 - lz;            // index of the leading bit
+  int lsb = beta<T>(I + K - 1);
+  int E = topbit + lsb;
+  int q = E - G::P + 1;
+  if (q < G::QMIN) q = G::QMIN;
+  int drop = q - (topbit - 63 + lsb);          // low bits of `top` below the quantum (>= 64 - P)
+  uint64_t m;
+  bool half, sticky;
+  if (drop >= 64) {
+    // value below half the smallest quantum cannot occur for a binned value
+    m = 0;
+    half = (drop == 64) ? ((top >> 63) != 0) : false;
+    sticky = st0 || below || (drop == 64 ? ((top << 1) != 0) : (top != 0));
+  } else if (drop > 0) {
+    m = top >> drop;
+    half = ((top >> (drop - 1)) & 1) != 0;
+    sticky = st0 || below || ((drop >= 2) ? ((top << (65 - drop)) != 0) : false);
+  } else {
+    m = top << (-drop);     // every bit kept (few significant bits)
+    half = false;
+    sticky = false;
+  }
+  if (half && (sticky || (m & 1))) m += 1;
+  if (m == (1ull << G::P)) { m >>= 1; q += 1; }
+  return assemble<T>(neg, m, q);
 }
 
 }  // namespace repro

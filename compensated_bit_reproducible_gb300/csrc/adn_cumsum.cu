@@ -131,95 +131,245 @@ __device__ __forceinline__ int load_tile(const T* __restrict__ in, int64_t n, in
   return cnt;
 }
 
-template <typename T, int KT>
-__global__ void __launch_bounds__(CS_BLOCK) cumsum_tile_reduce(const T* __restrict__ in, int64_t n, int K,
-                                                               unsigned char* __restrict__ tstate) {
-  constexpr int N = KArr<T, KT>::N;
-  __shared__ T sm[CS_TILE + CS_TILE / CS_ITEMS];
-  int cnt = load_tile<T>(in, n, blockIdx.x, sm);
-  SState<N> s;
-  sstate_zero(s, Geom<T>::NB - K);
-  int b = threadIdx.x * CS_ITEMS;
-  for (int i = 0; i < CS_ITEMS; ++i)
-    if (b + i < cnt) sstate_deposit<T, N>(s, sm[b + i + b / CS_ITEMS], K);
-  int64_t L[N];
-  // block merge works on int64 lanes; a tile's fold sums fit (4096 * 2^39)
-#pragma unroll(N <= 8 ? N : 1)
-  for (int k = 0; k < N; ++k) L[k] = (int64_t)s.F[k].lo;
-  State<N> st;
-  block_merge<N>(s.I, s.flags, L, K, &st);
-  if (threadIdx.x == 0) store_partial<N>(tstate, blockIdx.x, K, st);
+// ------------------------------------------------------------------
+// Compile-time K (2..8): every state lives in registers.
+//  A. tile totals: the sum kernel's per-thread accumulators and block merge;
+//  B. one block scans the tile totals (per-thread sequential runs, then a
+//     warp-shuffle scan of the run totals);
+//  C. replay: each thread owns ITEMS contiguous elements; the block scan of
+//     the threads' own totals plus the tile prefix gives its incoming state;
+//     each element's digits are added to that running state, which is then
+//     rounded (convert_fast).
+template <int K> struct RS {   // register state: index, flags, 128-bit fold sums
+  int I;
+  int flags;
+  W128 F[K];
+};
+
+template <int K>
+__device__ __forceinline__ void rs_zero(RS<K>& s, int I0) {
+  s.I = I0;
+  s.flags = 0;
+#pragma unroll
+  for (int k = 0; k < K; ++k) s.F[k] = W128{0, 0};
 }
 
-template <int N>
-__device__ __forceinline__ void load_sstate(SState<N>& s, const unsigned char* base, int64_t idx, int K) {
-  const unsigned char* p = base + (size_t)idx * (16 + 16 * (size_t)K);
+template <int K>
+__device__ __forceinline__ void rs_shift(RS<K>& s, int d) {
+  // re-express at index s.I - d (d >= 0): fold k -> k + d
+#pragma unroll
+  for (int k = K - 1; k >= 0; --k) {
+    W128 v = W128{0, 0};
+#pragma unroll
+    for (int j = 0; j < K; ++j)
+      if (j == k - d) v = s.F[j];
+    s.F[k] = v;
+  }
+}
+
+template <int K>
+__device__ __forceinline__ void rs_merge(RS<K>& a, const RS<K>& b) {
+  RS<K> t = b;
+  if (b.I < a.I) { rs_shift(a, a.I - b.I); a.I = b.I; }
+  else if (a.I < b.I) { rs_shift(t, b.I - a.I); }
+#pragma unroll
+  for (int k = 0; k < K; ++k) a.F[k] = w_add(a.F[k], t.F[k]);
+  a.flags |= b.flags;
+}
+
+template <int K>
+__device__ __forceinline__ RS<K> rs_shfl_up(const RS<K>& s, int d) {
+  RS<K> o;
+  o.I = __shfl_up_sync(0xffffffffu, s.I, d);
+  o.flags = __shfl_up_sync(0xffffffffu, s.flags, d);
+#pragma unroll
+  for (int k = 0; k < K; ++k) o.F[k] = shfl_up_w(s.F[k], d);
+  return o;
+}
+
+template <int K>
+__device__ __forceinline__ void rs_load(RS<K>& s, const unsigned char* p) {
   s.I = ((const int*)p)[0];
   s.flags = ((const int*)p)[1];
-#pragma unroll(N <= 8 ? N : 1)
-  for (int k = 0; k < N; ++k) {
-    const int64_t* q = (const int64_t*)(p + 16) + 2 * k;
-    s.F[k] = (k < K) ? W128{(uint64_t)q[0], q[1]} : W128{0, 0};
-  }
+  const int64_t* F = (const int64_t*)(p + 16);
+#pragma unroll
+  for (int k = 0; k < K; ++k) s.F[k] = W128{(uint64_t)F[2 * k], F[2 * k + 1]};
 }
 
-template <int N>
-__device__ __forceinline__ void store_sstate(const SState<N>& s, unsigned char* base, int64_t idx, int K) {
-  unsigned char* p = base + (size_t)idx * (16 + 16 * (size_t)K);
+template <int K>
+__device__ __forceinline__ void rs_store(const RS<K>& s, unsigned char* p) {
   ((int*)p)[0] = s.I;
   ((int*)p)[1] = s.flags;
-  for (int k = 0; k < K; ++k) {
-    int64_t* q = (int64_t*)(p + 16) + 2 * k;
-    q[0] = (int64_t)s.F[k].lo;
-    q[1] = s.F[k].hi;
-  }
+  int64_t* F = (int64_t*)(p + 16);
+#pragma unroll
+  for (int k = 0; k < K; ++k) { F[2 * k] = (int64_t)s.F[k].lo; F[2 * k + 1] = s.F[k].hi; }
 }
 
-// One block: exclusive scan of the tile totals into tile prefixes.
+// Exclusive block scan of register states (identity at index I0).
+template <int K>
+__device__ __forceinline__ RS<K> rs_block_exclusive(const RS<K>& mine, int I0, RS<K>* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  RS<K> inc = mine;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    RS<K> o = rs_shfl_up(inc, d);
+    if (lane >= d) {
+      rs_merge(o, inc);
+      inc = o;
+    }
+  }
+  RS<K> exc = rs_shfl_up(inc, 1);
+  if (lane == 0) rs_zero(exc, I0);
+  if (lane == 31) sm[warp] = inc;
+  __syncthreads();
+  RS<K> base;
+  rs_zero(base, I0);
+  for (int w = 0; w < warp; ++w) rs_merge(base, sm[w]);
+  rs_merge(base, exc);
+  __syncthreads();
+  return base;
+}
+
+// Digits of one finite element at index I (compile-time K).
+template <typename T, int K> struct Digits;
+template <int K> struct Digits<float, K> {
+  float P0[K];
+  uint32_t thr;
+  float thrf;
+  __device__ __forceinline__ void set(int I) {
+    thr = index_threshold<float>(I);
+    thrf = (I == 0) ? 0.0f : __uint_as_float(thr);
+#pragma unroll
+    for (int k = 0; k < K; ++k)
+      P0[k] = (I >= 1) ? __uint_as_float(((uint32_t)(beta<float>(I + k) + 23 + 127) << 23) | 0x400000u) : 1.0f;
+  }
+  __device__ __forceinline__ bool fits(float x) const { return fabsf(x) < thrf; }
+  // exact digits through fresh primaries (the README's sticky-bit deposit)
+  __device__ __forceinline__ void get(float x, int I, int64_t* a) const {
+    float r = x;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      float q = __uint_as_float(__float_as_uint(r) | 1u);
+      float S = __fadd_rn(P0[k], q);
+      a[k] = (int32_t)(__float_as_uint(S) - __float_as_uint(P0[k]));
+      if (k + 1 < K) r = __fadd_rn(r, __fsub_rn(P0[k], S));
+    }
+  }
+};
+template <int K> struct Digits<double, K> {
+  FastD<K> fc;
+  uint32_t thr_hi;
+  __device__ __forceinline__ void set(int I) {
+    fc.set(I);
+    thr_hi = (uint32_t)(index_threshold<double>(I) >> 32);
+  }
+  __device__ __forceinline__ bool fits(double x) const {
+    return ((uint32_t)__double2hiint(x) & 0x7FFFFFFFu) < thr_hi;
+  }
+  __device__ __forceinline__ void get(double x, int I, int64_t* a) const { fast_digits_f64<K>(x, fc, a); }
+};
+
+// Deposit x into a running register state.
+template <typename T, int K>
+__device__ __forceinline__ void rs_deposit(RS<K>& s, Digits<T, K>& dg, T x) {
+  if (!dg.fits(x)) {
+    if (!(abs_bits<T>(x) < (sizeof(T) == 4 ? 0x7F800000ull : 0x7FF0000000000000ull))) {
+      s.flags |= special_flag(x);
+      return;
+    }
+    if (x == (T)0) return;
+    int j = bin_index<T>(x);
+    if (j < s.I) {
+      rs_shift(s, s.I - j);
+      s.I = j;
+      dg.set(j);
+    }
+    if (sizeof(T) == 4 && s.I == 0) {
+      // bin 0: the float primary would overflow; exact integer digits
+      int64_t a[K];
+      chain_digits<T>(x, s.I, K, a);
+#pragma unroll
+      for (int k = 0; k < K; ++k) s.F[k] = w_add(s.F[k], w_from(a[k]));
+      return;
+    }
+  }
+  int64_t a[K];
+  dg.get(x, s.I, a);
+#pragma unroll
+  for (int k = 0; k < K; ++k) s.F[k] = w_add(s.F[k], w_from(a[k]));
+}
+
 template <typename T, int KT>
-__global__ void __launch_bounds__(1024) cumsum_tile_scan(const unsigned char* __restrict__ tstate, int64_t ntiles,
-                                                         int K, unsigned char* __restrict__ tpref) {
-  constexpr int N = KArr<T, KT>::N;
-  __shared__ SState<N> sm[32];
-  const int I0 = Geom<T>::NB - K;
+__global__ void __launch_bounds__(CS_BLOCK) cumsum_fast_reduce(const T* __restrict__ in, int64_t n, int K,
+                                                               unsigned char* __restrict__ tstate) {
+  typedef typename AccOf<T, KT>::type Acc;
+  int64_t base = (int64_t)blockIdx.x * CS_TILE;
+  int64_t cnt = min((int64_t)CS_TILE, n - base);
+  Acc acc;
+  acc.init(K);
+  const T* p = in + base;
+  for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+    T v[1] = {p[i]};
+    acc.template chunk<1>(v);
+  }
+  acc.finish();
+  State<KT> st;
+  block_merge<KT>(acc.I, acc.flags, acc.L, K, &st);
+  if (threadIdx.x == 0) store_partial<KT>(tstate, blockIdx.x, K, st);
+}
+
+template <typename T, int KT>
+__global__ void __launch_bounds__(1024) cumsum_fast_scan(const unsigned char* __restrict__ tstate, int64_t ntiles,
+                                                         unsigned char* __restrict__ tpref) {
+  __shared__ RS<KT> sm[32];
+  const int I0 = Geom<T>::NB - KT;
+  const size_t st = 16 + 16 * (size_t)KT;
   int64_t per = (ntiles + blockDim.x - 1) / blockDim.x;
   int64_t b = (int64_t)threadIdx.x * per, e = min(ntiles, b + per);
-  SState<N> agg, x;
-  sstate_zero(agg, I0);
+  RS<KT> agg, x;
+  rs_zero(agg, I0);
   for (int64_t t = b; t < e; ++t) {
-    load_sstate(x, tstate, t, K);
-    sstate_merge(agg, x, K);
+    rs_load(x, tstate + (size_t)t * st);
+    rs_merge(agg, x);
   }
-  SState<N> run = block_exclusive_scan<N>(agg, K, I0, sm, nullptr);
+  RS<KT> run = rs_block_exclusive<KT>(agg, I0, sm);
   for (int64_t t = b; t < e; ++t) {
-    store_sstate(run, tpref, t, K);
-    load_sstate(x, tstate, t, K);
-    sstate_merge(run, x, K);
+    rs_store(run, tpref + (size_t)t * st);
+    rs_load(x, tstate + (size_t)t * st);
+    rs_merge(run, x);
   }
 }
 
 template <typename T, int KT>
-__global__ void __launch_bounds__(CS_BLOCK) cumsum_replay(const T* in, T* out, int64_t n, int K,
-                                                          const unsigned char* __restrict__ tpref) {
-  constexpr int N = KArr<T, KT>::N;
+__global__ void __launch_bounds__(CS_BLOCK) cumsum_fast_replay(const T* in, T* out, int64_t n,
+                                                               const unsigned char* __restrict__ tpref) {
   __shared__ T sm[CS_TILE + CS_TILE / CS_ITEMS];
-  __shared__ SState<N> wsm[CS_BLOCK / 32];
-  const int I0 = Geom<T>::NB - K;
+  __shared__ RS<KT> wsm[CS_BLOCK / 32];
+  const int I0 = Geom<T>::NB - KT;
   int cnt = load_tile<T>(in, n, blockIdx.x, sm);
-  int b = threadIdx.x * CS_ITEMS;
-  SState<N> mine;
-  sstate_zero(mine, I0);
-  for (int i = 0; i < CS_ITEMS; ++i)
-    if (b + i < cnt) sstate_deposit<T, N>(mine, sm[b + i + b / CS_ITEMS], K);
-  SState<N> run = block_exclusive_scan<N>(mine, K, I0, wsm, nullptr);
-  SState<N> tp;
-  load_sstate(tp, tpref, blockIdx.x, K);
-  sstate_merge(tp, run, K);
+  const int b = threadIdx.x * CS_ITEMS;
+  const int sb = b + threadIdx.x;    // padded position of this thread's first element
+  // this thread's own total, then its incoming state
+  RS<KT> mine;
+  rs_zero(mine, I0);
+  {
+    Digits<T, KT> dg;
+    dg.set(I0);
+#pragma unroll 4
+    for (int i = 0; i < CS_ITEMS; ++i)
+      if (b + i < cnt) rs_deposit<T, KT>(mine, dg, sm[sb + i]);
+  }
+  RS<KT> run = rs_block_exclusive<KT>(mine, I0, wsm);
+  RS<KT> s;
+  rs_load(s, tpref + (size_t)blockIdx.x * (16 + 16 * (size_t)KT));
+  rs_merge(s, run);
+  Digits<T, KT> dg;
+  dg.set(s.I);
+#pragma unroll 4
   for (int i = 0; i < CS_ITEMS; ++i) {
     if (b + i < cnt) {
-      int si = b + i + b / CS_ITEMS;
-      sstate_deposit<T, N>(tp, sm[si], K);
-      sm[si] = sstate_value<T, N>(tp, K);
+      rs_deposit<T, KT>(s, dg, sm[sb + i]);
+      sm[sb + i] = convert_fast<T, KT>(s.I, s.flags, s.F);
     }
   }
   __syncthreads();
@@ -391,6 +541,7 @@ __global__ void cumsum_generic_replay(const T* in, T* out, int64_t n, int K, con
 
 template <typename T>
 size_t cumsum_workspace_bytes(int64_t n, int K) {
+  if (K == 3) return cumsum_k3_workspace_bytes<T>(n);
   int64_t nt = (n + CS_TILE - 1) / CS_TILE;
   return 2 * (size_t)nt * (16 + 16 * (size_t)K) + 64;
 }
@@ -400,9 +551,9 @@ static cudaError_t launch_cumsum_k(const T* in, T* out, int64_t n, int K, unsign
   int64_t nt = (n + CS_TILE - 1) / CS_TILE;
   unsigned char* tstate = ws;
   unsigned char* tpref = ws + (size_t)nt * (16 + 16 * (size_t)K);
-  cumsum_tile_reduce<T, KT><<<(unsigned)nt, CS_BLOCK, 0, s>>>(in, n, K, tstate);
-  cumsum_tile_scan<T, KT><<<1, 1024, 0, s>>>(tstate, nt, K, tpref);
-  cumsum_replay<T, KT><<<(unsigned)nt, CS_BLOCK, 0, s>>>(in, out, n, K, tpref);
+  cumsum_fast_reduce<T, KT><<<(unsigned)nt, CS_BLOCK, 0, s>>>(in, n, K, tstate);
+  cumsum_fast_scan<T, KT><<<1, 1024, 0, s>>>(tstate, nt, tpref);
+  cumsum_fast_replay<T, KT><<<(unsigned)nt, CS_BLOCK, 0, s>>>(in, out, n, tpref);
   return cudaGetLastError();
 }
 
@@ -422,7 +573,7 @@ cudaError_t launch_cumsum(const T* in, T* out, int64_t n, int K, unsigned char* 
   (void)block;
   switch (K) {
     case 2: return launch_cumsum_k<T, 2>(in, out, n, K, ws, s);
-    case 3: return launch_cumsum_k<T, 3>(in, out, n, K, ws, s);
+    case 3: return launch_cumsum_k3<T>(in, out, n, ws, s);
     case 4: return launch_cumsum_k<T, 4>(in, out, n, K, ws, s);
     case 5: return launch_cumsum_k<T, 5>(in, out, n, K, ws, s);
     case 6: return launch_cumsum_k<T, 6>(in, out, n, K, ws, s);

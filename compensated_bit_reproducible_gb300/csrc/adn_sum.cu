@@ -38,14 +38,30 @@ __device__ __forceinline__ void accumulate_range(Acc& acc, const T* __restrict__
   const V* xv = (const V*)(x + head);
   int64_t nv = (n - head) / VW;
   int64_t i = t;
-  for (; i + (int64_t)(U - 1) * nt < nv; i += (int64_t)U * nt) {
+  const int64_t step = (int64_t)U * nt;
+  if (i + (int64_t)(U - 1) * nt < nv) {
+    // software pipelined: the next group's loads are in flight while the
+    // current group is deposited
     V r[U];
 #pragma unroll
     for (int u = 0; u < U; ++u) r[u] = ldg_stream(xv + i + (int64_t)u * nt);
-    T v[U * VW];
+    for (;;) {
+      int64_t inext = i + step;
+      bool more = inext + (int64_t)(U - 1) * nt < nv;
+      V q[U];
+      if (more) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) unpack<T>(r[u], v + u * VW);
-    acc.template chunk<U * VW>(v);
+        for (int u = 0; u < U; ++u) q[u] = ldg_stream(xv + inext + (int64_t)u * nt);
+      }
+      T v[U * VW];
+#pragma unroll
+      for (int u = 0; u < U; ++u) unpack<T>(r[u], v + u * VW);
+      acc.template chunk<U * VW>(v);
+      i = inext;
+      if (!more) break;
+#pragma unroll
+      for (int u = 0; u < U; ++u) r[u] = q[u];
+    }
   }
   for (; i < nv; i += nt) {
     T v[VW];
@@ -213,6 +229,34 @@ cudaError_t launch_sum(const T* x, int64_t n, int K, unsigned char* ws, T* resul
 template cudaError_t launch_sum<float>(const float*, int64_t, int, unsigned char*, float*, int, int, cudaStream_t);
 template cudaError_t launch_sum<double>(const double*, int64_t, int, unsigned char*, double*, int, int,
                                         cudaStream_t);
+
+// Resident blocks per SM of the sum kernel for this K and block size (one
+// wave of blocks covers the GPU; more would leave a partial second wave).
+template <typename T, int KT>
+static int occ_k(int block) {
+  int nb = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, adn_sum_kernel<T, KT, 4>, block, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  return nb > 0 ? nb : 1;
+}
+
+template <typename T>
+int sum_blocks_per_sm(int K, int block) {
+  switch (K) {
+    case 2: return occ_k<T, 2>(block);
+    case 3: return occ_k<T, 3>(block);
+    case 4: return occ_k<T, 4>(block);
+    case 5: return occ_k<T, 5>(block);
+    case 6: return occ_k<T, 6>(block);
+    case 7: return occ_k<T, 7>(block);
+    case 8: return occ_k<T, 8>(block);
+    default: return occ_k<T, 0>(block);
+  }
+}
+template int sum_blocks_per_sm<float>(int, int);
+template int sum_blocks_per_sm<double>(int, int);
 
 size_t sum_workspace_bytes(int K, int grid) { return 256 + (size_t)grid * (16 + 16 * (size_t)K) + 64; }
 

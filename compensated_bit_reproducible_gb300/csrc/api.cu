@@ -121,14 +121,14 @@ bool launch_ok(const repro_launch* l) {
 // Grid for the binned sum: enough blocks to fill the GPU, no more than the
 // work needs, and few enough elements per thread that int64 lanes cannot
 // overflow (<= 2^23 deposits per thread).
-int sum_grid(int64_t n, int block, int elems_per_iter, const repro_launch* l) {
+int sum_grid(int64_t n, int block, int elems_per_iter, int blocks_per_sm, const repro_launch* l) {
   if (l && l->grid > 0) {
     int64_t g = l->grid;
     int64_t need = (n + ((int64_t)block << 23) - 1) / ((int64_t)block << 23);
     return (int)(g > need ? g : need);
   }
   int64_t work = (n + (int64_t)block * elems_per_iter - 1) / ((int64_t)block * elems_per_iter);
-  int64_t cap = (int64_t)sm_count() * (2048 / block);
+  int64_t cap = (int64_t)sm_count() * blocks_per_sm;
   int64_t g = work < cap ? work : cap;
   if (g < 1) g = 1;
   return (int)g;
@@ -143,7 +143,8 @@ repro_status sum_async_impl(const T* x, size_t n, int K, cudaStream_t stream, T*
   st = validate_env(stream);
   if (st != REPRO_OK) return st;
   int block = (l && l->block) ? l->block : 256;
-  int grid = sum_grid((int64_t)n, block, 16 * (int)(16 / sizeof(T)) / 4, l);
+  int grid = sum_grid((int64_t)n, block, 4 * (int)(16 / sizeof(T)), sum_blocks_per_sm<T>(K, block),
+                      l);   // 4 vectors per thread per iteration, one wave of blocks
   size_t wsb = sum_workspace_bytes(K, grid);
   Scratch ws;
   ws.s = stream;

@@ -1,0 +1,537 @@
+// Binned cumulative sum, K = 3 (the default fold count), float and double.
+//
+// Same tile structure as the general path (tile totals, their exclusive scan,
+// replay; "SyclReproSum" README, "How It Works", cumsum paragraph), with the
+// replay state kept in registers as its three fold sums F0, F1, F2 plus the
+// exact total T = F0 2^(2W) + F1 2^W + F2 in units of the finest grid.  Each
+// element adds its digits to the folds and their combination to T, so each
+// prefix is one rounding of T; T is rebuilt from the folds only when a larger
+// value raises the bin index (the finest folds drop).
+#include "accum.cuh"
+#include "launch.h"
+
+namespace repro {
+
+constexpr int C3_BLOCK = 256;
+constexpr int C3_ITEMS = 16;
+constexpr int C3_TILE = C3_BLOCK * C3_ITEMS;
+constexpr int C3_WARPS = C3_BLOCK / 32;
+constexpr size_t C3_STATE = 16 + 16 * 3;   // stored state: header + 3 x 128-bit folds
+
+// ----------------------------------------------------------- rounding of T
+// float: T is a signed 128-bit integer (hi, lo) times 2^lsb.
+__device__ __forceinline__ float round_t128_f(int64_t hi, uint64_t lo, int lsb) {
+  bool neg = hi < 0;
+  uint64_t h = (uint64_t)hi, l = lo;
+  if (neg) {
+    l = ~l + 1;
+    h = ~h + (l == 0 ? 1 : 0);
+  }
+  if ((h | l) == 0) return 0.0f;
+  int lz = h ? __clzll((long long)h) : 64 + __clzll((long long)l);
+  uint64_t t64, rest;
+  if (lz == 0) { t64 = h; rest = l; }
+  else if (lz < 64) { t64 = (h << lz) | (l >> (64 - lz)); rest = l << lz; }
+  else if (lz == 64) { t64 = l; rest = 0; }
+  else { t64 = l << (lz - 64); rest = 0; }
+  int E = 127 - lz + lsb;
+  int q = E - 23;
+  if (q < -149) q = -149;
+  int drop = q - (E - 63);   // 40 .. 63: bits of t64 below the quantum
+  uint64_t m = t64 >> drop;
+  bool half = ((t64 >> (drop - 1)) & 1) != 0;
+  bool sticky = ((t64 << (65 - drop)) != 0) || rest != 0;
+  if (half && (sticky || (m & 1))) m += 1;
+  if (m == (1ull << 24)) { m >>= 1; q += 1; }
+  return assemble<float>(neg, m, q);
+}
+
+// double: T is a signed 192-bit integer (t2:t1:t0) times 2^lsb.
+__device__ __forceinline__ double round_t192_d(int64_t t2, uint64_t t1, uint64_t t0, int lsb) {
+  bool neg = t2 < 0;
+  uint64_t a = (uint64_t)t2, b = t1, c = t0;
+  if (neg) {
+    c = ~c + 1;
+    uint64_t cb = (c == 0) ? 1 : 0;
+    b = ~b + cb;
+    uint64_t ca = (cb && b == 0) ? 1 : 0;
+    a = ~a + ca;
+  }
+  if ((a | b | c) == 0) return 0.0;
+  // leading word and the word below it
+  uint64_t w1, w0;
+  bool rest;
+  int topw;
+  if (a) { w1 = a; w0 = b; rest = c != 0; topw = 2; }
+  else if (b) { w1 = b; w0 = c; rest = false; topw = 1; }
+  else { w1 = c; w0 = 0; rest = false; topw = 0; }
+  int lz = __clzll((long long)w1);
+  uint64_t t64 = lz ? ((w1 << lz) | (w0 >> (64 - lz))) : w1;
+  bool st0 = (lz ? (w0 << lz) : w0) != 0 || rest;
+  int E = 64 * topw + 63 - lz + lsb;
+  int q = E - 52;
+  if (q < -1074) q = -1074;
+  int drop = q - (E - 63);   // 11 .. 63
+  uint64_t m = t64 >> drop;
+  bool half = ((t64 >> (drop - 1)) & 1) != 0;
+  bool sticky = ((t64 << (65 - drop)) != 0) || st0;
+  if (half && (sticky || (m & 1))) m += 1;
+  if (m == (1ull << 53)) { m >>= 1; q += 1; }
+  return assemble<double>(neg, m, q);
+}
+
+// ------------------------------------------------------------- run state
+template <typename T> struct Run3;
+
+template <> struct Run3<float> {
+  bool withT;
+  int I, flags;
+  int64_t F0, F1, F2;      // fold sums (float: |F| < 2^45 within capacity)
+  int64_t Th;              // T = F0 2^26 + F1 2^13 + F2 as (Th, Tl)
+  uint64_t Tl;
+  float P0[3];             // fresh primaries of the current index
+  float thrf;
+
+  __device__ __forceinline__ void set_index(int j) {
+    I = j;
+    thrf = (j == 0) ? 0.0f : __uint_as_float(index_threshold<float>(j));
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+      P0[k] = (j >= 1) ? __uint_as_float(((uint32_t)(beta<float>(j + k) + 23 + 127) << 23) | 0x400000u) : 1.0f;
+  }
+  __device__ __forceinline__ void rebuild_T() {
+    int64_t s = F1 * ((int64_t)1 << 13) + F2;
+    uint64_t lo = (uint64_t)F0 << 26;
+    int64_t hi = F0 >> 38;
+    uint64_t nl = lo + (uint64_t)s;
+    hi += (s >> 63) + (int64_t)(nl < lo);
+    Tl = nl;
+    Th = hi;
+  }
+  __device__ __forceinline__ void add_digits(int64_t a0, int64_t a1, int64_t a2) {
+    F0 += a0; F1 += a1; F2 += a2;
+    if (!withT) return;
+    int64_t c = a0 * ((int64_t)1 << 26) + a1 * ((int64_t)1 << 13) + a2;
+    uint64_t nl = Tl + (uint64_t)c;
+    Th += (c >> 63) + (int64_t)(nl < Tl);
+    Tl = nl;
+  }
+  __device__ __forceinline__ void raise(int j) {
+    int d = I - j;
+    int64_t f0 = F0, f1 = F1, f2 = F2;
+    F0 = (d == 0) ? f0 : 0;
+    F1 = (d == 0) ? f1 : (d == 1 ? f0 : 0);
+    F2 = (d == 0) ? f2 : (d == 1 ? f1 : (d == 2 ? f0 : 0));
+    set_index(j);
+    if (withT) rebuild_T();
+  }
+  __device__ __forceinline__ void deposit(float x) {
+    if (!(fabsf(x) < thrf)) {
+      if (!(fabsf(x) <= 3.4028235e38f)) {
+        flags |= special_flag(x);
+        return;
+      }
+      if (x == 0.0f) return;
+      int j = bin_index<float>(x);
+      if (j < I) raise(j);
+      if (I == 0) {   // bin 0: the float primary would overflow; integer digits
+        int64_t a[3];
+        chain_digits<float>(x, 0, 3, a);
+        add_digits(a[0], a[1], a[2]);
+        return;
+      }
+    }
+    float r = x;
+    int64_t a[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      float q = __uint_as_float(__float_as_uint(r) | 1u);
+      float S = __fadd_rn(P0[k], q);
+      a[k] = (int32_t)(__float_as_uint(S) - __float_as_uint(P0[k]));
+      if (k < 2) r = __fadd_rn(r, __fsub_rn(P0[k], S));
+    }
+    add_digits(a[0], a[1], a[2]);
+  }
+  __device__ __forceinline__ float value() const {
+    if (flags) return from_flags<float>(flags);
+    return round_t128_f(Th, Tl, beta<float>(I + 2));
+  }
+};
+
+template <> struct Run3<double> {
+  bool withT;
+  int I, flags;
+  W128 F0, F1, F2;
+  int64_t T2;              // T = F0 2^80 + F1 2^40 + F2 as (T2, T1, T0)
+  uint64_t T1, T0;
+  FastD<3> fc;
+  uint32_t thr_hi;
+
+  __device__ __forceinline__ void set_index(int j) {
+    I = j;
+    fc.set(j);
+    thr_hi = (uint32_t)(index_threshold<double>(j) >> 32);
+  }
+  // T += v * 2^off for a sign-extended 128-bit v and off in {0, 40, 80}
+  __device__ __forceinline__ void add_shifted(W128 v, int off) {
+    uint64_t ext = (v.hi < 0) ? ~0ull : 0ull;
+    uint64_t s0, s1, s2;
+    if (off == 0) { s0 = v.lo; s1 = (uint64_t)v.hi; s2 = ext; }
+    else if (off == 40) {
+      s0 = v.lo << 40;
+      s1 = ((uint64_t)v.hi << 40) | (v.lo >> 24);
+      s2 = (uint64_t)(v.hi >> 24);
+    } else {   // 80 = 64 + 16
+      s0 = 0;
+      s1 = v.lo << 16;
+      s2 = ((uint64_t)v.hi << 16) | (v.lo >> 48);
+    }
+    uint64_t n0 = T0 + s0;
+    uint64_t c0 = n0 < T0;
+    uint64_t n1 = T1 + s1;
+    uint64_t c1 = n1 < T1;
+    uint64_t n1b = n1 + c0;
+    c1 |= (n1b < n1);
+    T0 = n0;
+    T1 = n1b;
+    T2 = (int64_t)((uint64_t)T2 + s2 + c1);
+  }
+  __device__ __forceinline__ void rebuild_T() {
+    T0 = 0; T1 = 0; T2 = 0;
+    add_shifted(F2, 0);
+    add_shifted(F1, 40);
+    add_shifted(F0, 80);
+  }
+  __device__ __forceinline__ void add_digits(int64_t a0, int64_t a1, int64_t a2) {
+    F0 = w_add(F0, w_from(a0));
+    F1 = w_add(F1, w_from(a1));
+    F2 = w_add(F2, w_from(a2));
+    if (!withT) return;
+    add_shifted(w_from(a2), 0);
+    add_shifted(w_from(a1), 40);
+    add_shifted(w_from(a0), 80);
+  }
+  __device__ __forceinline__ void raise(int j) {
+    int d = I - j;
+    W128 f0 = F0, f1 = F1, f2 = F2, z = W128{0, 0};
+    F0 = (d == 0) ? f0 : z;
+    F1 = (d == 0) ? f1 : (d == 1 ? f0 : z);
+    F2 = (d == 0) ? f2 : (d == 1 ? f1 : (d == 2 ? f0 : z));
+    set_index(j);
+    if (withT) rebuild_T();
+  }
+  __device__ __forceinline__ void deposit(double x) {
+    if (((uint32_t)__double2hiint(x) & 0x7FFFFFFFu) >= thr_hi) {
+      if (((uint32_t)__double2hiint(x) & 0x7FFFFFFFu) >= 0x7FF00000u) {
+        flags |= special_flag(x);
+        return;
+      }
+      int j = bin_index<double>(x);
+      if (j < I) raise(j);
+    }
+    int64_t a[3];
+    fast_digits_f64<3>(x, fc, a);
+    add_digits(a[0], a[1], a[2]);
+  }
+  __device__ __forceinline__ double value() const {
+    if (flags) return from_flags<double>(flags);
+    return round_t192_d(T2, T1, T0, beta<double>(I + 2));
+  }
+};
+
+// ------------------------------------------------------ state helpers
+struct S3 {   // merged state: index, flags, three 128-bit folds
+  int I;
+  int flags;
+  W128 F[3];
+};
+
+__device__ __forceinline__ S3 s3_zero(int I0) {
+  S3 s;
+  s.I = I0;
+  s.flags = 0;
+  s.F[0] = s.F[1] = s.F[2] = W128{0, 0};
+  return s;
+}
+
+__device__ __forceinline__ void s3_shift(S3& s, int d) {   // fold k -> k + d
+  W128 z = W128{0, 0};
+  W128 f0 = s.F[0], f1 = s.F[1], f2 = s.F[2];
+  s.F[0] = (d == 0) ? f0 : z;
+  s.F[1] = (d == 0) ? f1 : (d == 1 ? f0 : z);
+  s.F[2] = (d == 0) ? f2 : (d == 1 ? f1 : (d == 2 ? f0 : z));
+}
+
+__device__ __forceinline__ void s3_merge(S3& a, S3 b) {
+  if (b.I < a.I) { s3_shift(a, a.I - b.I); a.I = b.I; }
+  else if (a.I < b.I) { s3_shift(b, b.I - a.I); }
+  a.F[0] = w_add(a.F[0], b.F[0]);
+  a.F[1] = w_add(a.F[1], b.F[1]);
+  a.F[2] = w_add(a.F[2], b.F[2]);
+  a.flags |= b.flags;
+}
+
+__device__ __forceinline__ S3 s3_shfl_up(const S3& s, int d) {
+  S3 o;
+  o.I = __shfl_up_sync(0xffffffffu, s.I, d);
+  o.flags = __shfl_up_sync(0xffffffffu, s.flags, d);
+  o.F[0] = shfl_up_w(s.F[0], d);
+  o.F[1] = shfl_up_w(s.F[1], d);
+  o.F[2] = shfl_up_w(s.F[2], d);
+  return o;
+}
+
+__device__ __forceinline__ S3 s3_shfl_xor(const S3& s, int m) {
+  S3 o;
+  o.I = __shfl_xor_sync(0xffffffffu, s.I, m);
+  o.flags = __shfl_xor_sync(0xffffffffu, s.flags, m);
+  o.F[0] = shfl_xor_w(s.F[0], m);
+  o.F[1] = shfl_xor_w(s.F[1], m);
+  o.F[2] = shfl_xor_w(s.F[2], m);
+  return o;
+}
+
+__device__ __forceinline__ S3 s3_load(const unsigned char* p) {
+  int4 h = *(const int4*)p;
+  longlong2 f0 = *(const longlong2*)(p + 16), f1 = *(const longlong2*)(p + 32), f2 = *(const longlong2*)(p + 48);
+  S3 s;
+  s.I = h.x;
+  s.flags = h.y;
+  s.F[0] = W128{(uint64_t)f0.x, (int64_t)f0.y};
+  s.F[1] = W128{(uint64_t)f1.x, (int64_t)f1.y};
+  s.F[2] = W128{(uint64_t)f2.x, (int64_t)f2.y};
+  return s;
+}
+
+__device__ __forceinline__ void s3_store(const S3& s, unsigned char* p) {
+  *(int4*)p = make_int4(s.I, s.flags, 0, 0);
+  *(longlong2*)(p + 16) = make_longlong2((long long)s.F[0].lo, (long long)s.F[0].hi);
+  *(longlong2*)(p + 32) = make_longlong2((long long)s.F[1].lo, (long long)s.F[1].hi);
+  *(longlong2*)(p + 48) = make_longlong2((long long)s.F[2].lo, (long long)s.F[2].hi);
+}
+
+// inclusive warp scan (lane l gets the merge of lanes 0..l)
+__device__ __forceinline__ S3 s3_warp_inclusive(S3 v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    S3 o = s3_shfl_up(v, d);
+    if (lane >= d) {
+      s3_merge(o, v);
+      v = o;
+    }
+  }
+  return v;
+}
+
+template <typename T>
+__device__ __forceinline__ S3 run_to_s3(const Run3<T>& r);
+template <>
+__device__ __forceinline__ S3 run_to_s3<float>(const Run3<float>& r) {
+  S3 s;
+  s.I = r.I;
+  s.flags = r.flags;
+  s.F[0] = w_from(r.F0);
+  s.F[1] = w_from(r.F1);
+  s.F[2] = w_from(r.F2);
+  return s;
+}
+template <>
+__device__ __forceinline__ S3 run_to_s3<double>(const Run3<double>& r) {
+  S3 s;
+  s.I = r.I;
+  s.flags = r.flags;
+  s.F[0] = r.F0;
+  s.F[1] = r.F1;
+  s.F[2] = r.F2;
+  return s;
+}
+
+template <typename T>
+__device__ __forceinline__ void run_from_s3(Run3<T>& r, const S3& s);
+template <>
+__device__ __forceinline__ void run_from_s3<float>(Run3<float>& r, const S3& s) {
+  r.flags = s.flags;
+  r.F0 = (int64_t)s.F[0].lo;   // float fold sums fit in 64 bits within capacity
+  r.F1 = (int64_t)s.F[1].lo;
+  r.F2 = (int64_t)s.F[2].lo;
+  r.set_index(s.I);
+  if (r.withT) r.rebuild_T();
+}
+template <>
+__device__ __forceinline__ void run_from_s3<double>(Run3<double>& r, const S3& s) {
+  r.flags = s.flags;
+  r.F0 = s.F[0];
+  r.F1 = s.F[1];
+  r.F2 = s.F[2];
+  r.set_index(s.I);
+  if (r.withT) r.rebuild_T();
+}
+
+template <typename T>
+__device__ __forceinline__ Run3<T> run_zero(bool withT) {
+  Run3<T> r;
+  r.withT = withT;
+  r.flags = 0;
+  if constexpr (sizeof(T) == 4) { r.F0 = r.F1 = r.F2 = 0; r.Th = 0; r.Tl = 0; }
+  else { r.F0 = r.F1 = r.F2 = W128{0, 0}; r.T0 = r.T1 = 0; r.T2 = 0; }
+  r.set_index(Geom<T>::NB - 3);
+  return r;
+}
+
+// ------------------------------------------------------------------ A
+// Per-warp totals: warp w of a tile covers its elements [w * 512, w * 512 +
+// 512); lane l takes every 32nd element (coalesced).  Totals are order free.
+template <typename T>
+__global__ void __launch_bounds__(C3_BLOCK) c3_warp_totals(const T* __restrict__ in, int64_t n,
+                                                           unsigned char* __restrict__ wtot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t tile = blockIdx.x;
+  const int64_t base = tile * C3_TILE + (int64_t)warp * (C3_TILE / C3_WARPS);
+  Run3<T> r = run_zero<T>(false);
+#pragma unroll 4
+  for (int i = 0; i < C3_TILE / C3_WARPS / 32; ++i) {
+    int64_t idx = base + lane + 32 * i;
+    if (idx < n) r.deposit(__ldcs(in + idx));
+  }
+  S3 s = run_to_s3<T>(r);
+  // warp merge (xor butterfly: every lane ends with the total)
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) {
+    S3 o = s3_shfl_xor(s, m);
+    s3_merge(s, o);
+  }
+  if (lane == 0) s3_store(s, wtot + (size_t)(tile * C3_WARPS + warp) * C3_STATE);
+}
+
+// ------------------------------------------------------------------ B
+// B1: one thread per tile (1024 tiles per block): tile total = merge of its
+// warp totals; exclusive scan within the block -> local tile prefix; block
+// total.  B2: one block scans the block totals exclusively.
+__global__ void __launch_bounds__(1024) c3_scan_tiles(const unsigned char* __restrict__ wtot, int64_t ntiles,
+                                                      int I0, unsigned char* __restrict__ tloc,
+                                                      unsigned char* __restrict__ btot) {
+  __shared__ S3 sm[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  S3 tot = s3_zero(I0);
+  if (t < ntiles) {
+#pragma unroll
+    for (int w = 0; w < C3_WARPS; ++w) s3_merge(tot, s3_load(wtot + (size_t)(t * C3_WARPS + w) * C3_STATE));
+  }
+  S3 inc = s3_warp_inclusive(tot);
+  if (lane == 31) sm[warp] = inc;
+  __syncthreads();
+  S3 base = s3_zero(I0);
+  for (int w = 0; w < warp; ++w) s3_merge(base, sm[w]);
+  S3 exc = s3_shfl_up(inc, 1);
+  if (lane == 0) exc = s3_zero(I0);
+  s3_merge(base, exc);
+  if (t < ntiles) s3_store(base, tloc + (size_t)t * C3_STATE);
+  if (threadIdx.x == blockDim.x - 1) {
+    S3 all = base;
+    s3_merge(all, tot);
+    s3_store(all, btot + (size_t)blockIdx.x * C3_STATE);
+  }
+}
+
+__global__ void __launch_bounds__(1024) c3_scan_blocks(unsigned char* __restrict__ btot, int64_t nb, int I0,
+                                                       unsigned char* __restrict__ bpre) {
+  __shared__ S3 sm[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // nb <= 1024 * per; thread t handles [t * per, ...)
+  int64_t per = (nb + blockDim.x - 1) / blockDim.x;
+  int64_t b = (int64_t)threadIdx.x * per, e = min(nb, b + per);
+  S3 agg = s3_zero(I0);
+  for (int64_t i = b; i < e; ++i) s3_merge(agg, s3_load(btot + (size_t)i * C3_STATE));
+  S3 inc = s3_warp_inclusive(agg);
+  if (lane == 31) sm[warp] = inc;
+  __syncthreads();
+  S3 run = s3_zero(I0);
+  for (int w = 0; w < warp; ++w) s3_merge(run, sm[w]);
+  S3 exc = s3_shfl_up(inc, 1);
+  if (lane == 0) exc = s3_zero(I0);
+  s3_merge(run, exc);
+  for (int64_t i = b; i < e; ++i) {
+    S3 x = s3_load(btot + (size_t)i * C3_STATE);
+    s3_store(run, bpre + (size_t)i * C3_STATE);
+    s3_merge(run, x);
+  }
+}
+
+// ------------------------------------------------------------------ C
+template <typename T>
+__global__ void __launch_bounds__(C3_BLOCK) c3_replay(const T* in, T* out, int64_t n,
+                                                      const unsigned char* __restrict__ tloc,
+                                                      const unsigned char* __restrict__ bpre) {
+  __shared__ T sm[C3_TILE + C3_TILE / C3_ITEMS];
+  __shared__ S3 wsm[C3_WARPS];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t tile = blockIdx.x;
+  const int64_t base = tile * C3_TILE;
+  const int cnt = (int)min((int64_t)C3_TILE, n - base);
+  for (int i = threadIdx.x; i < cnt; i += blockDim.x) sm[i + i / C3_ITEMS] = in[base + i];
+  __syncthreads();
+  const int b = threadIdx.x * C3_ITEMS;
+  const int sb = b + threadIdx.x;
+  const int I0 = Geom<T>::NB - 3;
+  // this thread's own total
+  Run3<T> own = run_zero<T>(false);
+#pragma unroll 4
+  for (int i = 0; i < C3_ITEMS; ++i)
+    if (b + i < cnt) own.deposit(sm[sb + i]);
+  S3 mine = run_to_s3<T>(own);
+  // exclusive scan across the block
+  S3 inc = s3_warp_inclusive(mine);
+  if (lane == 31) wsm[warp] = inc;
+  __syncthreads();
+  S3 st = s3_load(bpre + (size_t)(tile / 1024) * C3_STATE);
+  s3_merge(st, s3_load(tloc + (size_t)tile * C3_STATE));
+  for (int w = 0; w < warp; ++w) s3_merge(st, wsm[w]);
+  S3 exc = s3_shfl_up(inc, 1);
+  if (lane == 0) exc = s3_zero(I0);
+  s3_merge(st, exc);
+  // replay
+  Run3<T> r;
+  r.withT = true;
+  run_from_s3<T>(r, st);
+#pragma unroll 4
+  for (int i = 0; i < C3_ITEMS; ++i) {
+    if (b + i < cnt) {
+      r.deposit(sm[sb + i]);
+      sm[sb + i] = r.value();
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < cnt; i += blockDim.x) out[base + i] = sm[i + i / C3_ITEMS];
+}
+
+template <typename T>
+size_t cumsum_k3_workspace_bytes(int64_t n) {
+  int64_t nt = (n + C3_TILE - 1) / C3_TILE;
+  int64_t nb = (nt + 1023) / 1024;
+  return ((size_t)nt * C3_WARPS + (size_t)nt + 2 * (size_t)nb) * C3_STATE + 256;
+}
+
+template <typename T>
+cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, cudaStream_t s) {
+  int64_t nt = (n + C3_TILE - 1) / C3_TILE;
+  int64_t nb = (nt + 1023) / 1024;
+  unsigned char* wtot = ws;
+  unsigned char* tloc = wtot + (size_t)nt * C3_WARPS * C3_STATE;
+  unsigned char* btot = tloc + (size_t)nt * C3_STATE;
+  unsigned char* bpre = btot + (size_t)nb * C3_STATE;
+  const int I0 = Geom<T>::NB - 3;
+  c3_warp_totals<T><<<(unsigned)nt, C3_BLOCK, 0, s>>>(in, n, wtot);
+  c3_scan_tiles<<<(unsigned)nb, 1024, 0, s>>>(wtot, nt, I0, tloc, btot);
+  c3_scan_blocks<<<1, 1024, 0, s>>>(btot, nb, I0, bpre);
+  c3_replay<T><<<(unsigned)nt, C3_BLOCK, 0, s>>>(in, out, n, tloc, bpre);
+  return cudaGetLastError();
+}
+
+template size_t cumsum_k3_workspace_bytes<float>(int64_t);
+template size_t cumsum_k3_workspace_bytes<double>(int64_t);
+template cudaError_t launch_cumsum_k3<float>(const float*, float*, int64_t, unsigned char*, cudaStream_t);
+template cudaError_t launch_cumsum_k3<double>(const double*, double*, int64_t, unsigned char*, cudaStream_t);
+
+}  // namespace repro

@@ -11,6 +11,8 @@ template <typename T>
 cudaError_t launch_sum(const T* x, int64_t n, int K, unsigned char* ws, T* result, int grid, int block,
                        cudaStream_t s);
 size_t sum_workspace_bytes(int K, int grid);
+template <typename T>
+int sum_blocks_per_sm(int K, int block);
 cudaError_t launch_segsum(const float* x, int64_t rows, int64_t cols, int axis, int K, float* out, int grid,
                           int block, cudaStream_t s);
 
@@ -19,6 +21,10 @@ template <typename T>
 size_t cumsum_workspace_bytes(int64_t n, int K);
 template <typename T>
 cudaError_t launch_cumsum(const T* in, T* out, int64_t n, int K, unsigned char* ws, int block, cudaStream_t s);
+template <typename T>
+size_t cumsum_k3_workspace_bytes(int64_t n);
+template <typename T>
+cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, cudaStream_t s);
 
 // variance
 cudaError_t launch_var(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out, float* mean,
