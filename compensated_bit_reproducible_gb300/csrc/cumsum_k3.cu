@@ -9,6 +9,7 @@
 // value raises the bin index (the finest folds drop).
 #include "accum.cuh"
 #include "launch.h"
+#include <type_traits>
 
 namespace repro {
 
@@ -69,6 +70,16 @@ __device__ __forceinline__ double round_t192_d(int64_t t2, uint64_t t1, uint64_t
   uint64_t t64 = lz ? ((w1 << lz) | (w0 >> (64 - lz))) : w1;
   bool st0 = (lz ? (w0 << lz) : w0) != 0 || rest;
   int E = 64 * topw + 63 - lz + lsb;
+  if (E >= -1022 && E < 1023) {
+    // normal result: 53 bits of t64, round bit, sticky; a carry out of the
+    // significand moves into the exponent field by the addition itself
+    uint64_t m = t64 >> 11;
+    bool half = ((t64 >> 10) & 1) != 0;
+    bool sticky = ((t64 & 0x3FF) != 0) || st0;
+    m += (half && (sticky || (m & 1))) ? 1 : 0;
+    uint64_t bits = ((uint64_t)(E + 1022) << 52) + m;
+    return __longlong_as_double((long long)(bits | (neg ? 0x8000000000000000ull : 0ull)));
+  }
   int q = E - 52;
   if (q < -1074) q = -1074;
   int drop = q - (E - 63);   // 11 .. 63
@@ -154,7 +165,19 @@ template <> struct Run3<float> {
   }
   __device__ __forceinline__ float value() const {
     if (flags) return from_flags<float>(flags);
-    return round_t128_f(Th, Tl, beta<float>(I + 2));
+    const int lsb = beta<float>(I + 2);
+    if (Th == ((int64_t)Tl >> 63)) {
+      // T fits in 64 bits: one correctly rounded integer conversion, then an
+      // exact power-of-two scaling by moving the exponent field, valid while
+      // the scaled result stays a normal float
+      float f = __ll2float_rn((long long)Tl);
+      uint32_t fb = __float_as_uint(f);
+      int ef = (int)((fb >> 23) & 0xFF);
+      if (ef == 0) return 0.0f;                 // T == 0: +0
+      int en = ef + lsb;
+      if (en >= 1 && en <= 254) return __uint_as_float(fb + ((uint32_t)lsb << 23));
+    }
+    return round_t128_f(Th, Tl, lsb);
   }
 };
 
@@ -207,9 +230,23 @@ template <> struct Run3<double> {
     F1 = w_add(F1, w_from(a1));
     F2 = w_add(F2, w_from(a2));
     if (!withT) return;
-    add_shifted(w_from(a2), 0);
-    add_shifted(w_from(a1), 40);
-    add_shifted(w_from(a0), 80);
+    // c = a0 2^80 + a1 2^40 + a2 as three words (|a_k| <= 2^39 + 1)
+    uint64_t l1 = (uint64_t)a1 << 40;
+    uint64_t c0 = l1 + (uint64_t)a2;
+    int64_t c1 = (a1 >> 24) + (a2 >> 63) + (int64_t)(c0 < l1);   // bits 64..127 before a0
+    uint64_t x1 = (uint64_t)a0 << 16;                               // a0 2^80, word 1
+    int64_t x2 = a0 >> 48;                                          // a0 2^80, word 2
+    uint64_t m1 = (uint64_t)c1 + x1;
+    int64_t c2 = (c1 >> 63) + x2 + (int64_t)(m1 < x1);
+    uint64_t n0 = T0 + c0;
+    uint64_t k0 = n0 < T0;
+    uint64_t n1 = T1 + m1;
+    uint64_t k1 = n1 < T1;
+    uint64_t n1b = n1 + k0;
+    k1 |= (n1b < n1);
+    T0 = n0;
+    T1 = n1b;
+    T2 = (int64_t)((uint64_t)T2 + (uint64_t)c2 + k1);
   }
   __device__ __forceinline__ void raise(int j) {
     int d = I - j;
@@ -385,17 +422,44 @@ __device__ __forceinline__ Run3<T> run_zero(bool withT) {
 template <typename T>
 __global__ void __launch_bounds__(C3_BLOCK) c3_warp_totals(const T* __restrict__ in, int64_t n,
                                                            unsigned char* __restrict__ wtot) {
+  typedef typename AccOf<T, 3>::type Acc;
+  typedef typename std::conditional<sizeof(T) == 4, float4, double2>::type V;
+  constexpr int VW = 16 / sizeof(T);
+  constexpr int PER = C3_TILE / C3_WARPS;          // elements per warp
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t tile = blockIdx.x;
-  const int64_t base = tile * C3_TILE + (int64_t)warp * (C3_TILE / C3_WARPS);
-  Run3<T> r = run_zero<T>(false);
-#pragma unroll 4
-  for (int i = 0; i < C3_TILE / C3_WARPS / 32; ++i) {
-    int64_t idx = base + lane + 32 * i;
-    if (idx < n) r.deposit(__ldcs(in + idx));
+  const int64_t base = tile * C3_TILE + (int64_t)warp * PER;
+  Acc acc;
+  acc.init(3);
+  const bool vec = ((((uintptr_t)(in + base)) & 15) == 0) && base + PER <= n;
+  if (vec) {
+    const V* p = (const V*)(in + base);
+    constexpr int NV = PER / VW / 32;               // vectors per lane
+    V r[NV];
+#pragma unroll
+    for (int u = 0; u < NV; ++u) r[u] = __ldcs(p + lane + 32 * u);
+    T v[NV * VW];
+#pragma unroll
+    for (int u = 0; u < NV; ++u) {
+      if constexpr (sizeof(T) == 4) { v[4 * u] = r[u].x; v[4 * u + 1] = r[u].y; v[4 * u + 2] = r[u].z; v[4 * u + 3] = r[u].w; }
+      else { v[2 * u] = r[u].x; v[2 * u + 1] = r[u].y; }
+    }
+    acc.template chunk<NV * VW>(v);
+  } else {
+    for (int i = 0; i < PER / 32; ++i) {
+      int64_t idx = base + lane + 32 * i;
+      if (idx < n) {
+        T v[1] = {in[idx]};
+        acc.template chunk<1>(v);
+      }
+    }
   }
-  S3 s = run_to_s3<T>(r);
-  // warp merge (xor butterfly: every lane ends with the total)
+  acc.finish();
+  S3 s = s3_zero(acc.I);
+  s.flags = acc.flags;
+  s.F[0] = w_from(acc.L[0]);
+  s.F[1] = w_from(acc.L[1]);
+  s.F[2] = w_from(acc.L[2]);
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) {
     S3 o = s3_shfl_xor(s, m);
