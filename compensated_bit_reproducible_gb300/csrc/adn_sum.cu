@@ -155,7 +155,8 @@ __global__ void __launch_bounds__(1024) adn_sum_kernel(const T* __restrict__ x, 
   __threadfence();
   merge_partials_cg<N>(parts, gridDim.x, K, &st);
   if (threadIdx.x == 0) {
-    *result = convert_state<T, N>(st, K);
+    if constexpr (KT != 0) *result = convert_fast<T, KT>(st.I, st.flags, st.F);
+    else *result = convert_state<T, N>(st, K);
     *ticket = 0u;
   }
 }
@@ -175,7 +176,10 @@ __global__ void __launch_bounds__(1024) segsum_rows_kernel(const float* __restri
     acc.finish();
     State<N> st;
     block_merge<N>(acc.I, acc.flags, acc.L, K, &st);
-    if (threadIdx.x == 0) out[r] = convert_state<float, N>(st, K);
+    if (threadIdx.x == 0) {
+      if constexpr (KT != 0) out[r] = convert_fast<float, KT>(st.I, st.flags, st.F);
+      else out[r] = convert_state<float, N>(st, K);
+    }
     __syncthreads();
   }
 }

@@ -168,9 +168,6 @@ __global__ void __launch_bounds__(1024) var_rows_kernel(const float* __restrict_
     }
     N2 v2;
     bool h2 = st2.root(v2, n2_combine);
-    if (MODE == 1) {
-      // reference: the d^2 tree is a plain tree (carry stays zero and unused)
-    }
     N2 tot = tree_combine_block<N2>(v2, h2, blockDim.x, sm2, smv, n2_combine);
     if (threadIdx.x == 0) {
       float var;
@@ -281,6 +278,100 @@ __global__ void __launch_bounds__(256) var_cols_kernel(const float* __restrict__
   }
 }
 
+// Register version for rows of at most 256 * 16 elements: thread t owns the
+// C leaves [t C, t C + C) (C a power of two <= 16) in registers; the subtree
+// is the statically unrolled adjacent-pair tree over its valid prefix.
+template <typename Node, int C, typename F>
+__device__ __forceinline__ bool reg_tree(Node* a, int m, F comb) {
+  // a[0..C) with the first m valid; returns whether the root exists (in a[0])
+  int cnt = m;
+#pragma unroll
+  for (int w = C; w > 1; w >>= 1) {
+#pragma unroll
+    for (int i = 0; i < w / 2; ++i) {
+      if (2 * i + 1 < cnt) a[i] = comb(a[2 * i], a[2 * i + 1]);
+      else if (2 * i < cnt) a[i] = a[2 * i];
+    }
+    cnt = (cnt + 1) >> 1;
+  }
+  return m > 0;
+}
+
+template <int C, int MODE>
+__global__ void __launch_bounds__(256) var_rows_reg(const float* __restrict__ x, int64_t rows, int64_t cols, int ddof,
+                                                    float* __restrict__ out, float* __restrict__ mean_out) {
+  __shared__ float smf[32];
+  __shared__ N2 sm2[32];
+  __shared__ bool smv[32];
+  __shared__ float bc[1];
+  const int n = (int)cols;
+  const float nf = (float)n;
+  const int b = threadIdx.x * C;
+  int m = n - b;
+  m = m < 0 ? 0 : (m > C ? C : m);
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const float* row = x + r * cols;
+    const float x0 = __ldg(row);
+    float v[C];
+    if (C % 4 == 0 && m == C && ((((uintptr_t)(row + b)) & 15) == 0)) {
+#pragma unroll
+      for (int u = 0; u < C / 4; ++u) {
+        float4 q = __ldcs((const float4*)(row + b) + u);
+        v[4 * u] = q.x; v[4 * u + 1] = q.y; v[4 * u + 2] = q.z; v[4 * u + 3] = q.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < C; ++i) v[i] = (i < m) ? row[b + i] : 0.0f;
+    }
+    // pass 1
+    float t1[C];
+#pragma unroll
+    for (int i = 0; i < C; ++i) t1[i] = (MODE == 0) ? __fsub_rn(v[i], x0) : v[i];
+    bool h1 = reg_tree<float, C>(t1, m, f_combine);
+    float sum1 = tree_combine_block<float>(t1[0], h1, blockDim.x, smf, smv, f_combine);
+    if (threadIdx.x == 0) bc[0] = (MODE == 0) ? __fdiv_rn(sum1, nf) : __fmul_rn(sum1, __fdiv_rn(1.0f, nf));
+    __syncthreads();
+    const float mu = bc[0];
+    // pass 2
+    N2 t2[C];
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      float d = (MODE == 0) ? __fsub_rn(__fsub_rn(v[i], x0), mu) : __fsub_rn(v[i], mu);
+      t2[i] = N2{TS{__fmul_rn(d, d), 0.0f}, d};
+    }
+    bool h2 = reg_tree<N2, C>(t2, m, n2_combine);
+    N2 tot = tree_combine_block<N2>(t2[0], h2, blockDim.x, sm2, smv, n2_combine);
+    if (threadIdx.x == 0) {
+      float var;
+      if (MODE == 0) {
+        float s2 = __fadd_rn(tot.q.s, tot.q.c);
+        float t = __fdiv_rn(tot.d, nf);
+        var = max_nan0(__fsub_rn(__fdiv_rn(s2, nf), __fmul_rn(t, t)));
+      } else {
+        float inv = __fdiv_rn(1.0f, nf);
+        float md = __fmul_rn(tot.d, inv);
+        var = max_nan0(__fsub_rn(__fmul_rn(tot.q.s, inv), __fmul_rn(md, md)));
+      }
+      if (ddof != 0) var = __fmul_rn(var, __fdiv_rn(nf, (float)(n - ddof)));
+      out[r] = var;
+      if (mean_out) mean_out[r] = (MODE == 0) ? __fadd_rn(x0, mu) : mu;
+    }
+    __syncthreads();
+  }
+}
+
+template <int MODE>
+static void launch_rows_reg(int64_t C, const float* x, int64_t rows, int64_t cols, int ddof, float* out, float* mean,
+                            unsigned grid, cudaStream_t s) {
+  switch (C) {
+    case 1: var_rows_reg<1, MODE><<<grid, 256, 0, s>>>(x, rows, cols, ddof, out, mean); break;
+    case 2: var_rows_reg<2, MODE><<<grid, 256, 0, s>>>(x, rows, cols, ddof, out, mean); break;
+    case 4: var_rows_reg<4, MODE><<<grid, 256, 0, s>>>(x, rows, cols, ddof, out, mean); break;
+    case 8: var_rows_reg<8, MODE><<<grid, 256, 0, s>>>(x, rows, cols, ddof, out, mean); break;
+    default: var_rows_reg<16, MODE><<<grid, 256, 0, s>>>(x, rows, cols, ddof, out, mean); break;
+  }
+}
+
 static int64_t pow2_ceil(int64_t v) {
   int64_t p = 1;
   while (p < v) p <<= 1;
@@ -297,6 +388,11 @@ cudaError_t launch_var(const float* x, int64_t rows, int64_t cols, int axis, int
     int64_t C = np / block;
     if (C < 1) C = 1;
     int64_t grid = rows < 65535 * 16 ? rows : 65535 * 16;
+    if (C <= 16) {
+      if (twoterm) launch_rows_reg<1>(C, x, rows, cols, ddof, out, mean, (unsigned)grid, s);
+      else launch_rows_reg<0>(C, x, rows, cols, ddof, out, mean, (unsigned)grid, s);
+      return cudaGetLastError();
+    }
     if (twoterm)
       var_rows_kernel<1><<<(unsigned)grid, block, 0, s>>>(x, rows, cols, ddof, out, mean, C);
     else
