@@ -60,7 +60,7 @@ struct Lanes {
 };
 
 // --------------------------------------------------- float primary form
-// Floating-point primaries (README "How It Works": deposit with the sticky
+// Floating-point primaries ("SyclReproSum", "How It Works": deposit with the sticky
 // bit, renormalise), one per fold, each with ulp equal to the fold's grid:
 // P starts at 1.5 * 2^e, and a deposit S = P + sticky(r) rounds r on the grid
 // with ties away from zero; r + (P - S) is the exact remainder.  Every <= 512

@@ -1,6 +1,6 @@
 // Binned (Ahrens-Demmel-Nguyen) summation: device-side building blocks.
 //
-// The binned format follows the SyclReproSum README ("How It Works",
+// The binned format follows the SyclReproSum ("How It Works",
 // "Template Parameters", "Accumulator capacity"): a value is split into K
 // pieces on a fixed global grid of exponent bins, bin width W = 13 (float) /
 // 40 (double), at most 21 / 52 bins.  Bin j has grid unit g_j = 2^(B0 - W j)
@@ -13,7 +13,7 @@
 // correct rounding of their total.
 //
 // Two deposit forms produce the same fold sums:
-//  - float: the README's floating-point primaries (deposit with a forced
+//  - float: the SyclReproSum page's floating-point primaries (deposit with a forced
 //    least-significant "sticky" bit so the grid rounding is order
 //    independent, periodic renormalisation), flushed into int64 lanes;
 //  - double (and every rare case): integer digits of the same chained
@@ -52,7 +52,7 @@ template <> struct Geom<double> {
 template <typename T> __host__ __device__ constexpr int beta(int j) { return Geom<T>::B0 - Geom<T>::W * j; }
 
 // Special-value flags: any NaN, or +Inf with -Inf, gives the canonical quiet
-// NaN; otherwise an Inf propagates (README, "How It Works").
+// NaN; otherwise an Inf propagates ("SyclReproSum", "How It Works").
 enum : int { FL_NAN = 1, FL_PINF = 2, FL_NINF = 4 };
 
 // ---------------------------------------------------------------- decoding

@@ -1,4 +1,4 @@
-// Binned cumulative sum (SyclReproSum README, "How It Works", cumsum
+// Binned cumulative sum (SyclReproSum, "How It Works", cumsum
 // paragraph): contiguous tiles are reduced to binned totals, the totals are
 // scanned exclusively in binned form, and each tile is replayed from its
 // incoming state, converting every prefix.  Only tile totals and tile
@@ -244,7 +244,7 @@ template <int K> struct Digits<float, K> {
       P0[k] = (I >= 1) ? __uint_as_float(((uint32_t)(beta<float>(I + k) + 23 + 127) << 23) | 0x400000u) : 1.0f;
   }
   __device__ __forceinline__ bool fits(float x) const { return fabsf(x) < thrf; }
-  // exact digits through fresh primaries (the README's sticky-bit deposit)
+  // exact digits through fresh primaries (the SyclReproSum sticky-bit deposit)
   __device__ __forceinline__ void get(float x, int I, int64_t* a) const {
     float r = x;
 #pragma unroll

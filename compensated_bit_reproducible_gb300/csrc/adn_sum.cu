@@ -1,5 +1,5 @@
 // Binned sum: one read of the input, per-thread binned accumulation, exact
-// block merge, and a last-block grid merge + conversion (SyclReproSum README,
+// block merge, and a last-block grid merge + conversion (SyclReproSum,
 // "How It Works": deposit, renormalize, merge; the sum reads each input
 // element exactly once).  The result bits depend only on the multiset of
 // inputs, never on the grid, block size or scheduling.

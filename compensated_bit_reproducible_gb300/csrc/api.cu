@@ -1,6 +1,6 @@
 // C-ABI entry points (declared in include/repro.h).  Argument, capacity and
 // overlap checks run before any pointer is touched or memory allocated
-// ("SyclReproSum" README, "Accumulator capacity": the length error comes
+// ("SyclReproSum", "Accumulator capacity": the length error comes
 // before the pointer is inspected).  Temporary memory comes from the
 // stream-ordered allocator on the caller's stream.
 #include <cuda_runtime.h>
@@ -211,6 +211,8 @@ repro_status var_impl(const float* x, int64_t rows, int64_t cols, int axis, int 
   if (ddof < 0 || ddof >= n) return REPRO_ERR_INVALID_ARG;
   if (n > (1ll << 24)) return REPRO_ERR_INVALID_ARG;   // n must be exact in float32
   if (!x || !out || !aligned(x) || !aligned(out) || (mean && !aligned(mean))) return REPRO_ERR_INVALID_ARG;
+  repro_status st = validate_env(stream);
+  if (st != REPRO_OK) return st;
   CK(launch_var(x, rows, cols, axis, ddof, out, mean, twoterm, nullptr, stream));
   return REPRO_OK;
 }
@@ -219,6 +221,8 @@ template <typename T>
 repro_status compare_impl(const T* x, size_t n, int mode, T* result, cudaStream_t stream) {
   if ((n > 0 && (!x || !aligned(x))) || !result || !aligned(result)) return REPRO_ERR_INVALID_ARG;
   if (n > (1ull << 40)) return REPRO_ERR_CAPACITY;
+  repro_status st = validate_env(stream);
+  if (st != REPRO_OK) return st;
   Scratch ws;
   ws.s = stream;
   CK(cudaMallocAsync(&ws.p, compare_workspace_bytes<T>((int64_t)n, mode), stream));

@@ -1,6 +1,6 @@
 // Comparison summation modes ("Reduction order and compensation solve related
 // but different problems"; "Kahan's Summation Formula") and the environment
-// probe ("SyclReproSum" README, "Runtime environment validation").
+// probe ("SyclReproSum", "Runtime environment validation").
 #include <cuda_runtime.h>
 #include <cstdint>
 #include "launch.h"

@@ -1,7 +1,7 @@
 // Binned cumulative sum, K = 3 (the default fold count), float and double.
 //
 // Same tile structure as the general path (tile totals, their exclusive scan,
-// replay; "SyclReproSum" README, "How It Works", cumsum paragraph), with the
+// replay; "SyclReproSum", "How It Works", cumsum paragraph), with the
 // replay state kept in registers as its three fold sums F0, F1, F2 plus the
 // exact total T = F0 2^(2W) + F1 2^W + F2 in units of the finest grid.  Each
 // element adds its digits to the folds and their combination to T, so each

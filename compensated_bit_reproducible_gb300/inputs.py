@@ -4,7 +4,7 @@ This module only draws numbers: it holds none of the summation or variance
 arithmetic, so the CUDA path and the CPU oracle can both consume its arrays.
 Every generator is `numpy.random.default_rng(seed)` based and returns host
 numpy arrays; shapes, value distributions and structure follow the workloads
-the pages measure (the SyclReproSum README's 100M-element sums, the variance
+the pages measure (the SyclReproSum's 100M-element sums, the variance
 note's D1-D4 datasets, identical-value rows and [4096, 4096] speed array).
 """
 from __future__ import annotations
@@ -13,7 +13,7 @@ import numpy as np
 
 
 def quickstart_f64() -> np.ndarray:
-    """5 pairs (1e16, -1e16) then 10000 ones (SyclReproSum README, Quick Start)."""
+    """5 pairs (1e16, -1e16) then 10000 ones (SyclReproSum, Quick Start)."""
     return np.array([1e16, -1e16] * 5 + [1.0] * 10000, dtype=np.float64)
 
 

@@ -21,7 +21,7 @@
  *    on the input values (for sums: on the multiset; for cumulative sums: on
  *    the sequence), never on launch configuration, scheduling or stream.
  *
- * Sources: "SyclReproSum" README (sections "How It Works", "API Reference",
+ * Sources: "SyclReproSum" (sections "How It Works", "API Reference",
  * "Accumulator capacity", "Template Parameters", "Runtime environment
  * validation"); "Variance in float32 with a first-element shift, a local
  * centring and a compensated tree sum" (section 2); "Reduction order and
@@ -74,9 +74,11 @@ int repro_max_k_f64(void);
 /* ---- environment ("Runtime environment validation") --------------------- */
 /* Runs a probe kernel on the current device checking IEEE binary32/64
    layouts, round-to-nearest-even, unflushed subnormals, signed zero and
-   Inf/NaN arithmetic.  The result is cached per device; every sum and
-   cumulative sum calls it on first use.  Synchronous.  REPRO_ERR_ENV when a
-   check fails. */
+   Inf/NaN arithmetic.  The result is cached per device; every compute call
+   of this library calls it on first use.  Synchronous.  REPRO_ERR_ENV when a
+   check fails.  With the environment variable REPRO_FORCE_ENV_FAIL=1 every
+   validation fails with REPRO_ERR_ENV before any device work (a test hook
+   for the failure path). */
 repro_status repro_validate_environment(cudaStream_t stream);
 
 /* ---- binned sums ("How It Works": deposit, renormalize, merge) ---------- */
@@ -130,7 +132,8 @@ repro_status repro_cumsum_f64_ex(const double* in, double* out, size_t n, int K,
 repro_status repro_segsum_f32(const float* x, int64_t rows, int64_t cols, int axis, int K, float* out,
                               cudaStream_t stream);
 
-/* ---- float32 variance (variance note, section 2) ------------------------ */
+/* ---- float32 variance ("Variance in float32 with a first-element shift, a
+   local centring and a compensated tree sum", section 2) ------------------ */
 /* Per-slice variance of a row-major [rows, cols] float array along `axis`
    (1: each row, 0: each column), entirely in float32:
      y = x - x[0];  m = sum(y) / n;  d = y - m;
@@ -143,8 +146,9 @@ repro_status repro_segsum_f32(const float* x, int64_t rows, int64_t cols, int ax
 repro_status stable_var_f32(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out,
                             float* mean_out, cudaStream_t stream);
 
-/* ---- comparison modes (reductions page; Kahan's Summation Formula) ------ */
-/* Formula of reference for the variance (tf.nn.moments, variance note
+/* ---- comparison modes ("Reduction order and compensation solve related but
+   different problems"; "Kahan's Summation Formula") ---------------------- */
+/* Formula of reference for the variance (tf.nn.moments; variance page,
    section 1): m = mean(x); d = x - m; var = max(mean(d^2) - mean(d)^2, 0),
    mean(v) = RN(tree_sum(v) * RN(1/n)), same ddof rescale.  Stream-ordered. */
 repro_status twoterm_var_f32(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out,

@@ -1,6 +1,6 @@
 /*
  * Oracle: Ahrens-Demmel-Nguyen (ADN) binned summation, restated from the
- * "SyclReproSum" README.  TEST INFRASTRUCTURE ONLY (see oracle.h).
+ * "SyclReproSum".  TEST INFRASTRUCTURE ONLY (see oracle.h).
  *
  * Geometry ("How It Works", "Template Parameters", "Accumulator capacity"):
  *   bin width W = 40 (double) / 13 (float); at most nb = 52 / 21 bins, which
@@ -221,7 +221,7 @@ void orc_adn_state_closed_f32(const float* x, int64_t n, int K, int* I, int64_t*
 
 /* ------------------------------------------------------------------------
  * Floating-point primary form, one value at a time in input order, as the
- * README's "How It Works" describes it:
+ * "SyclReproSum" page's "How It Works" describes it:
  *  - each fold keeps a primary P whose ulp is the fold's grid unit, started
  *    at 1.5 * 2^e (ulp(P) = 2^(e - p + 1) = g), and a carry counter C;
  *  - Deposit: with the least significant bit of the remainder forced to 1

@@ -1,7 +1,7 @@
 /*
  * Oracle: exact sums.  TEST INFRASTRUCTURE ONLY (see oracle.h).
  * The exact sum of the inputs is the reference every binned result is held
- * to ("SyclReproSum" README, "Template Parameters": the binned error term is
+ * to ("SyclReproSum", "Template Parameters": the binned error term is
  * an absolute error against it).
  */
 #include "oracle.h"

@@ -3,7 +3,7 @@
  * TEST INFRASTRUCTURE ONLY (see oracle.h).
  *
  * The exact sum is the plain definition every binned result is measured
- * against ("SyclReproSum" README, "How It Works": the binned error term is an
+ * against ("SyclReproSum", "How It Works": the binned error term is an
  * absolute error against the exact sum).  Rounding follows IEEE 754
  * round-to-nearest-even, including subnormal results and overflow to Inf.
  */

@@ -8,7 +8,7 @@
  * restated from the pages it cites.
  *
  * Sources (by page title and section):
- *  - "SyclReproSum" README: "How It Works" (deposit / renormalize / merge,
+ *  - "SyclReproSum": "How It Works" (deposit / renormalize / merge,
  *    Inf/NaN rules, absorption threshold), "Accumulator capacity",
  *    "Template Parameters" (bin width W, max K, error term), "Quick Start".
  *  - "Variance in float32 with a first-element shift, a local centring and a

@@ -110,7 +110,7 @@ def tie_heavy(dt, n, seed, K=3):
 
 # --------------------------------------------------------------------- pins
 def test_quickstart_example(orc):
-    """SyclReproSum README, Quick Start: 1e16 pairs + 10000 ones."""
+    """SyclReproSum, Quick Start: 1e16 pairs + 10000 ones."""
     g = load_kv("quickstart.txt")
     x = inputs.quickstart_f64()
     assert x.size == 2 * int(g["pairs"]) + int(g["ones"])
