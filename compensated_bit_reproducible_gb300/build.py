@@ -17,7 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librepro_gb300.so")
-SOURCES = ["api.cu", "adn_sum.cu", "adn_cumsum.cu", "cumsum_k3.cu", "var.cu", "compare.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "adn_sum.cu", "sum_f64_fixed.cu", "adn_cumsum.cu", "cumsum_k3.cu", "var.cu", "compare.cu",
+           "noalloc.cu"]
 HEADERS = ["adn.cuh", "accum.cuh", "launch.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

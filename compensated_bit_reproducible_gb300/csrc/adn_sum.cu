@@ -129,9 +129,18 @@ __device__ void merge_partials_cg(const unsigned char* base, int np, int K, Stat
 }
 
 // Workspace: [0, 256) ticket counter (zero at launch); [256, ...) partials.
+// With a gate, the kernel runs only if *gate is nonzero (it is the fallback
+// of a faster path that decides on the device).
 template <typename T, int KT, int U>
 __global__ void __launch_bounds__(1024) adn_sum_kernel(const T* __restrict__ x, int64_t n, int K,
-                                                       unsigned char* __restrict__ ws, T* __restrict__ result) {
+                                                       unsigned char* __restrict__ ws, T* __restrict__ result,
+                                                       const unsigned* __restrict__ gate) {
+  if (gate) {
+    // launched as a programmatic dependent of the fast path: wait until that
+    // grid has completed and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (*gate == 0u) return;
+  }
   typedef typename AccOf<T, KT>::type Acc;
   constexpr int N = Acc::N;
   Acc acc;
@@ -209,30 +218,46 @@ __global__ void __launch_bounds__(256) segsum_cols_kernel(const float* __restric
 // ------------------------------------------------------------------ launch
 template <typename T, int KT>
 static cudaError_t launch_sum_k(const T* x, int64_t n, int K, unsigned char* ws, T* result, int grid, int block,
-                                cudaStream_t s) {
+                                const unsigned* gate, cudaStream_t s) {
   constexpr int U = 4;
-  adn_sum_kernel<T, KT, U><<<grid, block, 0, s>>>(x, n, K, ws, result);
-  return cudaGetLastError();
+  if (!gate) {
+    adn_sum_kernel<T, KT, U><<<grid, block, 0, s>>>(x, n, K, ws, result, gate);
+    return cudaGetLastError();
+  }
+  // gated fallback: programmatic dependent launch overlaps its launch with
+  // the tail of the preceding kernel on the stream
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, adn_sum_kernel<T, KT, U>, x, n, K, ws, result, gate);
 }
 
 template <typename T>
 cudaError_t launch_sum(const T* x, int64_t n, int K, unsigned char* ws, T* result, int grid, int block,
-                       cudaStream_t s) {
+                       cudaStream_t s, const unsigned* gate) {
   switch (K) {
-    case 2: return launch_sum_k<T, 2>(x, n, K, ws, result, grid, block, s);
-    case 3: return launch_sum_k<T, 3>(x, n, K, ws, result, grid, block, s);
-    case 4: return launch_sum_k<T, 4>(x, n, K, ws, result, grid, block, s);
-    case 5: return launch_sum_k<T, 5>(x, n, K, ws, result, grid, block, s);
-    case 6: return launch_sum_k<T, 6>(x, n, K, ws, result, grid, block, s);
-    case 7: return launch_sum_k<T, 7>(x, n, K, ws, result, grid, block, s);
-    case 8: return launch_sum_k<T, 8>(x, n, K, ws, result, grid, block, s);
-    default: return launch_sum_k<T, 0>(x, n, K, ws, result, grid, block, s);
+    case 2: return launch_sum_k<T, 2>(x, n, K, ws, result, grid, block, gate, s);
+    case 3: return launch_sum_k<T, 3>(x, n, K, ws, result, grid, block, gate, s);
+    case 4: return launch_sum_k<T, 4>(x, n, K, ws, result, grid, block, gate, s);
+    case 5: return launch_sum_k<T, 5>(x, n, K, ws, result, grid, block, gate, s);
+    case 6: return launch_sum_k<T, 6>(x, n, K, ws, result, grid, block, gate, s);
+    case 7: return launch_sum_k<T, 7>(x, n, K, ws, result, grid, block, gate, s);
+    case 8: return launch_sum_k<T, 8>(x, n, K, ws, result, grid, block, gate, s);
+    default: return launch_sum_k<T, 0>(x, n, K, ws, result, grid, block, gate, s);
   }
 }
 
-template cudaError_t launch_sum<float>(const float*, int64_t, int, unsigned char*, float*, int, int, cudaStream_t);
+template cudaError_t launch_sum<float>(const float*, int64_t, int, unsigned char*, float*, int, int, cudaStream_t,
+                                       const unsigned*);
 template cudaError_t launch_sum<double>(const double*, int64_t, int, unsigned char*, double*, int, int,
-                                        cudaStream_t);
+                                        cudaStream_t, const unsigned*);
 
 // Resident blocks per SM of the sum kernel for this K and block size (one
 // wave of blocks covers the GPU; more would leave a partial second wave).

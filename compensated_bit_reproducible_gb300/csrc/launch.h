@@ -9,10 +9,18 @@ namespace repro {
 // binned sum
 template <typename T>
 cudaError_t launch_sum(const T* x, int64_t n, int K, unsigned char* ws, T* result, int grid, int block,
-                       cudaStream_t s);
+                       cudaStream_t s, const unsigned* gate = nullptr);
 size_t sum_workspace_bytes(int K, int grid);
 template <typename T>
 int sum_blocks_per_sm(int K, int block);
+// double sum at a sampled fixed index (K = 2, 3): blocks per GPU for this
+// block size (0: not available), workspace after the control words, launch.
+// ctl points at 16 zeroed bytes; ctl[2] becomes nonzero when the general
+// kernel must compute the result (pass it as that kernel's gate).
+int sum_f64_fixed_grid(int K, int block, int sms);
+size_t sum_f64_fixed_workspace_bytes(int grid);
+cudaError_t launch_sum_f64_fixed(const double* x, int64_t n, int K, unsigned* ctl, unsigned char* parts,
+                                 double* result, int grid, int block, cudaStream_t s);
 cudaError_t launch_segsum(const float* x, int64_t rows, int64_t cols, int axis, int K, float* out, int grid,
                           int block, cudaStream_t s);
 
