@@ -8,6 +8,7 @@
 // prefix is one rounding of T; T is rebuilt from the folds only when a larger
 // value raises the bin index (the finest folds drop).
 #include "accum.cuh"
+#include "fixed_index.cuh"
 #include "launch.h"
 #include <type_traits>
 
@@ -416,18 +417,25 @@ __device__ __forceinline__ Run3<T> run_zero(bool withT) {
   return r;
 }
 
+// Gate of the fallback launches: run only if *gate is nonzero; launched as
+// programmatic dependents, they first wait for the preceding grid.
+__device__ __forceinline__ bool c3_gated_off(const unsigned* gate) {
+  if (!gate) return false;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  return *gate == 0u;
+}
+
 // ------------------------------------------------------------------ A
 // Per-warp totals: warp w of a tile covers its elements [w * 512, w * 512 +
 // 512); lane l takes every 32nd element (coalesced).  Totals are order free.
 template <typename T>
-__global__ void __launch_bounds__(C3_BLOCK) c3_warp_totals(const T* __restrict__ in, int64_t n,
-                                                           unsigned char* __restrict__ wtot) {
+__device__ __forceinline__ void c3_warp_total_tile(const T* __restrict__ in, int64_t n, int64_t tile,
+                                                   unsigned char* __restrict__ wtot) {
   typedef typename AccOf<T, 3>::type Acc;
   typedef typename std::conditional<sizeof(T) == 4, float4, double2>::type V;
   constexpr int VW = 16 / sizeof(T);
   constexpr int PER = C3_TILE / C3_WARPS;          // elements per warp
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t tile = blockIdx.x;
   const int64_t base = tile * C3_TILE + (int64_t)warp * PER;
   Acc acc;
   acc.init(3);
@@ -468,14 +476,22 @@ __global__ void __launch_bounds__(C3_BLOCK) c3_warp_totals(const T* __restrict__
   if (lane == 0) s3_store(s, wtot + (size_t)(tile * C3_WARPS + warp) * C3_STATE);
 }
 
+template <typename T>
+__global__ void __launch_bounds__(C3_BLOCK) c3_warp_totals(const T* __restrict__ in, int64_t n, int64_t ntiles,
+                                                           unsigned char* __restrict__ wtot, const unsigned* gate) {
+  if (c3_gated_off(gate)) return;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) c3_warp_total_tile<T>(in, n, tile, wtot);
+}
+
 // ------------------------------------------------------------------ B
 // B1: one thread per tile (1024 tiles per block): tile total = merge of its
 // warp totals; exclusive scan within the block -> local tile prefix; block
 // total.  B2: one block scans the block totals exclusively.
 __global__ void __launch_bounds__(1024) c3_scan_tiles(const unsigned char* __restrict__ wtot, int64_t ntiles,
                                                       int I0, unsigned char* __restrict__ tloc,
-                                                      unsigned char* __restrict__ btot) {
+                                                      unsigned char* __restrict__ btot, const unsigned* gate) {
   __shared__ S3 sm[32];
+  if (c3_gated_off(gate)) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   S3 tot = s3_zero(I0);
@@ -500,8 +516,9 @@ __global__ void __launch_bounds__(1024) c3_scan_tiles(const unsigned char* __res
 }
 
 __global__ void __launch_bounds__(1024) c3_scan_blocks(unsigned char* __restrict__ btot, int64_t nb, int I0,
-                                                       unsigned char* __restrict__ bpre) {
+                                                       unsigned char* __restrict__ bpre, const unsigned* gate) {
   __shared__ S3 sm[32];
+  if (c3_gated_off(gate)) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // nb <= 1024 * per; thread t handles [t * per, ...)
   int64_t per = (nb + blockDim.x - 1) / blockDim.x;
@@ -524,14 +541,11 @@ __global__ void __launch_bounds__(1024) c3_scan_blocks(unsigned char* __restrict
 }
 
 // ------------------------------------------------------------------ C
+// Replay of one tile from its incoming state (prefix of everything before
+// the tile).  sm: C3_TILE + C3_TILE / C3_ITEMS elements, wsm: C3_WARPS states.
 template <typename T>
-__global__ void __launch_bounds__(C3_BLOCK) c3_replay(const T* in, T* out, int64_t n,
-                                                      const unsigned char* __restrict__ tloc,
-                                                      const unsigned char* __restrict__ bpre) {
-  __shared__ T sm[C3_TILE + C3_TILE / C3_ITEMS];
-  __shared__ S3 wsm[C3_WARPS];
+__device__ void c3_replay_tile(const T* in, T* out, int64_t n, int64_t tile, S3 st, T* sm, S3* wsm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t tile = blockIdx.x;
   const int64_t base = tile * C3_TILE;
   const int cnt = (int)min((int64_t)C3_TILE, n - base);
   for (int i = threadIdx.x; i < cnt; i += blockDim.x) sm[i + i / C3_ITEMS] = in[base + i];
@@ -549,8 +563,6 @@ __global__ void __launch_bounds__(C3_BLOCK) c3_replay(const T* in, T* out, int64
   S3 inc = s3_warp_inclusive(mine);
   if (lane == 31) wsm[warp] = inc;
   __syncthreads();
-  S3 st = s3_load(bpre + (size_t)(tile / 1024) * C3_STATE);
-  s3_merge(st, s3_load(tloc + (size_t)tile * C3_STATE));
   for (int w = 0; w < warp; ++w) s3_merge(st, wsm[w]);
   S3 exc = s3_shfl_up(inc, 1);
   if (lane == 0) exc = s3_zero(I0);
@@ -568,13 +580,399 @@ __global__ void __launch_bounds__(C3_BLOCK) c3_replay(const T* in, T* out, int64
   }
   __syncthreads();
   for (int i = threadIdx.x; i < cnt; i += blockDim.x) out[base + i] = sm[i + i / C3_ITEMS];
+  __syncthreads();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(C3_BLOCK) c3_replay(const T* in, T* out, int64_t n, int64_t ntiles,
+                                                      const unsigned char* __restrict__ tloc,
+                                                      const unsigned char* __restrict__ bpre,
+                                                      const unsigned* gate) {
+  __shared__ T sm[C3_TILE + C3_TILE / C3_ITEMS];
+  __shared__ S3 wsm[C3_WARPS];
+  if (c3_gated_off(gate)) return;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    S3 st = s3_load(bpre + (size_t)(tile / 1024) * C3_STATE);
+    s3_merge(st, s3_load(tloc + (size_t)tile * C3_STATE));
+    c3_replay_tile<T>(in, out, n, tile, st, sm, wsm);
+  }
+}
+
+
+// ================================================ fixed-index fast path (K = 3)
+// See fixed_index.cuh: with the index L guessed from a sample and checked,
+// every prefix from the first element of bin L on (position i*) has index L,
+// so its value is the correct rounding of sum_{j <= i} R_j g_f, R_j the
+// single rounding of x_j at g_f.  Positions before i* (a finer prefix index)
+// exist only at the start; when they all lie in the first tile, that tile is
+// replayed with the per-fold state above.  Otherwise (i* beyond the first
+// tile, a wrong guess, Inf/NaN, or an index too fine) the general kernels,
+// launched gated after the fast ones, compute everything.
+//
+// Layout: tiles of C3_TILE elements; thread t of a block owns elements
+// [16 t, 16 t + 16) of a tile.  Pass 1 (totals) writes, per tile, each
+// thread's exclusive prefix within the tile and the tile total; pass 2 scans
+// the tile totals; pass 3 (replay) starts each thread from tile prefix +
+// thread prefix and converts after every element.
+
+struct CsCtl {                 // in the zeroed workspace header
+  unsigned fail;               // guess failed / Inf, NaN / index too fine
+  unsigned general;            // set by the scan: the general path runs
+  int L;                       // the guessed index (written by block 0)
+  unsigned exact0;             // set by the scan: the first tile is replayed per fold
+  unsigned long long istar;    // max over elements of bin L of (2^63 - 1 - position)
+  unsigned ticket;             // finished blocks of the scan
+};
+
+template <typename T> struct CsTraits;
+template <> struct CsTraits<float> {
+  static constexpr int MAX_BETA_F = -124;   // g_f / 2 above every forced-hidden-bit value
+};
+template <> struct CsTraits<double> {
+  static constexpr int MAX_BETA_F = -1019;
+};
+
+__device__ __forceinline__ fx::I192 i192_from_i64(int64_t v) {
+  return fx::I192{(uint64_t)v, (uint64_t)(v >> 63), (uint64_t)(v >> 63)};
+}
+__device__ __forceinline__ fx::I192 i192_shfl_up(fx::I192 v, int d) {
+  fx::I192 r;
+  r.w0 = __shfl_up_sync(0xffffffffu, v.w0, d);
+  r.w1 = __shfl_up_sync(0xffffffffu, v.w1, d);
+  r.w2 = __shfl_up_sync(0xffffffffu, v.w2, d);
+  return r;
+}
+// Warp sums of signed 192-bit values (every lane gets the total).
+__device__ __forceinline__ fx::I192 i192_warp_sum(fx::I192 v) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) v = fx::i192_add(v, fx::i192_shfl_xor(v, m));
+  return v;
+}
+// Exclusive warp scan; *total gets the warp sum.
+__device__ __forceinline__ fx::I192 i192_warp_exclusive(fx::I192 v, fx::I192* total) {
+  const int lane = threadIdx.x & 31;
+  fx::I192 inc = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    fx::I192 o = i192_shfl_up(inc, d);
+    if (lane >= d) inc = fx::i192_add(inc, o);
+  }
+  total->w0 = __shfl_sync(0xffffffffu, inc.w0, 31);
+  total->w1 = __shfl_sync(0xffffffffu, inc.w1, 31);
+  total->w2 = __shfl_sync(0xffffffffu, inc.w2, 31);
+  fx::I192 neg{~v.w0, ~v.w1, ~v.w2};   // inc - v
+  return fx::i192_add(fx::i192_add(inc, neg), fx::I192{1, 0, 0});
+}
+
+constexpr int CF_CHUNK = 512;    // elements per warp chunk: lane l owns [16 l, 16 l + 16)
+constexpr int CF_PAD = CF_CHUNK + CF_CHUNK / 16;
+constexpr int CF_WARPS = C3_BLOCK / 32;
+
+// Signed rounded value of x at g_f as I192 (double: one-hot shift; float:
+// 64-bit).
+template <typename T>
+__device__ __forceinline__ fx::I192 cf_round(T v, const fx::FxConst& kc, int tsh24) {
+  if constexpr (sizeof(T) == 8) {
+    const uint32_t hi = (uint32_t)__double2hiint(v);
+    uint64_t rl, rh;
+    fx::round_f64(hi, (uint32_t)__double2loint(v), kc, rl, rh);
+    const uint64_t sgn = (uint64_t)((int64_t)(int32_t)hi >> 31);
+    return fx::i192_add(fx::I192{rl ^ sgn, rh ^ sgn, sgn}, fx::I192{sgn & 1u, 0, 0});
+  } else {
+    const uint32_t bits = __float_as_uint(v);
+    const int64_t r = (int64_t)fx::round_f32(bits, tsh24);
+    return i192_from_i64((bits >> 31) ? -r : r);
+  }
+}
+
+// Coalesced copy of a chunk (cnt elements at g) into the warp's padded buffer.
+template <typename T>
+__device__ __forceinline__ void cf_stage(T* buf, const T* g, int cnt, int lane) {
+  if (cnt == CF_CHUNK && ((((uintptr_t)g) & 15) == 0)) {
+    typedef typename std::conditional<sizeof(T) == 4, float4, double2>::type V;
+    constexpr int VW = 16 / sizeof(T);
+    const V* p = (const V*)g;
+#pragma unroll
+    for (int k = 0; k < CF_CHUNK / VW / 32; ++k) {
+      const int i = (k * 32 + lane) * VW;
+      V v = __ldcs(p + k * 32 + lane);
+      if constexpr (sizeof(T) == 8) {
+        buf[i + i / 16] = v.x;
+        buf[i + 1 + (i + 1) / 16] = v.y;
+      } else {
+        buf[i + i / 16] = v.x;
+        buf[i + 1 + (i + 1) / 16] = v.y;
+        buf[i + 2 + (i + 2) / 16] = v.z;
+        buf[i + 3 + (i + 3) / 16] = v.w;
+      }
+    }
+  } else {
+    for (int i = lane; i < cnt; i += 32) buf[i + i / 16] = g[i];
+  }
+}
+
+// Pass 1.  Persistent blocks; each warp takes whole chunks: staged in shared
+// memory, lane l sums its 16 contiguous elements, an exclusive warp scan
+// gives each lane's prefix within the chunk (stored) and the chunk total.
+template <typename T>
+__global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, int64_t n, int64_t nch,
+                                                      uint32_t one, CsCtl* ctl, unsigned char* __restrict__ lanep,
+                                                      fx::I192* __restrict__ ctot) {
+  typedef Geom<T> G;
+  __shared__ T sm[CF_WARPS * CF_PAD];
+  __shared__ unsigned s_emax;
+  int eb_max;
+  const int L = fx::guess_index<T>(in, n, 3, &s_emax, &eb_max);
+  const int bf = beta<T>(L + 2);
+  const bool usable = bf >= CsTraits<T>::MAX_BETA_F && eb_max < (sizeof(T) == 8 ? 0x7FF : 0xFF);
+  if (blockIdx.x == 0 && threadIdx.x == 0) ctl->L = L;
+  if (!usable) {
+    if (threadIdx.x == 0) atomicOr(&ctl->fail, 1u);
+    return;
+  }
+  const int eb_top = fx::bin_top_exponent<T>(L);
+  const int eb_bot = G::BIAS + beta<T>(L + 1) + G::W - 1;   // bottom of bin L
+  const fx::FxConst kc = fx::make_const(bf, one);
+  const int tsh24 = -150 - bf + 24;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  T* buf = sm + warp * CF_PAD;
+  int ebmax = 0;                       // largest exponent field seen
+  int64_t first = INT64_MAX;           // first position of bin L seen by this thread
+  const int64_t gw = (int64_t)blockIdx.x * CF_WARPS + warp, GW = (int64_t)gridDim.x * CF_WARPS;
+  for (int64_t ch = gw; ch < nch; ch += GW) {
+    const int64_t c0 = ch * CF_CHUNK;
+    const int cnt = (int)min((int64_t)CF_CHUNK, n - c0);
+    cf_stage<T>(buf, in + c0, cnt, lane);
+    __syncwarp();
+    const int b = lane * 16, sb = b + lane;
+    fx::I192 own{0, 0, 0};
+    int64_t own32 = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const T v = b + i < cnt ? buf[sb + i] : (T)0;
+      uint32_t hi;
+      if constexpr (sizeof(T) == 8) hi = (uint32_t)__double2hiint(v);
+      else hi = __float_as_uint(v);
+      const int eb = (int)((hi << 1) >> (sizeof(T) == 8 ? 21 : 24));
+      ebmax = max(ebmax, eb);
+      if (eb >= eb_bot && first == INT64_MAX) first = c0 + b + i;
+      if constexpr (sizeof(T) == 8) own = fx::i192_add(own, cf_round<T>(v, kc, tsh24));
+      else {
+        const int64_t r = (int64_t)fx::round_f32(hi, tsh24);
+        own32 += (hi >> 31) ? -r : r;
+      }
+    }
+    if constexpr (sizeof(T) == 4) own = i192_from_i64(own32);
+    fx::I192 tot;
+    const fx::I192 exc = i192_warp_exclusive(own, &tot);
+    const size_t li = (size_t)ch * 32 + lane;
+    if constexpr (sizeof(T) == 8) {
+      const size_t plane = (size_t)nch * 32;
+      uint64_t* lp = (uint64_t*)lanep;
+      lp[li] = exc.w0;
+      lp[plane + li] = exc.w1;
+      lp[2 * plane + li] = exc.w2;
+    } else {
+      ((int64_t*)lanep)[li] = (int64_t)exc.w0;   // |prefix| < 512 2^38
+    }
+    if (lane == 0) ctot[ch] = tot;
+    __syncwarp();
+  }
+  const int bad = __syncthreads_or(ebmax > eb_top);
+  int64_t f = first;
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) f = min(f, (int64_t)__shfl_xor_sync(0xffffffffu, (long long)f, m));
+  if (lane == 0 && f != INT64_MAX) atomicMax(&ctl->istar, 0x7FFFFFFFFFFFFFFFull - (unsigned long long)f);
+  if (threadIdx.x == 0 && bad) atomicOr(&ctl->fail, 1u);
+}
+
+// Pass 2: exclusive scan of the chunk totals.  Block b scans chunks
+// [1024 b, 1024 b + 1024) into lpre; the last block to finish scans the
+// block totals into bpre and decides the path.  Prefix of chunk c:
+// bpre[c >> 10] + lpre[c].
+__global__ void __launch_bounds__(1024) cf_scan(const fx::I192* __restrict__ ctot, int64_t nch, CsCtl* ctl,
+                                                fx::I192* __restrict__ lpre, fx::I192* __restrict__ btot,
+                                                fx::I192* __restrict__ bpre) {
+  __shared__ fx::I192 sm[32];
+  __shared__ bool last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t ci = (int64_t)blockIdx.x * 1024 + threadIdx.x;
+  fx::I192 v = ci < nch ? ctot[ci] : fx::I192{0, 0, 0};
+  fx::I192 wt;
+  fx::I192 exc = i192_warp_exclusive(v, &wt);
+  if (lane == 0) sm[warp] = wt;
+  __syncthreads();
+  fx::I192 base{0, 0, 0}, all{0, 0, 0};
+  for (int w = 0; w < 32; ++w) {
+    if (w < warp) base = fx::i192_add(base, sm[w]);
+    all = fx::i192_add(all, sm[w]);
+  }
+  if (ci < nch) lpre[ci] = fx::i192_add(base, exc);
+  if (threadIdx.x == 0) {
+    btot[blockIdx.x] = all;
+    __threadfence();
+    last = atomicAdd(&ctl->ticket, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const int64_t nb = gridDim.x;
+  const int64_t per = (nb + 1023) / 1024;
+  const int64_t b0 = (int64_t)threadIdx.x * per, b1 = min(nb, b0 + per);
+  fx::I192 agg{0, 0, 0};
+  for (int64_t i = b0; i < b1; ++i) {
+    const fx::I192* q = btot + i;
+    agg = fx::i192_add(agg, fx::I192{__ldcg(&q->w0), __ldcg(&q->w1), __ldcg(&q->w2)});
+  }
+  fx::I192 exc2 = i192_warp_exclusive(agg, &wt);
+  __syncthreads();
+  if (lane == 0) sm[warp] = wt;
+  __syncthreads();
+  fx::I192 run{0, 0, 0};
+  for (int w = 0; w < warp; ++w) run = fx::i192_add(run, sm[w]);
+  run = fx::i192_add(run, exc2);
+  for (int64_t i = b0; i < b1; ++i) {
+    bpre[i] = run;
+    const fx::I192* q = btot + i;
+    run = fx::i192_add(run, fx::I192{__ldcg(&q->w0), __ldcg(&q->w1), __ldcg(&q->w2)});
+  }
+  if (threadIdx.x == 0) {
+    const unsigned long long code = ctl->istar;
+    const int64_t istar = code ? (int64_t)(0x7FFFFFFFFFFFFFFFull - code) : INT64_MAX;
+    ctl->general = (ctl->fail != 0u || istar >= (int64_t)C3_TILE) ? 1u : 0u;
+    ctl->exact0 = (istar > 0) ? 1u : 0u;   // the first tile needs the per-fold replay
+  }
+}
+
+// Pass 3.  Each warp replays whole chunks staged in shared memory (coalesced
+// global traffic); lane l starts from chunk prefix + its lane prefix and
+// converts after every one of its 16 elements.
+template <typename T>
+__global__ void __launch_bounds__(C3_BLOCK) cf_replay(const T* in, T* out, int64_t n, int64_t nch, uint32_t one,
+                                                      const CsCtl* ctl, const unsigned char* __restrict__ lanep,
+                                                      const fx::I192* __restrict__ lpre,
+                                                      const fx::I192* __restrict__ bpre) {
+  __shared__ T sm[C3_TILE + C3_TILE / C3_ITEMS];   // 8 warp buffers, or one tile
+  __shared__ S3 wsm[C3_WARPS];
+  if (ctl->general) return;
+  const int L = ctl->L;
+  const bool exact0 = ctl->exact0 != 0u;
+  const int bf = beta<T>(L + 2);
+  const fx::FxConst kc = fx::make_const(bf, one);
+  const int tsh24 = -150 - bf + 24;
+  if (blockIdx.x == 0 && exact0) c3_replay_tile<T>(in, out, n, 0, s3_zero(Geom<T>::NB - 3), sm, wsm);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  T* buf = sm + warp * CF_PAD;
+  const int64_t gw = (int64_t)blockIdx.x * CF_WARPS + warp, GW = (int64_t)gridDim.x * CF_WARPS;
+  const int64_t ch_first = exact0 ? C3_TILE / CF_CHUNK : 0;
+  int64_t ch = gw;
+  while (ch < ch_first) ch += GW;
+  for (; ch < nch; ch += GW) {
+    const int64_t c0 = ch * CF_CHUNK;
+    const int cnt = (int)min((int64_t)CF_CHUNK, n - c0);
+    cf_stage<T>(buf, in + c0, cnt, lane);
+    const size_t li = (size_t)ch * 32 + lane;
+    fx::I192 t = fx::i192_add(bpre[ch >> 10], lpre[ch]);
+    if constexpr (sizeof(T) == 8) {
+      const size_t plane = (size_t)nch * 32;
+      const uint64_t* lp = (const uint64_t*)lanep;
+      t = fx::i192_add(t, fx::I192{lp[li], lp[plane + li], lp[2 * plane + li]});
+    } else {
+      t = fx::i192_add(t, i192_from_i64(((const int64_t*)lanep)[li]));
+    }
+    __syncwarp();
+    const int b = lane * 16, sb = b + lane;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (b + i < cnt) {
+        const T v = buf[sb + i];
+        t = fx::i192_add(t, cf_round<T>(v, kc, tsh24));
+        if constexpr (sizeof(T) == 8) buf[sb + i] = round_t192_d((int64_t)t.w2, t.w1, t.w0, bf);
+        else buf[sb + i] = round_t128_f((int64_t)t.w1, t.w0, bf);
+      }
+    }
+    __syncwarp();
+    T* g = out + c0;
+    if (cnt == CF_CHUNK && ((((uintptr_t)g) & 15) == 0)) {
+      typedef typename std::conditional<sizeof(T) == 4, float4, double2>::type V;
+      constexpr int VW = 16 / sizeof(T);
+#pragma unroll
+      for (int k = 0; k < CF_CHUNK / VW / 32; ++k) {
+        const int i = (k * 32 + lane) * VW;
+        V v;
+        if constexpr (sizeof(T) == 8) {
+          v.x = buf[i + i / 16];
+          v.y = buf[i + 1 + (i + 1) / 16];
+        } else {
+          v.x = buf[i + i / 16];
+          v.y = buf[i + 1 + (i + 1) / 16];
+          v.z = buf[i + 2 + (i + 2) / 16];
+          v.w = buf[i + 3 + (i + 3) / 16];
+        }
+        ((V*)g)[k * 32 + lane] = v;
+      }
+    } else {
+      for (int i = lane; i < cnt; i += 32) g[i] = buf[i + i / 16];
+    }
+    __syncwarp();
+  }
+}
+
+// Below this many elements the fixed launch costs of the fast path (four
+// kernels and the idle fallback) outweigh its gain.
+constexpr int64_t CF_MIN_N = 1 << 17;
+
+static int cf_sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 1;
+  }
+  if (!cached[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+      cudaGetLastError();
+      v = 1;
+    }
+    cached[dev] = v;
+  }
+  return cached[dev];
+}
+
+template <typename K, typename... A>
+static cudaError_t launch_gated(K kernel, int64_t grid, int block, size_t smem, cudaStream_t s, bool pdl, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <typename T>
+static size_t c3_general_bytes(int64_t n) {
+  int64_t nt = (n + C3_TILE - 1) / C3_TILE;
+  int64_t nb = (nt + 1023) / 1024;
+  size_t b = ((size_t)nt * C3_WARPS + (size_t)nt + 2 * (size_t)nb) * C3_STATE + 256;
+  return (b + 255) & ~(size_t)255;
+}
+
+template <typename T>
+static size_t cf_bytes(int64_t n) {
+  int64_t nc = (n + CF_CHUNK - 1) / CF_CHUNK;
+  int64_t nb = (nc + 1023) / 1024;
+  return 256 + (size_t)nc * 32 * (sizeof(T) == 8 ? 24 : 8) + ((size_t)2 * nc + 2 * (size_t)nb) * sizeof(fx::I192);
 }
 
 template <typename T>
 size_t cumsum_k3_workspace_bytes(int64_t n) {
-  int64_t nt = (n + C3_TILE - 1) / C3_TILE;
-  int64_t nb = (nt + 1023) / 1024;
-  return ((size_t)nt * C3_WARPS + (size_t)nt + 2 * (size_t)nb) * C3_STATE + 256;
+  return c3_general_bytes<T>(n) + (n >= CF_MIN_N ? cf_bytes<T>(n) : 0);
 }
 
 template <typename T>
@@ -586,11 +984,45 @@ cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, 
   unsigned char* btot = tloc + (size_t)nt * C3_STATE;
   unsigned char* bpre = btot + (size_t)nb * C3_STATE;
   const int I0 = Geom<T>::NB - 3;
-  c3_warp_totals<T><<<(unsigned)nt, C3_BLOCK, 0, s>>>(in, n, wtot);
-  c3_scan_tiles<<<(unsigned)nb, 1024, 0, s>>>(wtot, nt, I0, tloc, btot);
-  c3_scan_blocks<<<1, 1024, 0, s>>>(btot, nb, I0, bpre);
-  c3_replay<T><<<(unsigned)nt, C3_BLOCK, 0, s>>>(in, out, n, tloc, bpre);
-  return cudaGetLastError();
+  const unsigned* gate = nullptr;
+  int64_t ggrid = nt;
+  cudaError_t e;
+  if (n >= CF_MIN_N) {
+    // fixed-index fast path; the general kernels below become its gated fallback
+    unsigned char* f = ws + c3_general_bytes<T>(n);
+    CsCtl* ctl = (CsCtl*)f;
+    const int64_t nc = (n + CF_CHUNK - 1) / CF_CHUNK;
+    const int64_t ncb = (nc + 1023) / 1024;
+    unsigned char* lanep = f + 256;
+    fx::I192* ctot = (fx::I192*)(lanep + (size_t)nc * 32 * (sizeof(T) == 8 ? 24 : 8));
+    fx::I192* lpre = ctot + nc;
+    fx::I192* btot = lpre + nc;
+    fx::I192* bpre = btot + ncb;
+    if ((e = cudaMemsetAsync(ctl, 0, 256, s)) != cudaSuccess) return e;
+    int bt = 0, br = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bt, cf_totals<T>, C3_BLOCK, 0) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&br, cf_replay<T>, C3_BLOCK, 0) != cudaSuccess) {
+      cudaGetLastError();
+      bt = br = 1;
+    }
+    const int64_t sms = cf_sm_count();
+    const int64_t wb = (nc + CF_WARPS - 1) / CF_WARPS;   // blocks that have a chunk
+    const int64_t gt = max((int64_t)1, min(wb, sms * max(bt, 1))), gr = max((int64_t)1, min(wb, sms * max(br, 1)));
+    cf_totals<T><<<(unsigned)gt, C3_BLOCK, 0, s>>>(in, n, nc, 1u, ctl, lanep, ctot);
+    cf_scan<<<(unsigned)ncb, 1024, 0, s>>>(ctot, nc, ctl, lpre, btot, bpre);
+    cf_replay<T><<<(unsigned)gr, C3_BLOCK, 0, s>>>(in, out, n, nc, 1u, ctl, lanep, lpre, bpre);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    gate = &ctl->general;
+    ggrid = min(nt, sms);
+  }
+  const bool pdl = gate != nullptr;
+  if ((e = launch_gated(c3_warp_totals<T>, ggrid, C3_BLOCK, 0, s, pdl, in, n, nt, wtot, gate)) != cudaSuccess) return e;
+  if ((e = launch_gated(c3_scan_tiles, nb, 1024, 0, s, pdl, (const unsigned char*)wtot, nt, I0, tloc, btot, gate)) !=
+      cudaSuccess)
+    return e;
+  if ((e = launch_gated(c3_scan_blocks, 1, 1024, 0, s, pdl, btot, nb, I0, bpre, gate)) != cudaSuccess) return e;
+  return launch_gated(c3_replay<T>, ggrid, C3_BLOCK, 0, s, pdl, in, out, n, nt, (const unsigned char*)tloc,
+                      (const unsigned char*)bpre, gate);
 }
 
 template size_t cumsum_k3_workspace_bytes<float>(int64_t);

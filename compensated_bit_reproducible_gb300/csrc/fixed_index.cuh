@@ -1,0 +1,258 @@
+// Binned sums at an index fixed before the deposit: device helpers shared
+// by the double sum and the K = 3 cumulative sums.
+//
+// The binned result is a function of the multiset alone: it is the correct
+// rounding of sum_i C_I(x_i), where I is the bin index of max|x| (capped at
+// nb - K) and C_I(x) is x after the chained round-half-away decomposition on
+// the grids g_I .. g_{I+K-1} with the last remainder dropped
+// ("SyclReproSum", "How It Works": one-pass index updates give the same
+// folds as depositing at the final index from the start).  The per-fold
+// split only matters for raising the index in flight; summed over the folds,
+// C_I(x) is x rounded to a multiple of the finest grid g_f = g_{I+K-1}, to
+// nearest, with exact ties broken by the chained rule: away from zero unless
+// the rounding bit of fold K-2 (g_f 2^(W-1)) is set, in which case toward
+// zero.  So when I is known, a deposit is one rounding of |x| at g_f and an
+// exact integer addition.
+//
+// The index is guessed from a fixed sample of the input: a subset's maximum
+// lies in the same bin as the true maximum or in a finer one, so a guess is
+// either right or some element lies above its bin -- which the kernels
+// check, falling back to the general one-pass path.
+//
+// Double rounding.  With P' = |x| 2^64 / g_f = M 2^u (M the 53-bit
+// significand), the rounded value is floor((P' + 2^63 - b) / 2^64), b the
+// tie bit above (bit 103 of P').  Adding h - b to M (h = 2^(63-u)) and
+// shifting by u gives P'' whose bits at and above 64 are exactly that value.
+#pragma once
+#include "adn.cuh"
+
+namespace repro {
+namespace fx {
+
+constexpr int SAMPLE = 256;   // elements sampled for the index guess
+constexpr int STRIDE = 7;     // sum cells per sign: 32-bit word positions 0..6 of P''
+constexpr int CELLS = 14;     // both signs
+
+__device__ __forceinline__ uint32_t shl_clamp32(uint32_t v, int s) {   // s outside [0, 31] gives 0
+  uint32_t r;
+  asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(s));
+  return r;
+}
+__device__ __forceinline__ uint32_t funnel_l(uint32_t lo, uint32_t hi, uint32_t n) {   // (hi:lo << n%32).hi
+  uint32_t r;
+  asm("shf.l.wrap.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(lo), "r"(hi), "r"(n));
+  return r;
+}
+// a * b + c kept as multiply-adds: with b a kernel argument equal to 1 the
+// compiler cannot turn them into integer-ALU additions (the ALU pipe is the
+// one this kernel saturates; the multiply-add pipe has room).
+__device__ __forceinline__ uint32_t mad32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t madw(uint32_t a, uint32_t b, uint64_t c) {
+  uint64_t r;
+  asm("mad.wide.u32 %0, %1, %2, %3;" : "=l"(r) : "r"(a), "r"(b), "l"(c));
+  return r;
+}
+
+struct FxConst {
+  uint32_t one, negone, c63, c31, c256, c7, Cp;
+};
+
+// One deposit.  A: 64-bit cells (stride NT), B: 32-bit cells; sign s word k
+// at cell k + 7 s (B: k - 2 + 7 s, only k >= 2 is used).
+__device__ __forceinline__ void fx_deposit(uint32_t hi, uint32_t lo, const FxConst& k, uint64_t* A, uint32_t* B,
+                                           uint32_t NT, int& umax) {
+  uint32_t eb = mad32(hi, k.one + k.one, 0u) >> 21;          // biased exponent
+  int us = (int)mad32(eb, k.one, k.Cp);                       // shift of M
+  umax = max(umax, us);
+  uint32_t u = (uint32_t)max(us, 0);   // tiny values: their words stay below position 2
+  uint32_t c = min(u >> 5, 5u);        // beyond the bin (flagged through umax): kept in bounds
+  uint32_t mh = (hi & 0xFFFFFu) | 0x100000u;
+  uint32_t hl = shl_clamp32(1u, (int)mad32(u, k.negone, k.c63));
+  uint32_t hh = shl_clamp32(1u, (int)mad32(u, k.negone, k.c31));
+  uint32_t b = min(mh & mad32(hl, k.c256, 0u), 1u);          // bit 103 of P': rounding bit of fold K-2
+  uint64_t Mp = ((((uint64_t)mh) << 32) | lo) + ((((uint64_t)hh) << 32) | hl) - (uint64_t)b;
+  uint32_t lo2 = (uint32_t)Mp, mh2 = (uint32_t)(Mp >> 32);
+  uint32_t w0 = funnel_l(0u, lo2, u);
+  uint32_t w1 = funnel_l(lo2, mh2, u);
+  uint32_t w2 = funnel_l(mh2, 0u, u);
+  uint32_t off = mad32(mad32(hi >> 31, k.c7, c), NT, 0u);
+  uint64_t* p = A + off;
+  uint32_t* pb = B + off;
+  p[0] = madw(w0, k.one, p[0]);
+  p[NT] = madw(w1, k.one, p[NT]);
+  pb[0] = mad32(w2, k.one, pb[0]);
+}
+
+__device__ __forceinline__ void fx_fold(uint64_t* A, uint32_t* B, uint32_t NT) {
+#pragma unroll
+  for (int s = 0; s < 2; ++s)
+#pragma unroll
+    for (int w = 2; w < STRIDE; ++w) {
+      A[(w + STRIDE * s) * NT] += B[(w - 2 + STRIDE * s) * NT];
+      B[(w - 2 + STRIDE * s) * NT] = 0;
+    }
+}
+
+// Signed 192-bit integer.
+struct I192 {
+  uint64_t w0, w1, w2;
+};
+__device__ __forceinline__ I192 i192_add(I192 a, I192 b) {
+  I192 r;
+  asm("add.cc.u64 %0, %3, %6;\n\taddc.cc.u64 %1, %4, %7;\n\taddc.u64 %2, %5, %8;"
+      : "=l"(r.w0), "=l"(r.w1), "=l"(r.w2)
+      : "l"(a.w0), "l"(a.w1), "l"(a.w2), "l"(b.w0), "l"(b.w1), "l"(b.w2));
+  return r;
+}
+__device__ __forceinline__ I192 i192_shfl_xor(I192 v, int m) {
+  I192 r;
+  r.w0 = __shfl_xor_sync(0xffffffffu, v.w0, m);
+  r.w1 = __shfl_xor_sync(0xffffffffu, v.w1, m);
+  r.w2 = __shfl_xor_sync(0xffffffffu, v.w2, m);
+  return r;
+}
+// v * 2^(32 j) for a W128 v >= 0 (j = 0..4), as I192 (upper bits beyond 192 dropped: |total| < 2^160)
+__device__ __forceinline__ I192 i192_from_shifted(W128 v, int j) {
+  uint32_t src[4] = {(uint32_t)v.lo, (uint32_t)(v.lo >> 32), (uint32_t)v.hi, (uint32_t)((uint64_t)v.hi >> 32)};
+  uint32_t d[6] = {0, 0, 0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (i + j < 6) d[i + j] = src[i];
+  return I192{((uint64_t)d[1] << 32) | d[0], ((uint64_t)d[3] << 32) | d[2], ((uint64_t)d[5] << 32) | d[4]};
+}
+__device__ __forceinline__ I192 i192_neg(I192 a) {
+  I192 r{~a.w0, ~a.w1, ~a.w2};
+  return i192_add(r, I192{1, 0, 0});
+}
+
+// Block sum of the thread cells into a signed 192-bit total (units of g_f),
+// valid in thread 0.  `scratch` (32 x 10 W128) may alias the cells: they are
+// read into registers before it is written.
+__device__ __forceinline__ I192 fx_block_total(const uint64_t* A, uint32_t NT, W128 (*red)[10]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (int)(NT >> 5);
+  W128 col[10];
+#pragma unroll
+  for (int s = 0; s < 2; ++s)
+#pragma unroll
+    for (int w = 2; w < STRIDE; ++w) col[s * 5 + (w - 2)] = W128{A[(w + STRIDE * s) * NT], 0};
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) col[i] = w_add(col[i], shfl_xor_w(col[i], m));
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < 10; ++i) red[warp][i] = col[i];
+  }
+  __syncthreads();
+  I192 t{0, 0, 0};
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 10; ++i) {
+      W128 s = W128{0, 0};
+      for (int w = 0; w < nw; ++w) s = w_add(s, red[w][i]);
+      I192 v = i192_from_shifted(s, i % 5);
+      t = i192_add(t, i < 5 ? v : i192_neg(v));
+    }
+  }
+  return t;
+}
+
+
+// Index guess from the largest exponent field over SAMPLE evenly spaced
+// elements (every block computes the same value).  Returns the bin index;
+// *emax_out gets the largest biased exponent seen (all-ones: Inf/NaN).
+// s_emax: one shared word.  All threads of the block must call it.
+template <typename T>
+__device__ __forceinline__ int guess_index(const T* __restrict__ x, int64_t n, int K, unsigned* s_emax,
+                                           int* emax_out) {
+  typedef Geom<T> G;
+  constexpr unsigned EMASK = sizeof(T) == 8 ? 0x7FF00000u : 0x7F800000u;
+  constexpr int ESH = sizeof(T) == 8 ? 20 : 23;
+  if (threadIdx.x == 0) *s_emax = 0;
+  __syncthreads();
+  const int64_t S = n < SAMPLE ? n : SAMPLE;
+  unsigned em = 0;
+  for (int64_t j = threadIdx.x; j < S; j += blockDim.x) {
+    int64_t pos = (j * n) / S;
+    unsigned hi;
+    if constexpr (sizeof(T) == 8) hi = (unsigned)__double2hiint(__ldg(x + pos));
+    else hi = __float_as_uint(__ldg(x + pos));
+    em = max(em, hi & EMASK);
+  }
+  em = __reduce_max_sync(0xffffffffu, em);
+  if ((threadIdx.x & 31) == 0) atomicMax(s_emax, em);
+  __syncthreads();
+  const int eb = (int)(*s_emax >> ESH);
+  *emax_out = eb;
+  if (eb == 0) return G::NB - K;
+  int j = (G::B0 + G::W - 2 - (eb - G::BIAS)) / G::W;
+  j = min(j, G::NB - 1);
+  return min(j, G::NB - K);
+}
+
+// Largest biased exponent inside bin I: |x| < 2^(beta_I + W - 1).
+template <typename T>
+__device__ __forceinline__ int bin_top_exponent(int I) {
+  typedef Geom<T> G;
+  return I == 0 ? (sizeof(T) == 8 ? 2046 : 254) : G::BIAS + beta<T>(I) + G::W - 2;
+}
+
+__device__ __forceinline__ FxConst make_const(int bf, uint32_t one) {
+  FxConst k;
+  k.one = one;
+  k.negone = 0u - one;
+  k.c63 = 63u * one;
+  k.c31 = 31u * one;
+  k.c256 = 256u * one;
+  k.c7 = (uint32_t)STRIDE * one;
+  k.Cp = (uint32_t)(-1011 - bf);
+  return k;
+}
+
+// Rounded value of a finite double |x| at g_f as a 128-bit integer (< 2^122),
+// same arithmetic as fx_deposit but in registers: P'' = M' 2^u over six
+// 32-bit words through one-hot multipliers 2^(u - 32 j) (no variable word
+// selection), value = words 2..5.
+__device__ __forceinline__ void round_f64(uint32_t hi, uint32_t lo, const FxConst& k, uint64_t& r_lo, uint64_t& r_hi) {
+  uint32_t eb = mad32(hi, k.one + k.one, 0u) >> 21;
+  int us = (int)mad32(eb, k.one, k.Cp);
+  uint32_t u = (uint32_t)max(us, 0);
+  uint32_t mh = (hi & 0xFFFFFu) | 0x100000u;
+  uint32_t hl = shl_clamp32(1u, (int)mad32(u, k.negone, k.c63));
+  uint32_t hh = shl_clamp32(1u, (int)mad32(u, k.negone, k.c31));
+  uint32_t b = min(mh & mad32(hl, k.c256, 0u), 1u);
+  uint64_t Mp = ((((uint64_t)mh) << 32) | lo) + ((((uint64_t)hh) << 32) | hl) - (uint64_t)b;
+  uint32_t lo2 = (uint32_t)Mp, mh2 = (uint32_t)(Mp >> 32);
+  uint32_t q0 = shl_clamp32(1u, (int)u), q1 = shl_clamp32(1u, (int)u - 32), q2 = shl_clamp32(1u, (int)u - 64),
+           q3 = shl_clamp32(1u, (int)u - 96), q4 = shl_clamp32(1u, (int)u - 128);
+  uint64_t a0 = madw(lo2, q0, 0), a1 = madw(lo2, q1, 0), a2 = madw(lo2, q2, 0), a3 = madw(lo2, q3, 0),
+           a4 = madw(lo2, q4, 0);
+  uint64_t s0 = madw(mh2, q0, a0 >> 32), s1 = madw(mh2, q1, a1 >> 32), s2 = madw(mh2, q2, a2 >> 32),
+           s3 = madw(mh2, q3, a3 >> 32), s4 = madw(mh2, q4, a4 >> 32);
+  uint32_t V0 = (uint32_t)a2 | (uint32_t)s1 | (uint32_t)(s0 >> 32);
+  uint32_t V1 = (uint32_t)a3 | (uint32_t)s2 | (uint32_t)(s1 >> 32);
+  uint32_t V2 = (uint32_t)a4 | (uint32_t)s3 | (uint32_t)(s2 >> 32);
+  uint32_t V3 = (uint32_t)s4 | (uint32_t)(s3 >> 32);
+  r_lo = ((uint64_t)V1 << 32) | V0;
+  r_hi = ((uint64_t)V3 << 32) | V2;
+}
+
+// Rounded value of a finite float |x| at g_f (|x| / g_f < 2^38): with
+// P = M 2^(t + 24) (t: shift of the significand, g_f at bit 24 of P) the
+// value is (P + 2^23 - b) >> 24, b = bit 36 of P (the rounding bit of fold
+// K-2, g_f 2^12).  Shifts below 2^-24 g_f give P = 0.
+__device__ __forceinline__ uint64_t round_f32(uint32_t bits, int tshift24) {
+  uint32_t eb = (bits >> 23) & 0xFFu;
+  uint64_t M = (uint64_t)((bits & 0x7FFFFFu) | 0x800000u);
+  uint64_t P;
+  asm("shl.b64 %0, %1, %2;" : "=l"(P) : "l"(M), "r"((int)eb + tshift24));   // negative amount: 0
+  return (P + (1ull << 23) - ((P >> 36) & 1)) >> 24;
+}
+
+}  // namespace fx
+}  // namespace repro
