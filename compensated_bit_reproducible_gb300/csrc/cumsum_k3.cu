@@ -712,8 +712,13 @@ __device__ __forceinline__ void cf_stage(T* buf, const T* g, int cnt, int lane) 
 }
 
 // Pass 1.  Persistent blocks; each warp takes whole chunks: staged in shared
-// memory, lane l sums its 16 contiguous elements, an exclusive warp scan
-// gives each lane's prefix within the chunk (stored) and the chunk total.
+// memory, lane l sums its 16 contiguous elements (double: one rounding each;
+// float: the binned sum's floating-point primaries at the fixed index, whose
+// fold sums combine to the same integer), and an exclusive warp scan gives
+// each lane's prefix within the chunk (stored) and the chunk total.  The
+// checks: any element above bin L (or Inf/NaN) fails the guess; the first
+// element of bin L matters only if it lies in the first tile, so only those
+// chunks look for it.
 template <typename T>
 __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, int64_t n, int64_t nch,
                                                       uint32_t one, CsCtl* ctl, unsigned char* __restrict__ lanep,
@@ -734,49 +739,65 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
   const int eb_bot = G::BIAS + beta<T>(L + 1) + G::W - 1;   // bottom of bin L
   const fx::FxConst kc = fx::make_const(bf, one);
   const int tsh24 = -150 - bf + 24;
+  const fx::F32Const fk = fx::make_f32_const(tsh24);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  T* buf = sm + warp * CF_PAD;
   int ebmax = 0;                       // largest exponent field seen
-  int64_t first = INT64_MAX;           // first position of bin L seen by this thread
+  int64_t first = INT64_MAX;           // first position of bin L (first tile only)
+  AccF<3> facc;                        // float: primaries fixed at index L
+  if constexpr (sizeof(T) == 4) {
+    facc.init(3);
+    if (L < facc.I) facc.raise(L);
+  }
   const int64_t gw = (int64_t)blockIdx.x * CF_WARPS + warp, GW = (int64_t)gridDim.x * CF_WARPS;
   for (int64_t ch = gw; ch < nch; ch += GW) {
     const int64_t c0 = ch * CF_CHUNK;
     const int cnt = (int)min((int64_t)CF_CHUNK, n - c0);
+    const bool look = c0 < C3_TILE;   // warp-uniform
+    fx::I192 tot;
+    T* buf = sm + warp * CF_PAD;
     cf_stage<T>(buf, in + c0, cnt, lane);
     __syncwarp();
     const int b = lane * 16, sb = b + lane;
-    fx::I192 own{0, 0, 0};
-    int64_t own32 = 0;
+    T v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const T v = b + i < cnt ? buf[sb + i] : (T)0;
+      v[i] = b + i < cnt ? buf[sb + i] : (T)0;
       uint32_t hi;
-      if constexpr (sizeof(T) == 8) hi = (uint32_t)__double2hiint(v);
-      else hi = __float_as_uint(v);
+      if constexpr (sizeof(T) == 8) hi = (uint32_t)__double2hiint(v[i]);
+      else hi = __float_as_uint(v[i]);
       const int eb = (int)((hi << 1) >> (sizeof(T) == 8 ? 21 : 24));
       ebmax = max(ebmax, eb);
-      if (eb >= eb_bot && first == INT64_MAX) first = c0 + b + i;
-      if constexpr (sizeof(T) == 8) own = fx::i192_add(own, cf_round<T>(v, kc, tsh24));
-      else {
-        const int64_t r = (int64_t)fx::round_f32(hi, tsh24);
-        own32 += (hi >> 31) ? -r : r;
-      }
+      if (look && eb >= eb_bot) first = min(first, c0 + b + i);
     }
-    if constexpr (sizeof(T) == 4) own = i192_from_i64(own32);
-    fx::I192 tot;
-    const fx::I192 exc = i192_warp_exclusive(own, &tot);
     const size_t li = (size_t)ch * 32 + lane;
     if constexpr (sizeof(T) == 8) {
+      fx::I192 own{0, 0, 0};
+#pragma unroll
+      for (int i = 0; i < 16; ++i) own = fx::i192_add(own, cf_round<T>(v[i], kc, tsh24));
+      const fx::I192 exc = i192_warp_exclusive(own, &tot);
       const size_t plane = (size_t)nch * 32;
       uint64_t* lp = (uint64_t*)lanep;
       lp[li] = exc.w0;
       lp[plane + li] = exc.w1;
       lp[2 * plane + li] = exc.w2;
     } else {
-      ((int64_t*)lanep)[li] = (int64_t)exc.w0;   // |prefix| < 512 2^38
+      // float primaries at the fixed index (the binned sum's deposit); lane
+      // sums and chunk totals stay below 2^47
+      facc.template chunk<16>(v);
+      facc.finish();
+      const int64_t own = (facc.L[0] << 26) + (facc.L[1] << 13) + facc.L[2];
+      facc.L[0] = facc.L[1] = facc.L[2] = 0;
+      int64_t inc = own;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int64_t o = (int64_t)__shfl_up_sync(0xffffffffu, (long long)inc, d);
+        if (lane >= d) inc += o;
+      }
+      ((int64_t*)lanep)[li] = inc - own;
+      tot = i192_from_i64((int64_t)__shfl_sync(0xffffffffu, (long long)inc, 31));
     }
-    if (lane == 0) ctot[ch] = tot;
     __syncwarp();
+    if (lane == 0) ctot[ch] = tot;
   }
   const int bad = __syncthreads_or(ebmax > eb_top);
   int64_t f = first;
@@ -860,6 +881,7 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_replay(const T* in, T* out, int64
   const int bf = beta<T>(L + 2);
   const fx::FxConst kc = fx::make_const(bf, one);
   const int tsh24 = -150 - bf + 24;
+  const fx::F32Const fk = fx::make_f32_const(tsh24);
   if (blockIdx.x == 0 && exact0) c3_replay_tile<T>(in, out, n, 0, s3_zero(Geom<T>::NB - 3), sm, wsm);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   T* buf = sm + warp * CF_PAD;
@@ -873,6 +895,7 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_replay(const T* in, T* out, int64
     cf_stage<T>(buf, in + c0, cnt, lane);
     const size_t li = (size_t)ch * 32 + lane;
     fx::I192 t = fx::i192_add(bpre[ch >> 10], lpre[ch]);
+    const int b = lane * 16, sb = b + lane;
     if constexpr (sizeof(T) == 8) {
       const size_t plane = (size_t)nch * 32;
       const uint64_t* lp = (const uint64_t*)lanep;
@@ -881,14 +904,27 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_replay(const T* in, T* out, int64
       t = fx::i192_add(t, i192_from_i64(((const int64_t*)lanep)[li]));
     }
     __syncwarp();
-    const int b = lane * 16, sb = b + lane;
+    if constexpr (sizeof(T) == 8) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (b + i < cnt) {
-        const T v = buf[sb + i];
-        t = fx::i192_add(t, cf_round<T>(v, kc, tsh24));
-        if constexpr (sizeof(T) == 8) buf[sb + i] = round_t192_d((int64_t)t.w2, t.w1, t.w0, bf);
-        else buf[sb + i] = round_t128_f((int64_t)t.w1, t.w0, bf);
+      for (int i = 0; i < 16; ++i) {
+        if (b + i < cnt) {
+          const T v = buf[sb + i];
+          t = fx::i192_add(t, cf_round<T>(v, kc, tsh24));
+          buf[sb + i] = round_t192_d((int64_t)t.w2, t.w1, t.w0, bf);
+        }
+      }
+    } else {
+      // |running total| < 2^71: 96-bit words
+      fx::I96 a{(uint32_t)t.w0, (uint32_t)(t.w0 >> 32), (uint32_t)t.w1};
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (b + i < cnt) {
+          const uint32_t bits = __float_as_uint(buf[sb + i]);
+          uint32_t rl, rh;
+          fx::round_f32w(bits, fk, rl, rh);
+          a = fx::i96_add_signed(a, rl, rh, (uint32_t)((int32_t)bits >> 31));
+          buf[sb + i] = fx::i96_to_float(a, bf);
+        }
       }
     }
     __syncwarp();

@@ -254,5 +254,80 @@ __device__ __forceinline__ uint64_t round_f32(uint32_t bits, int tshift24) {
   return (P + (1ull << 23) - ((P >> 36) & 1)) >> 24;
 }
 
+
+// ------------------------------------------------------------------ float
+// Float rounding at g_f in 32-bit pieces.  With s = eb + sh (the shift that
+// puts g_f at bit 24 of M 2^s), the rounded value is
+//   s <= 24:  (M + 2^(23 - s) - b) >> (24 - s),  b = bit 36 - s of M,
+//   s >= 24:  M << (s - 24)  (exact, below 2^38; at s = 24 both give M),
+// every shift clamped (out-of-range amounts give 0), so the two parts are
+// computed unconditionally and one of them is zero.
+struct F32Const {
+  int c23, c24, cm24, c56;   // constants minus the biased exponent
+};
+__device__ __forceinline__ F32Const make_f32_const(int sh) {
+  return F32Const{23 - sh, 24 - sh, sh - 24, 56 - sh};
+}
+__device__ __forceinline__ uint32_t shr_clamp32(uint32_t v, int s) {   // s outside [0, 31] gives 0
+  uint32_t r;
+  asm("shr.b32 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(s));
+  return r;
+}
+// |x| rounded at g_f as (lo, hi) 32-bit words; eb: biased exponent field.
+__device__ __forceinline__ void round_f32w(uint32_t bits, const F32Const& k, uint32_t& lo, uint32_t& hi) {
+  const int eb = (int)((bits >> 23) & 0xFFu);
+  const uint32_t M = (bits & 0x7FFFFFu) | 0x800000u;
+  const uint32_t h = shl_clamp32(1u, k.c23 - eb);
+  // tie bit 36 - s of M, as a mask derived from h: zero whenever h is (the
+  // exact case s >= 24, where M is not rounded)
+  const uint32_t b = min(M & (h << 13), 1u);
+  const uint32_t small = shr_clamp32(M + h - b, k.c24 - eb);
+  lo = small | shl_clamp32(M, eb + k.cm24);
+  hi = shr_clamp32(M, k.c56 - eb);
+}
+
+// Signed 96-bit integer in 32-bit words (float running totals: < 2^71).
+struct I96 {
+  uint32_t w0, w1, w2;
+};
+// a + (sign ? -(hi:lo) : (hi:lo)), sm = 0 or all ones
+__device__ __forceinline__ I96 i96_add_signed(I96 a, uint32_t lo, uint32_t hi, uint32_t sm) {
+  I96 r;
+  asm("add.cc.u32 %0, %3, %6;\n\taddc.cc.u32 %1, %4, %7;\n\taddc.u32 %2, %5, %8;"
+      : "=r"(r.w0), "=r"(r.w1), "=r"(r.w2)
+      : "r"(a.w0), "r"(a.w1), "r"(a.w2), "r"(lo ^ sm), "r"(hi ^ sm), "r"(sm));
+  // + 1 for a negation: added through the lowest word with carry
+  asm("add.cc.u32 %0, %0, %3;\n\taddc.cc.u32 %1, %1, 0;\n\taddc.u32 %2, %2, 0;"
+      : "+r"(r.w0), "+r"(r.w1), "+r"(r.w2)
+      : "r"(sm & 1u));
+  return r;
+}
+// Correct rounding of a * 2^lsb to float for |a| * 2^lsb >= 2^-126 or a = 0
+// (the fast path's grids guarantee it); overflow gives +-Inf.
+__device__ __forceinline__ float i96_to_float(I96 a, int lsb) {
+  const uint32_t sm = (uint32_t)((int32_t)a.w2 >> 31);
+  uint32_t x0 = a.w0 ^ sm, x1 = a.w1 ^ sm, x2 = a.w2 ^ sm;
+  asm("add.cc.u32 %0, %0, %3;\n\taddc.cc.u32 %1, %1, 0;\n\taddc.u32 %2, %2, 0;"
+      : "+r"(x0), "+r"(x1), "+r"(x2)
+      : "r"(sm & 1u));
+  const bool t2 = x2 != 0, t1 = x1 != 0;
+  const uint32_t top = t2 ? x2 : (t1 ? x1 : x0);
+  const uint32_t nxt = t2 ? x1 : (t1 ? x0 : 0u);
+  const uint32_t rest = t2 ? x0 : 0u;
+  if (top == 0u) return 0.0f;
+  const int tw = t2 ? 2 : (t1 ? 1 : 0);
+  const int lz = __clz((int)top);
+  const uint32_t v = funnel_l(nxt, top, (uint32_t)lz);      // leading bit at 31
+  const uint32_t lost = shl_clamp32(nxt, lz) | rest;         // bits below v
+  uint32_t m = v >> 8;
+  const uint32_t rb = (v >> 7) & 1u;
+  const uint32_t st = (v & 0x7Fu) | lost;
+  m += rb & ((st != 0u) | (m & 1u));
+  const int E = 32 * tw + 31 - lz + lsb;                      // exponent of the leading bit
+  uint32_t r = ((uint32_t)(E + 126) << 23) + m;                // a rounding carry moves into the exponent
+  if (E > 127) r = 0x7F800000u;
+  return __uint_as_float(r | (sm & 0x80000000u));
+}
+
 }  // namespace fx
 }  // namespace repro
