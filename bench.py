@@ -44,6 +44,14 @@ ROWS_SPEC = [
 ]
 
 
+def set_vector_length(n: int) -> None:
+    """Use n-element vectors for the 1e8-element rows (smaller profiling
+    captures); the row names keep their labels."""
+    global N_SUM, ROWS_SPEC
+    N_SUM = n
+    ROWS_SPEC = [(name, (n if name.endswith("1e8") else cnt), bpe) for name, cnt, bpe in ROWS_SPEC]
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -147,8 +155,11 @@ def run_ours(args):
         "sum_f64_1e8": lambda: api.repro_sum_async(x64, s64, 3),
         "cumsum_f64_1e8": lambda: api.repro_cumsum(x64, out=c64, K=3),
     }
+    # kernels per call: the double sum is the fixed-index kernel plus its
+    # gated fallback; a cumulative sum is totals, scan and replay plus four
+    # gated fallback kernels (the workspace memsets are not kernels)
     launches_per_row = {"var_f32_4096x4096": 1, "sum_f32_1e8": 1, "segsum_f32_4096x4096": 1,
-                        "cumsum_f32_1e8": 4, "sum_f64_1e8": 1, "cumsum_f64_1e8": 4}
+                        "cumsum_f32_1e8": 7, "sum_f64_1e8": 2, "cumsum_f64_1e8": 7}
 
     active = [r for r in ROWS_SPEC if not args.rows or r[0] in args.rows.split(",")]
 
@@ -218,7 +229,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "f32+f64 inputs, exact int64/int128 binned lanes",
         "data": "synthetic (seeded numpy generators, shapes and distributions of the pages' workloads)",
-        "config": {"workload": WORKLOAD, "K": 3, "elements_per_step_per_gpu": elems_step,
+        "config": {"workload": WORKLOAD if N_SUM == 100_000_000 else WORKLOAD.replace("1e8", "%d" % N_SUM), "K": 3,
+                   "elements_per_step_per_gpu": elems_step,
                    "l2": "every input is larger than L2 or follows >= 400 MB of other traffic in the step",
                    "parallelism": "independent replicas" if ws > 1 else "single GPU"},
         "rows": rows,
@@ -236,16 +248,21 @@ def run_ours(args):
 
 
 def load_traffic(kernel_row: str):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary (profiles/traffic.json), or None when not captured for the
-    current kernel version."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per call of a row from the committed ncu summary
+    (profiles/traffic_per_call.md), or None when not captured for the
+    current kernels."""
+    p = os.path.join(ROOT, "profiles", "traffic_per_call.md")
     if not os.path.exists(p):
         return None
     with open(p) as f:
-        d = json.load(f)
-    v = d.get(kernel_row)
-    return v.get("dram_bytes_per_launch") if isinstance(v, dict) and v.get("current") else None
+        for line in f:
+            cells = [c.strip() for c in line.strip().strip("|").split("|")]
+            if len(cells) == 3 and cells[0] == kernel_row and cells[2] == "yes":
+                try:
+                    return int(cells[1])
+                except ValueError:
+                    return None
+    return None
 
 
 def run_e2e(args, api, torch, h32, h64, hA, dev, stream):
@@ -455,7 +472,11 @@ def main(argv=None):
     ap.add_argument("--rows", default="", help="comma list of rows to run (profiling); default: all")
     ap.add_argument("--skip-extras", action="store_true",
                     help="skip the end-to-end, CPU-baseline and comparison legs (profiling)")
+    ap.add_argument("--n", type=int, default=0,
+                    help="vector length of the 1e8-element rows (profiling on a smaller case); default 1e8")
     args = ap.parse_args(argv)
+    if args.n:
+        set_vector_length(args.n)
     ws, _, _ = dist_env()
     if args.impl == "reference":
         run_reference(args)
