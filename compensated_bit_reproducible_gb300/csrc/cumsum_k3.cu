@@ -48,8 +48,60 @@ __device__ __forceinline__ float round_t128_f(int64_t hi, uint64_t lo, int lsb) 
   return assemble<float>(neg, m, q);
 }
 
+// Fast branch of round_t192_d for normal results: rounds the two's
+// complement directly, so a negative T needs no 192-bit negation.  With p
+// the leading bit of T (of ~T for T < 0), the 64 bits of T from p down hold
+// the significand field, the half bit and 10 more bits; every bit below
+// folds into one sticky bit.  Round half to even on the floor quotient
+// q = floor(T / 2^(p - 52)) + up (carry out of the window: q = 2^53).  For
+// T >= 0 the significand is q; for T < 0 the bits above p are ones, the
+// field is q - 2^53 and the magnitude 2^53 - q; either lies in [2^52, 2^53]
+// and 2^53 carries into the exponent.  Returns false (nothing written) for
+// T = 0 or -1 and for results outside the normal range.
+__device__ __forceinline__ bool t192_to_double_normal(uint64_t t0, uint64_t t1, uint64_t t2, int lsb,
+                                                      double* out) {
+  const uint32_t x0 = (uint32_t)t0, x1 = (uint32_t)(t0 >> 32), x2 = (uint32_t)t1, x3 = (uint32_t)(t1 >> 32),
+                 x4 = (uint32_t)t2, x5 = (uint32_t)(t2 >> 32);
+  const uint32_t s = (uint32_t)((int32_t)x5 >> 31);
+  // a window of four words W3..W0 with p in W3 (or W2 before the one-word
+  // step below); rest: the words under it; e: bit position of W0
+  const bool za = (x5 == s) & (x4 == s);
+  const bool zb = (x3 == s) & (x2 == s);
+  uint32_t W3 = za ? (zb ? x1 : x3) : x5;
+  uint32_t W2 = za ? (zb ? x0 : x2) : x4;
+  uint32_t W1 = za ? (zb ? 0u : x1) : x3;
+  uint32_t W0 = za ? (zb ? 0u : x0) : x2;
+  const uint32_t rest = za ? 0u : (x1 | x0);
+  int e = za ? (zb ? -64 : 0) : 64;
+  if (W3 == s) {
+    W3 = W2;
+    W2 = W1;
+    W1 = W0;
+    W0 = 0u;
+    e -= 32;
+  }
+  const uint32_t lz = (uint32_t)__clz((int)(W3 ^ s));   // 32 only for T = 0 or -1
+  const int E = e + 127 - (int)lz + lsb;                 // exponent of bit p
+  if (lz == 32u || (unsigned)(E + 1022) > 2045u) return false;
+  const uint32_t h = fx::funnel_l(W2, W3, lz);           // bits p .. p - 31
+  const uint32_t l = fx::funnel_l(W1, W2, lz);           // bits p - 32 .. p - 63
+  const uint32_t below = fx::shl_clamp32(W1, (int)lz) | W0 | rest;
+  const uint32_t st = ((l & 0x3FFu) | below) != 0u ? 1u : 0u;
+  const uint32_t odd = (l >> 11) & 1u;
+  const uint64_t w = (((uint64_t)h) << 32) | ((l & ~0x3FFu) | st);
+  const uint64_t v = w + 0x3FFu + odd;
+  const uint64_t q = (v >> 11) | ((uint64_t)(v < w) << 53);
+  const uint64_t S = (uint64_t)(int64_t)(int32_t)s;
+  const uint64_t m = (q ^ S) + (S & ((1ull << 53) + 1));
+  *out = __longlong_as_double(
+      (long long)((S & 0x8000000000000000ull) + ((uint64_t)(E + 1022) << 52) + m));
+  return true;
+}
+
 // double: T is a signed 192-bit integer (t2:t1:t0) times 2^lsb.
 __device__ __forceinline__ double round_t192_d(int64_t t2, uint64_t t1, uint64_t t0, int lsb) {
+  double r;
+  if (t192_to_double_normal(t0, t1, (uint64_t)t2, lsb, &r)) return r;
   bool neg = t2 < 0;
   uint64_t a = (uint64_t)t2, b = t1, c = t0;
   if (neg) {
@@ -668,21 +720,29 @@ constexpr int CF_CHUNK = 512;    // elements per warp chunk: lane l owns [16 l, 
 constexpr int CF_PAD = CF_CHUNK + CF_CHUNK / 16;
 constexpr int CF_WARPS = C3_BLOCK / 32;
 
-// Signed rounded value of x at g_f as I192 (double: one-hot shift; float:
-// 64-bit).
-template <typename T>
-__device__ __forceinline__ fx::I192 cf_round(T v, const fx::FxConst& kc, int tsh24) {
-  if constexpr (sizeof(T) == 8) {
-    const uint32_t hi = (uint32_t)__double2hiint(v);
-    uint64_t rl, rh;
-    fx::round_f64(hi, (uint32_t)__double2loint(v), kc, rl, rh);
-    const uint64_t sgn = (uint64_t)((int64_t)(int32_t)hi >> 31);
-    return fx::i192_add(fx::I192{rl ^ sgn, rh ^ sgn, sgn}, fx::I192{sgn & 1u, 0, 0});
-  } else {
-    const uint32_t bits = __float_as_uint(v);
-    const int64_t r = (int64_t)fx::round_f32(bits, tsh24);
-    return i192_from_i64((bits >> 31) ? -r : r);
-  }
+// t + X + (sgn & 1) for X = (xh:xl) sign-extended from sgn (0 or all ones):
+// with X = R xor sgn this adds +R or -R.  The +1 of a negation enters as the
+// carry into the first word (set by an add that overflows exactly for 1).
+__device__ __forceinline__ fx::I192 i192_add_x(fx::I192 t, uint64_t xl, uint64_t xh, uint64_t sgn) {
+  const uint32_t s = (uint32_t)sgn;
+  uint32_t r0, r1, r2, r3, r4, r5;
+  asm("{\n\t.reg .u32 c;\n\t"
+      "add.cc.u32 c, %6, 0xFFFFFFFF;\n\t"
+      "addc.cc.u32 %0, %7, %13;\n\t"
+      "addc.cc.u32 %1, %8, %14;\n\t"
+      "addc.cc.u32 %2, %9, %15;\n\t"
+      "addc.cc.u32 %3, %10, %16;\n\t"
+      "addc.cc.u32 %4, %11, %17;\n\t"
+      "addc.u32 %5, %12, %17;\n\t}"
+      : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3), "=r"(r4), "=r"(r5)
+      : "r"(s & 1u), "r"((uint32_t)t.w0), "r"((uint32_t)(t.w0 >> 32)), "r"((uint32_t)t.w1),
+        "r"((uint32_t)(t.w1 >> 32)), "r"((uint32_t)t.w2), "r"((uint32_t)(t.w2 >> 32)),
+        "r"((uint32_t)xl), "r"((uint32_t)(xl >> 32)), "r"((uint32_t)xh), "r"((uint32_t)(xh >> 32)), "r"(s));
+  return fx::I192{((uint64_t)r1 << 32) | r0, ((uint64_t)r3 << 32) | r2, ((uint64_t)r5 << 32) | r4};
+}
+// t + (sgn ? -R : R) for a 128-bit magnitude R = (rh:rl).
+__device__ __forceinline__ fx::I192 i192_add_signed(fx::I192 t, uint64_t rl, uint64_t rh, uint64_t sgn) {
+  return i192_add_x(t, rl ^ sgn, rh ^ sgn, sgn);
 }
 
 // Coalesced copy of a chunk (cnt elements at g) into the warp's padded buffer.
@@ -773,7 +833,12 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
     if constexpr (sizeof(T) == 8) {
       fx::I192 own{0, 0, 0};
 #pragma unroll
-      for (int i = 0; i < 16; ++i) own = fx::i192_add(own, cf_round<T>(v[i], kc, tsh24));
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t hi = (uint32_t)__double2hiint(v[i]);
+        uint64_t rl, rh;
+        fx::round_f64(hi, (uint32_t)__double2loint(v[i]), kc, rl, rh);
+        own = i192_add_signed(own, rl, rh, (uint64_t)((int64_t)(int32_t)hi >> 31));
+      }
       const fx::I192 exc = i192_warp_exclusive(own, &tot);
       const size_t plane = (size_t)nch * 32;
       uint64_t* lp = (uint64_t*)lanep;
@@ -908,8 +973,11 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_replay(const T* in, T* out, int64
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         if (b + i < cnt) {
-          const T v = buf[sb + i];
-          t = fx::i192_add(t, cf_round<T>(v, kc, tsh24));
+          const double v = buf[sb + i];
+          const uint32_t hi = (uint32_t)__double2hiint(v);
+          uint64_t rl, rh;
+          fx::round_f64(hi, (uint32_t)__double2loint(v), kc, rl, rh);
+          t = i192_add_signed(t, rl, rh, (uint64_t)((int64_t)(int32_t)hi >> 31));
           buf[sb + i] = round_t192_d((int64_t)t.w2, t.w1, t.w0, bf);
         }
       }

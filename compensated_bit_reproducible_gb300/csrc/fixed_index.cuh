@@ -242,18 +242,6 @@ __device__ __forceinline__ void round_f64(uint32_t hi, uint32_t lo, const FxCons
   r_hi = ((uint64_t)V3 << 32) | V2;
 }
 
-// Rounded value of a finite float |x| at g_f (|x| / g_f < 2^38): with
-// P = M 2^(t + 24) (t: shift of the significand, g_f at bit 24 of P) the
-// value is (P + 2^23 - b) >> 24, b = bit 36 of P (the rounding bit of fold
-// K-2, g_f 2^12).  Shifts below 2^-24 g_f give P = 0.
-__device__ __forceinline__ uint64_t round_f32(uint32_t bits, int tshift24) {
-  uint32_t eb = (bits >> 23) & 0xFFu;
-  uint64_t M = (uint64_t)((bits & 0x7FFFFFu) | 0x800000u);
-  uint64_t P;
-  asm("shl.b64 %0, %1, %2;" : "=l"(P) : "l"(M), "r"((int)eb + tshift24));   // negative amount: 0
-  return (P + (1ull << 23) - ((P >> 36) & 1)) >> 24;
-}
-
 
 // ------------------------------------------------------------------ float
 // Float rounding at g_f in 32-bit pieces.  With s = eb + sh (the shift that
@@ -302,9 +290,45 @@ __device__ __forceinline__ I96 i96_add_signed(I96 a, uint32_t lo, uint32_t hi, u
       : "r"(sm & 1u));
   return r;
 }
+// Normal results of a * 2^lsb, rounded on the two's complement (no
+// negation): with p the leading bit of a (of ~a for a < 0), the 32 bits from
+// p down hold the significand field, the half bit and 7 more; the bits below
+// fold into one sticky bit.  q = floor(a / 2^(p - 23)) + up (a carry out of
+// the window gives 2^24); the magnitude is q for a >= 0 and 2^24 - q for
+// a < 0 (bits above p are ones), in [2^23, 2^24], and 2^24 carries into the
+// exponent.  False (nothing written) for a = 0 or -1 and outside the normal
+// range.
+__device__ __forceinline__ bool i96_to_float_normal(I96 a, int lsb, uint32_t* out) {
+  const uint32_t s = (uint32_t)((int32_t)a.w2 >> 31);
+  const bool z2 = a.w2 == s;
+  uint32_t top = z2 ? a.w1 : a.w2, nxt = z2 ? a.w0 : a.w1;
+  const uint32_t rest = z2 ? 0u : a.w0;
+  int e = z2 ? 0 : 32;   // bit position of nxt
+  if (top == s) {
+    top = nxt;
+    nxt = 0u;
+    e -= 32;
+  }
+  const uint32_t lz = (uint32_t)__clz((int)(top ^ s));   // 32 only for a = 0 or -1
+  const int E = e + 63 - (int)lz + lsb;                   // exponent of bit p
+  if (lz == 32u || (unsigned)(E + 126) > 253u) return false;
+  const uint32_t v = funnel_l(nxt, top, lz);              // bits p .. p - 31
+  const uint32_t below = shl_clamp32(nxt, (int)lz) | rest;
+  const uint32_t st = ((v & 0x7Fu) | below) != 0u ? 1u : 0u;
+  const uint32_t odd = (v >> 8) & 1u;
+  const uint32_t w = (v & ~0x7Fu) | st;
+  const uint32_t u = w + 0x7Fu + odd;
+  const uint32_t q = (u >> 8) | ((uint32_t)(u < w) << 24);
+  const uint32_t m = (q ^ s) + (s & ((1u << 24) + 1u));
+  *out = (s & 0x80000000u) + ((uint32_t)(E + 126) << 23) + m;
+  return true;
+}
+
 // Correct rounding of a * 2^lsb to float for |a| * 2^lsb >= 2^-126 or a = 0
 // (the fast path's grids guarantee it); overflow gives +-Inf.
 __device__ __forceinline__ float i96_to_float(I96 a, int lsb) {
+  uint32_t fast;
+  if (i96_to_float_normal(a, lsb, &fast)) return __uint_as_float(fast);
   const uint32_t sm = (uint32_t)((int32_t)a.w2 >> 31);
   uint32_t x0 = a.w0 ^ sm, x1 = a.w1 ^ sm, x2 = a.w2 ^ sm;
   asm("add.cc.u32 %0, %0, %3;\n\taddc.cc.u32 %1, %1, 0;\n\taddc.u32 %2, %2, 0;"

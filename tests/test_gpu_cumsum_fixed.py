@@ -97,3 +97,19 @@ def test_cancellation_f64():
     dev()
     a = inputs.wide_f64(N // 2, seed=27)
     check(np.concatenate([a, -a[::-1], [1.0]]))
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_single_pass_many_tiles_repeatable(dt):
+    """Out of place (single pass with look-back over ~2000 tiles): equal to
+    the oracle, to the in-place (three-pass) result, and to itself on every
+    repeat, whatever order the tiles were claimed in."""
+    dev()
+    n = 1_000_003
+    x = inputs.wide_f64(n, seed=31).astype(dt) if dt == F64 else inputs.normal_f32(n, seed=31, spikes=True)
+    want = oracle.adn_cumsum(x, 3)
+    got = cumsum(x)
+    assert same_bits(got, want), first_diff(got, want)
+    assert same_bits(cumsum(x, inplace=True), want)
+    for _ in range(3):
+        assert same_bits(cumsum(x), got)
