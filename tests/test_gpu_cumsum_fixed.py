@@ -100,10 +100,9 @@ def test_cancellation_f64():
 
 
 @pytest.mark.parametrize("dt", [F32, F64])
-def test_single_pass_many_tiles_repeatable(dt):
-    """Out of place (single pass with look-back over ~2000 tiles): equal to
-    the oracle, to the in-place (three-pass) result, and to itself on every
-    repeat, whatever order the tiles were claimed in."""
+def test_many_chunks_in_and_out_of_place_repeatable(dt):
+    """About 2000 chunks (two levels of the chunk scan): out of place equal
+    to the oracle, in place equal to it, and repeats bit for bit."""
     dev()
     n = 1_000_003
     x = inputs.wide_f64(n, seed=31).astype(dt) if dt == F64 else inputs.normal_f32(n, seed=31, spikes=True)
