@@ -460,6 +460,65 @@ def init_dist(ws, backend=None):
         dist.init_process_group(backend=backend)
 
 
+SMALL_N_SIZES = (1, 64, 1024, 2048, 2049, 4096, 4097, 16384, 16385)
+
+
+def run_small_n(reps: int = 201):
+    """Call latency at small sizes, measured like the pages' small-N tables:
+    three warm-up calls, then `reps` synchronous calls alternating baseline
+    and ADN, median host wall time per call (internal allocation and
+    synchronisation included).  Sum: `repro_sum` (result on the host) against
+    `torch.sum(x).item()`; cumulative sum (K = 3): `repro_cumsum` plus a
+    stream synchronisation against `torch.cumsum` plus one.  Prints one JSON
+    object (not the benchmark line)."""
+    import numpy as np
+    import torch
+    from compensated_bit_reproducible_gb300 import api, inputs
+    dev = torch.device("cuda:0")
+    api.validate_environment()
+    table = {}
+    for name, dt in (("f32", torch.float32), ("f64", torch.float64)):
+        for n in SMALL_N_SIZES:
+            xh = inputs.normal_f32(n, seed=n) if name == "f32" else inputs.wide_f64(n, seed=n)
+            x = torch.from_numpy(xh).to(dev)
+            o1 = torch.empty_like(x)
+            o2 = torch.empty_like(x)
+
+            def adn_sum():
+                api.repro_sum(x, 3)
+
+            def base_sum():
+                torch.sum(x).item()
+
+            def adn_cs():
+                api.repro_cumsum(x, out=o1, K=3)
+                torch.cuda.synchronize()
+
+            def base_cs():
+                torch.cumsum(x, 0, out=o2)
+                torch.cuda.synchronize()
+
+            row = {}
+            for op, (fa, fb) in (("sum", (adn_sum, base_sum)), ("cumsum", (adn_cs, base_cs))):
+                for _ in range(3):
+                    fa()
+                    fb()
+                ta, tb = [], []
+                for _ in range(reps):
+                    t0 = time.perf_counter_ns()
+                    fb()
+                    tb.append(time.perf_counter_ns() - t0)
+                    t0 = time.perf_counter_ns()
+                    fa()
+                    ta.append(time.perf_counter_ns() - t0)
+                a = float(np.median(ta)) / 1e3
+                b = float(np.median(tb)) / 1e3
+                row[op] = {"adn_us": round(a, 2), "baseline_us": round(b, 2), "adn_over_baseline": round(a / b, 3)}
+            table["%s_%d" % (name, n)] = row
+    print(json.dumps({"small_n_latency": table, "reps": reps, "K": 3,
+                      "baselines": {"sum": "torch.sum(x).item()", "cumsum": "torch.cumsum + synchronize"}}))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -474,7 +533,12 @@ def main(argv=None):
                     help="skip the end-to-end, CPU-baseline and comparison legs (profiling)")
     ap.add_argument("--n", type=int, default=0,
                     help="vector length of the 1e8-element rows (profiling on a smaller case); default 1e8")
+    ap.add_argument("--small-n", action="store_true",
+                    help="print the small-size call latencies (not the benchmark line) and exit")
     args = ap.parse_args(argv)
+    if args.small_n:
+        run_small_n()
+        return
     if args.n:
         set_vector_length(args.n)
     ws, _, _ = dist_env()

@@ -170,6 +170,26 @@ __global__ void __launch_bounds__(1024) adn_sum_kernel(const T* __restrict__ x, 
   }
 }
 
+// Small inputs: one block, no workspace and no grid merge (the whole state
+// is merged inside the block and converted by thread 0).  The result bits
+// are the same as the grid path's.
+template <typename T, int KT, int U>
+__global__ void __launch_bounds__(1024) adn_sum_single(const T* __restrict__ x, int64_t n, int K,
+                                                       T* __restrict__ result) {
+  typedef typename AccOf<T, KT>::type Acc;
+  constexpr int N = Acc::N;
+  Acc acc;
+  acc.init(K);
+  accumulate_range<T, Acc, U>(acc, x, n, threadIdx.x, blockDim.x);
+  acc.finish();
+  State<N> st;
+  block_merge<N>(acc.I, acc.flags, acc.L, K, &st);
+  if (threadIdx.x == 0) {
+    if constexpr (KT != 0) *result = convert_fast<T, KT>(st.I, st.flags, st.F);
+    else *result = convert_state<T, N>(st, K);
+  }
+}
+
 // --------------------------------------------------------- segmented sums
 // One block per row (grid-stride over rows): rows of a row-major [rows, cols]
 // array, any cols.
@@ -253,6 +273,25 @@ cudaError_t launch_sum(const T* x, int64_t n, int K, unsigned char* ws, T* resul
     default: return launch_sum_k<T, 0>(x, n, K, ws, result, grid, block, gate, s);
   }
 }
+
+template <typename T>
+cudaError_t launch_sum_single(const T* x, int64_t n, int K, T* result, int block, cudaStream_t s) {
+  constexpr int U = 1;
+  switch (K) {
+    case 2: adn_sum_single<T, 2, U><<<1, block, 0, s>>>(x, n, K, result); break;
+    case 3: adn_sum_single<T, 3, U><<<1, block, 0, s>>>(x, n, K, result); break;
+    case 4: adn_sum_single<T, 4, U><<<1, block, 0, s>>>(x, n, K, result); break;
+    case 5: adn_sum_single<T, 5, U><<<1, block, 0, s>>>(x, n, K, result); break;
+    case 6: adn_sum_single<T, 6, U><<<1, block, 0, s>>>(x, n, K, result); break;
+    case 7: adn_sum_single<T, 7, U><<<1, block, 0, s>>>(x, n, K, result); break;
+    case 8: adn_sum_single<T, 8, U><<<1, block, 0, s>>>(x, n, K, result); break;
+    default: adn_sum_single<T, 0, U><<<1, block, 0, s>>>(x, n, K, result); break;
+  }
+  return cudaGetLastError();
+}
+
+template cudaError_t launch_sum_single<float>(const float*, int64_t, int, float*, int, cudaStream_t);
+template cudaError_t launch_sum_single<double>(const double*, int64_t, int, double*, int, cudaStream_t);
 
 template cudaError_t launch_sum<float>(const float*, int64_t, int, unsigned char*, float*, int, int, cudaStream_t,
                                        const unsigned*);

@@ -42,6 +42,66 @@ template <> struct Lim<double> {
   static constexpr int MAXK = MAXK_F64;
 };
 
+// Workspace comes from a pool of the library's own per device, which keeps
+// up to POOL_KEEP bytes mapped across synchronisations (a pool that returns
+// everything at each synchronisation makes the next call map its workspace
+// afresh, about 0.2 ms).  The process's default pool is left as it is.
+constexpr uint64_t POOL_KEEP = 1ull << 30;
+
+cudaError_t ws_alloc(void** p, size_t bytes, cudaStream_t stream) {
+  static cudaMemPool_t pools[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaMallocAsync(p, bytes, stream);
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (!pools[dev]) {
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      cudaMemPool_t np = nullptr;
+      if ((e = cudaMemPoolCreate(&np, &props)) != cudaSuccess) return e;
+      uint64_t keep = POOL_KEEP;
+      if ((e = cudaMemPoolSetAttribute(np, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+        cudaMemPoolDestroy(np);
+        return e;
+      }
+      pools[dev] = np;
+    }
+    pool = pools[dev];
+  }
+  return cudaMallocFromPoolAsync(p, bytes, pool, stream);
+}
+
+// At most this many elements, a sum runs in one block (no workspace, no
+// grid merge): below it the grid path's fixed steps cost more than the
+// block's longer pass.
+constexpr uint64_t SMALL_SUM_MAX = 16384;
+
+// Per host thread, one pinned and mapped slot that the synchronous sum's
+// kernel writes its result to (no device allocation and no copy per call).
+struct PinnedSlot {
+  void* p = nullptr;
+  ~PinnedSlot() {
+    if (p) cudaFreeHost(p);
+  }
+};
+thread_local PinnedSlot g_slot;
+
+void* result_slot() {
+  if (!g_slot.p) {
+    if (cudaHostAlloc(&g_slot.p, 64, cudaHostAllocPortable | cudaHostAllocMapped) != cudaSuccess) {
+      cudaGetLastError();
+      g_slot.p = nullptr;
+    }
+  }
+  return g_slot.p;
+}
+
 int sm_count() {
   static int cached[64] = {0};
   int dev = 0;
@@ -70,7 +130,7 @@ repro_status validate_env(cudaStream_t stream) {
     if (g_env_state[dev] == 2) return REPRO_ERR_ENV;
   }
   unsigned* d = nullptr;
-  CK(cudaMallocAsync((void**)&d, sizeof(unsigned), stream));
+  CK(ws_alloc((void**)&d, sizeof(unsigned), stream));
   unsigned h = 0xFFFFFFFFu;
   cudaError_t e = launch_env_probe(d, stream);
   if (e == cudaSuccess) e = cudaMemcpyAsync(&h, d, sizeof(unsigned), cudaMemcpyDeviceToHost, stream);
@@ -149,6 +209,11 @@ repro_status sum_async_impl(const T* x, size_t n, int K, cudaStream_t stream, T*
   st = validate_env(stream);
   if (st != REPRO_OK) return st;
   int block = (l && l->block) ? l->block : 256;
+  if ((uint64_t)n <= SMALL_SUM_MAX && !(l && l->grid > 0)) {
+    // one block, no workspace
+    CK(launch_sum_single<T>(x, (int64_t)n, K, result_dev, block, stream));
+    return REPRO_OK;
+  }
   int grid = sum_grid((int64_t)n, block, 4 * (int)(16 / sizeof(T)), sum_blocks_per_sm<T>(K, block),
                       l);   // 4 vectors per thread per iteration, one wave of blocks
   size_t wsb = sum_workspace_bytes(K, grid);
@@ -169,7 +234,7 @@ repro_status sum_async_impl(const T* x, size_t n, int K, cudaStream_t stream, T*
   }
   Scratch ws;
   ws.s = stream;
-  CK(cudaMallocAsync(&ws.p, wsb, stream));
+  CK(ws_alloc(&ws.p, wsb, stream));
   CK(cudaMemsetAsync(ws.p, 0, 256, stream));
   unsigned char* w = (unsigned char*)ws.p;
   if constexpr (sizeof(T) == 8) {
@@ -207,13 +272,23 @@ repro_status sum_sync_impl(const T* x, size_t n, int K, cudaStream_t stream, T* 
   in.s = stream;
   const T* xd = x;
   if (is_host_only(x)) {
-    CK(cudaMallocAsync(&in.p, n * sizeof(T), stream));
+    CK(ws_alloc(&in.p, n * sizeof(T), stream));
     CK(cudaMemcpyAsync(in.p, x, n * sizeof(T), cudaMemcpyHostToDevice, stream));
     xd = (const T*)in.p;
   }
+  // the result goes to this thread's pinned slot (mapped, so the kernel
+  // writes it directly); without one, to device memory and back
+  T* slot = (T*)result_slot();
+  if (slot) {
+    st = sum_async_impl<T>(xd, n, K, stream, slot, nullptr);
+    if (st != REPRO_OK) return st;
+    CK(cudaStreamSynchronize(stream));
+    *result = *(volatile T*)slot;
+    return REPRO_OK;
+  }
   Scratch r;
   r.s = stream;
-  CK(cudaMallocAsync(&r.p, 16, stream));
+  CK(ws_alloc(&r.p, 16, stream));
   st = sum_async_impl<T>(xd, n, K, stream, (T*)r.p, nullptr);
   if (st != REPRO_OK) return st;
   T h;
@@ -235,7 +310,8 @@ repro_status cumsum_impl(const T* in, T* out, size_t n, int K, cudaStream_t stre
   if (st != REPRO_OK) return st;
   Scratch ws;
   ws.s = stream;
-  CK(cudaMallocAsync(&ws.p, cumsum_workspace_bytes<T>((int64_t)n, K), stream));
+  const size_t wsb = cumsum_workspace_bytes<T>((int64_t)n, K);
+  if (wsb) CK(ws_alloc(&ws.p, wsb, stream));   // none for a single tile
   CK(launch_cumsum<T>(in, out, (int64_t)n, K, (unsigned char*)ws.p, l ? l->block : 0, stream));
   return REPRO_OK;
 }
@@ -262,7 +338,7 @@ repro_status compare_impl(const T* x, size_t n, int mode, T* result, cudaStream_
   if (st != REPRO_OK) return st;
   Scratch ws;
   ws.s = stream;
-  CK(cudaMallocAsync(&ws.p, compare_workspace_bytes<T>((int64_t)n, mode), stream));
+  CK(ws_alloc(&ws.p, compare_workspace_bytes<T>((int64_t)n, mode), stream));
   if (mode == 0) CK(cudaMemsetAsync(ws.p, 0, 256, stream));
   CK(launch_compare<T>(x, (int64_t)n, mode, result, (unsigned char*)ws.p, stream));
   return REPRO_OK;

@@ -635,6 +635,15 @@ __device__ void c3_replay_tile(const T* in, T* out, int64_t n, int64_t tile, S3 
   __syncthreads();
 }
 
+// Inputs of at most one tile: the whole cumulative sum in one block, no
+// workspace.
+template <typename T>
+__global__ void __launch_bounds__(C3_BLOCK) c3_single_tile(const T* in, T* out, int64_t n) {
+  __shared__ T sm[C3_TILE + C3_TILE / C3_ITEMS];
+  __shared__ S3 wsm[C3_WARPS];
+  c3_replay_tile<T>(in, out, n, 0, s3_zero(Geom<T>::NB - 3), sm, wsm);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(C3_BLOCK) c3_replay(const T* in, T* out, int64_t n, int64_t ntiles,
                                                       const unsigned char* __restrict__ tloc,
@@ -1076,11 +1085,16 @@ static size_t cf_bytes(int64_t n) {
 
 template <typename T>
 size_t cumsum_k3_workspace_bytes(int64_t n) {
+  if (n <= C3_TILE) return 0;   // one block, no workspace
   return c3_general_bytes<T>(n) + (n >= CF_MIN_N ? cf_bytes<T>(n) : 0);
 }
 
 template <typename T>
 cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, cudaStream_t s) {
+  if (n <= C3_TILE) {
+    c3_single_tile<T><<<1, C3_BLOCK, 0, s>>>(in, out, n);
+    return cudaGetLastError();
+  }
   int64_t nt = (n + C3_TILE - 1) / C3_TILE;
   int64_t nb = (nt + 1023) / 1024;
   unsigned char* wtot = ws;

@@ -10,6 +10,9 @@ namespace repro {
 template <typename T>
 cudaError_t launch_sum(const T* x, int64_t n, int K, unsigned char* ws, T* result, int grid, int block,
                        cudaStream_t s, const unsigned* gate = nullptr);
+// One block, no workspace: the single-block sum for small inputs.
+template <typename T>
+cudaError_t launch_sum_single(const T* x, int64_t n, int K, T* result, int block, cudaStream_t s);
 size_t sum_workspace_bytes(int K, int grid);
 template <typename T>
 int sum_blocks_per_sm(int K, int block);

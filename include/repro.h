@@ -8,9 +8,12 @@
  *  - Pointers: inputs and outputs are caller-owned device pointers (also
  *    managed memory, or host memory as stated per call); the library never
  *    frees them.  Floating-point pointers must be aligned to their element
- *    size.  Temporary device memory is taken from the stream-ordered
- *    allocator (cudaMallocAsync on `stream`) and returned before the call's
- *    work completes on that stream.
+ *    size.  Temporary device memory is taken, stream-ordered on `stream`,
+ *    from a memory pool the library creates per device (it keeps up to
+ *    1 GiB mapped between calls; the process's default pool is not
+ *    touched) and returned before the call's work completes on that stream.
+ *    Small inputs need none: a sum of at most 16384 elements runs in one
+ *    block, a K = 3 cumulative sum of at most 4096 in one tile.
  *  - Streams: work is enqueued on `stream` (0 = legacy default stream).
  *    Calls documented "synchronous" wait for their own work; the others
  *    return once the work is enqueued.
@@ -87,7 +90,10 @@ repro_status repro_validate_environment(cudaStream_t stream);
    the device first).  Synchronous; *result is a host pointer.  n == 0 gives
    +0.0.  Any NaN, or both +Inf and -Inf, gives the canonical quiet NaN
    (0x7fc00000 / 0x7ff8000000000000); otherwise an Inf propagates; an exact
-   zero is +0.0.  Result = correct rounding of the exact binned value. */
+   zero is +0.0.  Result = correct rounding of the exact binned value.  The
+   kernel writes the result to a pinned, mapped host slot owned by the
+   calling host thread (allocated on its first call), so a call on device
+   data makes no device allocation or copy for it. */
 repro_status repro_sum_f32(const float* x, size_t n, int K, cudaStream_t stream, float* result);
 repro_status repro_sum_f64(const double* x, size_t n, int K, cudaStream_t stream, double* result);
 /* Same sum, stream-ordered: x is device-accessible, *result_dev is a device
