@@ -326,8 +326,22 @@ def run_comparisons(api, torch, x32, x64, A, stream):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / reps
 
+    st32 = api.state_new(torch.float32, 3)
+    st64 = api.state_new(torch.float64, 3)
+    r32 = torch.empty(1, dtype=torch.float32, device=x32.device)
+    r64 = torch.empty(1, dtype=torch.float64, device=x64.device)
+
+    def chunked(x, st, r, parts=8):
+        # the binned-state path: init, eight deposits, finalize
+        api.state_init(st, x.dtype, 3, stream)
+        for c in torch.chunk(x, parts):
+            api.state_deposit(st, c, 3, stream)
+        api.state_finalize(st, x.dtype, 3, r, stream)
+
     out = {}
     for name, fn, n in (
+        ("state_8_chunks_f32_1e8", lambda: chunked(x32, st32, r32), N_SUM),
+        ("state_8_chunks_f64_1e8", lambda: chunked(x64, st64, r64), N_SUM),
         ("naive_sum_f32_1e8", lambda: api.compare_sum(x32, "naive"), N_SUM),
         ("pairwise_sum_f32_1e8", lambda: api.compare_sum(x32, "pairwise"), N_SUM),
         ("torch_sum_f32_1e8", lambda: torch.sum(x32), N_SUM),

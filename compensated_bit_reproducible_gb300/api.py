@@ -63,7 +63,13 @@ def lib():
             "stable_var_f32": (I, [P, I64, I64, I, I, P, P, P]),
             "twoterm_var_f32": (I, [P, I64, I64, I, I, P, P]),
             "repro_compensated_chunk": (I, []),
+            "repro_state_bytes": (S, [I]),
         }
+        for t in ("f32", "f64"):
+            sig["repro_state_init_" + t] = (I, [P, I, P])
+            sig["repro_state_deposit_" + t] = (I, [P, P, S, I, P])
+            sig["repro_state_merge_" + t] = (I, [P, P, I, P])
+            sig["repro_state_finalize_" + t] = (I, [P, I, P, P])
         for mode in ("naive", "pairwise", "kahan", "neumaier"):
             for t in ("f32", "f64"):
                 sig["repro_sum_%s_%s" % (mode, t)] = (I, [P, S, P, P])
@@ -209,3 +215,55 @@ def compare_sum(x: torch.Tensor, mode: str, out: torch.Tensor | None = None, str
 
 def compensated_chunk() -> int:
     return int(lib().repro_compensated_chunk())
+
+
+# ------------------------------------------------------------ binned states
+def _tsfx(dtype) -> str:
+    if dtype == torch.float32:
+        return "f32"
+    if dtype == torch.float64:
+        return "f64"
+    raise TypeError("float32 or float64 expected, got %s" % dtype)
+
+
+def state_bytes(K: int = 3) -> int:
+    return int(lib().repro_state_bytes(K))
+
+
+def state_new(dtype, K: int = 3, device=None, stream=None) -> torch.Tensor:
+    """A fresh (empty) binned state for `dtype` sums: a uint8 device tensor."""
+    n = state_bytes(K)
+    if n == 0:
+        raise ReproError(1, "repro_state_bytes")
+    st = torch.empty(n, dtype=torch.uint8, device=device or torch.device("cuda", torch.cuda.current_device()))
+    state_init(st, dtype, K, stream)
+    return st
+
+
+def state_init(state: torch.Tensor, dtype, K: int = 3, stream=None) -> None:
+    sfx = _tsfx(dtype)
+    _check(getattr(lib(), "repro_state_init_" + sfx)(_ptr(state), K, _stream(stream)), "repro_state_init_" + sfx)
+
+
+def state_deposit(state: torch.Tensor, x: torch.Tensor, K: int = 3, stream=None) -> None:
+    sfx = _sfx(x)
+    assert x.is_contiguous()
+    _check(getattr(lib(), "repro_state_deposit_" + sfx)(_ptr(state), _ptr(x), x.numel(), K, _stream(stream)),
+           "repro_state_deposit_" + sfx)
+
+
+def state_merge(dst: torch.Tensor, src: torch.Tensor, dtype, K: int = 3, stream=None) -> None:
+    sfx = _tsfx(dtype)
+    _check(getattr(lib(), "repro_state_merge_" + sfx)(_ptr(dst), _ptr(src), K, _stream(stream)),
+           "repro_state_merge_" + sfx)
+
+
+def state_finalize(state: torch.Tensor, dtype, K: int = 3, out: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """Correctly rounded value of the state, as a one-element device tensor."""
+    sfx = _tsfx(dtype)
+    if out is None:
+        out = torch.empty(1, dtype=dtype, device=state.device)
+    _check(getattr(lib(), "repro_state_finalize_" + sfx)(_ptr(state), K, _ptr(out), _stream(stream)),
+           "repro_state_finalize_" + sfx)
+    return out

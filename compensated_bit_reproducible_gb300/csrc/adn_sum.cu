@@ -128,13 +128,108 @@ __device__ void merge_partials_cg(const unsigned char* base, int np, int K, Stat
   __syncthreads();
 }
 
+// ------------------------------------------------------------ binned states
+// A caller-owned state in device memory (repro_state_* calls): a 32-byte
+// header {I, flags, K, kind, count (64-bit), 0} and K fold sums as 128-bit
+// integers {lo, hi}.  Merging states aligns them to the coarser index (fold k
+// of a state at index Ia moves to k + (Ia - I); the finest ones drop, which
+// is exact because a value inside bin Ia has zero pieces on coarser grids)
+// and adds the folds: the same operation as the grid merge, so any split of
+// the input into deposits and any merge order gives the sum's bits.
+constexpr int ST_HDR = 32;
+constexpr int FL_STATE_BAD = 8;   // K or element type mismatch: finalizes to NaN
+
+template <typename T> __host__ __device__ constexpr int state_kind() { return sizeof(T) == 4 ? 1 : 2; }
+
+__device__ __forceinline__ W128 state_fold(const unsigned char* sp, int K, int idx) {
+  if (idx < 0 || idx >= K) return W128{0, 0};
+  const int64_t* f = (const int64_t*)(sp + ST_HDR) + 2 * idx;
+  return W128{(uint64_t)f[0], f[1]};
+}
+
+// Fold k of a state at index Ifrom expressed at the coarser index I <= Ifrom.
+__device__ __forceinline__ W128 fold_shifted(const W128* F, int K, int Ifrom, int I, int k) {
+  const int src = k - (Ifrom - I);
+  return (src >= 0 && src < K) ? F[src] : W128{0, 0};
+}
+
+// dst := dst + (I, flags, F, count); one thread.  A header whose K or kind
+// differs from the call's only gets the poison flag: its buffer was sized
+// for its own K, so no fold is read or written.
+template <typename T>
+__device__ void state_add(unsigned char* dst, int K, int I, int flags, const W128* F, uint64_t count) {
+  int* h = (int*)dst;
+  if (h[2] != K || h[3] != state_kind<T>()) {
+    h[1] |= FL_STATE_BAD;
+    return;
+  }
+  W128 old[KMAXS_SHIFT];
+  const int Id = h[0];
+  const int fl = h[1] | flags;
+  for (int k = 0; k < K; ++k) old[k] = state_fold(dst, K, k);
+  const int In = min(Id, I);
+  int64_t* f = (int64_t*)(dst + ST_HDR);
+  for (int k = 0; k < K; ++k) {
+    const W128 v = w_add(fold_shifted(old, K, Id, In, k), fold_shifted(F, K, I, In, k));
+    f[2 * k] = (int64_t)v.lo;
+    f[2 * k + 1] = v.hi;
+  }
+  h[0] = In;
+  h[1] = fl;
+  *(unsigned long long*)(dst + 16) += count;
+}
+
+template <typename T>
+__global__ void state_init_kernel(unsigned char* st, int K) {
+  int* h = (int*)st;
+  h[0] = Geom<T>::NB - K;   // the empty state's index
+  h[1] = 0;
+  h[2] = K;
+  h[3] = state_kind<T>();
+  ((unsigned long long*)st)[2] = 0ull;
+  ((unsigned long long*)st)[3] = 0ull;
+  int64_t* f = (int64_t*)(st + ST_HDR);
+  for (int k = 0; k < 2 * K; ++k) f[k] = 0;
+}
+
+template <typename T>
+__global__ void state_merge_kernel(unsigned char* dst, const unsigned char* src, int K) {
+  W128 F[KMAXS_SHIFT];
+  const int* h = (const int*)src;
+  if (h[2] != K || h[3] != state_kind<T>()) {   // src sized for another K: no fold is read
+    const int* hd = (const int*)dst;
+    if (hd[2] == K && hd[3] == state_kind<T>()) ((int*)dst)[1] |= FL_STATE_BAD;
+    return;
+  }
+  for (int k = 0; k < K; ++k) F[k] = state_fold(src, K, k);
+  state_add<T>(dst, K, h[0], h[1], F, *(const unsigned long long*)(src + 16));
+}
+
+template <typename T>
+__global__ void state_finalize_kernel(const unsigned char* st, int K, uint64_t capacity, T* result) {
+  const int* h = (const int*)st;
+  if (h[2] != K || h[3] != state_kind<T>() || (h[1] & FL_STATE_BAD) ||
+      *(const unsigned long long*)(st + 16) > capacity) {
+    *result = canonical_nan<T>();
+    return;
+  }
+  State<KMax<T>::V> s;
+  s.I = h[0];
+  s.flags = h[1];
+  for (int k = 0; k < K; ++k) s.F[k] = state_fold(st, K, k);
+  *result = convert_state<T, KMax<T>::V>(s, K);
+}
+
 // Workspace: [0, 256) ticket counter (zero at launch); [256, ...) partials.
 // With a gate, the kernel runs only if *gate is nonzero (it is the fallback
 // of a faster path that decides on the device).
+// With `state`, the merged result is added to that binned state (no
+// conversion; `result` unused).
 template <typename T, int KT, int U>
 __global__ void __launch_bounds__(1024) adn_sum_kernel(const T* __restrict__ x, int64_t n, int K,
                                                        unsigned char* __restrict__ ws, T* __restrict__ result,
-                                                       const unsigned* __restrict__ gate) {
+                                                       const unsigned* __restrict__ gate,
+                                                       unsigned char* __restrict__ state) {
   if (gate) {
     // launched as a programmatic dependent of the fast path: wait until that
     // grid has completed and its writes are visible
@@ -164,7 +259,8 @@ __global__ void __launch_bounds__(1024) adn_sum_kernel(const T* __restrict__ x, 
   __threadfence();
   merge_partials_cg<N>(parts, gridDim.x, K, &st);
   if (threadIdx.x == 0) {
-    if constexpr (KT != 0) *result = convert_fast<T, KT>(st.I, st.flags, st.F);
+    if (state) state_add<T>(state, K, st.I, st.flags, st.F, (uint64_t)n);
+    else if constexpr (KT != 0) *result = convert_fast<T, KT>(st.I, st.flags, st.F);
     else *result = convert_state<T, N>(st, K);
     *ticket = 0u;
   }
@@ -175,7 +271,7 @@ __global__ void __launch_bounds__(1024) adn_sum_kernel(const T* __restrict__ x, 
 // are the same as the grid path's.
 template <typename T, int KT, int U>
 __global__ void __launch_bounds__(1024) adn_sum_single(const T* __restrict__ x, int64_t n, int K,
-                                                       T* __restrict__ result) {
+                                                       T* __restrict__ result, unsigned char* __restrict__ state) {
   typedef typename AccOf<T, KT>::type Acc;
   constexpr int N = Acc::N;
   Acc acc;
@@ -185,7 +281,8 @@ __global__ void __launch_bounds__(1024) adn_sum_single(const T* __restrict__ x, 
   State<N> st;
   block_merge<N>(acc.I, acc.flags, acc.L, K, &st);
   if (threadIdx.x == 0) {
-    if constexpr (KT != 0) *result = convert_fast<T, KT>(st.I, st.flags, st.F);
+    if (state) state_add<T>(state, K, st.I, st.flags, st.F, (uint64_t)n);
+    else if constexpr (KT != 0) *result = convert_fast<T, KT>(st.I, st.flags, st.F);
     else *result = convert_state<T, N>(st, K);
   }
 }
@@ -238,10 +335,10 @@ __global__ void __launch_bounds__(256) segsum_cols_kernel(const float* __restric
 // ------------------------------------------------------------------ launch
 template <typename T, int KT>
 static cudaError_t launch_sum_k(const T* x, int64_t n, int K, unsigned char* ws, T* result, int grid, int block,
-                                const unsigned* gate, cudaStream_t s) {
+                                const unsigned* gate, cudaStream_t s, unsigned char* state = nullptr) {
   constexpr int U = 4;
   if (!gate) {
-    adn_sum_kernel<T, KT, U><<<grid, block, 0, s>>>(x, n, K, ws, result, gate);
+    adn_sum_kernel<T, KT, U><<<grid, block, 0, s>>>(x, n, K, ws, result, gate, state);
     return cudaGetLastError();
   }
   // gated fallback: programmatic dependent launch overlaps its launch with
@@ -256,7 +353,7 @@ static cudaError_t launch_sum_k(const T* x, int64_t n, int K, unsigned char* ws,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, adn_sum_kernel<T, KT, U>, x, n, K, ws, result, gate);
+  return cudaLaunchKernelEx(&cfg, adn_sum_kernel<T, KT, U>, x, n, K, ws, result, gate, state);
 }
 
 template <typename T>
@@ -275,23 +372,60 @@ cudaError_t launch_sum(const T* x, int64_t n, int K, unsigned char* ws, T* resul
 }
 
 template <typename T>
-cudaError_t launch_sum_single(const T* x, int64_t n, int K, T* result, int block, cudaStream_t s) {
+cudaError_t launch_sum_single(const T* x, int64_t n, int K, T* result, int block, cudaStream_t s,
+                              unsigned char* state) {
   constexpr int U = 1;
   switch (K) {
-    case 2: adn_sum_single<T, 2, U><<<1, block, 0, s>>>(x, n, K, result); break;
-    case 3: adn_sum_single<T, 3, U><<<1, block, 0, s>>>(x, n, K, result); break;
-    case 4: adn_sum_single<T, 4, U><<<1, block, 0, s>>>(x, n, K, result); break;
-    case 5: adn_sum_single<T, 5, U><<<1, block, 0, s>>>(x, n, K, result); break;
-    case 6: adn_sum_single<T, 6, U><<<1, block, 0, s>>>(x, n, K, result); break;
-    case 7: adn_sum_single<T, 7, U><<<1, block, 0, s>>>(x, n, K, result); break;
-    case 8: adn_sum_single<T, 8, U><<<1, block, 0, s>>>(x, n, K, result); break;
-    default: adn_sum_single<T, 0, U><<<1, block, 0, s>>>(x, n, K, result); break;
+    case 2: adn_sum_single<T, 2, U><<<1, block, 0, s>>>(x, n, K, result, state); break;
+    case 3: adn_sum_single<T, 3, U><<<1, block, 0, s>>>(x, n, K, result, state); break;
+    case 4: adn_sum_single<T, 4, U><<<1, block, 0, s>>>(x, n, K, result, state); break;
+    case 5: adn_sum_single<T, 5, U><<<1, block, 0, s>>>(x, n, K, result, state); break;
+    case 6: adn_sum_single<T, 6, U><<<1, block, 0, s>>>(x, n, K, result, state); break;
+    case 7: adn_sum_single<T, 7, U><<<1, block, 0, s>>>(x, n, K, result, state); break;
+    case 8: adn_sum_single<T, 8, U><<<1, block, 0, s>>>(x, n, K, result, state); break;
+    default: adn_sum_single<T, 0, U><<<1, block, 0, s>>>(x, n, K, result, state); break;
   }
   return cudaGetLastError();
 }
 
-template cudaError_t launch_sum_single<float>(const float*, int64_t, int, float*, int, cudaStream_t);
-template cudaError_t launch_sum_single<double>(const double*, int64_t, int, double*, int, cudaStream_t);
+template cudaError_t launch_sum_single<float>(const float*, int64_t, int, float*, int, cudaStream_t,
+                                              unsigned char*);
+template cudaError_t launch_sum_single<double>(const double*, int64_t, int, double*, int, cudaStream_t,
+                                               unsigned char*);
+
+// ------------------------------------------------------------ state calls
+template <typename T>
+cudaError_t launch_state_deposit(const T* x, int64_t n, int K, unsigned char* ws, unsigned char* state, int grid,
+                                 int block, cudaStream_t s) {
+  switch (K) {
+    case 2: return launch_sum_k<T, 2>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
+    case 3: return launch_sum_k<T, 3>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
+    case 4: return launch_sum_k<T, 4>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
+    case 5: return launch_sum_k<T, 5>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
+    case 6: return launch_sum_k<T, 6>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
+    case 7: return launch_sum_k<T, 7>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
+    case 8: return launch_sum_k<T, 8>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
+    default: return launch_sum_k<T, 0>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
+  }
+}
+
+template <typename T>
+cudaError_t launch_state_op(int op, unsigned char* dst, const unsigned char* src, int K, uint64_t capacity,
+                            T* result, cudaStream_t s) {
+  if (op == 0) state_init_kernel<T><<<1, 1, 0, s>>>(dst, K);
+  else if (op == 1) state_merge_kernel<T><<<1, 1, 0, s>>>(dst, src, K);
+  else state_finalize_kernel<T><<<1, 1, 0, s>>>(src, K, capacity, result);
+  return cudaGetLastError();
+}
+
+template cudaError_t launch_state_deposit<float>(const float*, int64_t, int, unsigned char*, unsigned char*, int, int,
+                                                 cudaStream_t);
+template cudaError_t launch_state_deposit<double>(const double*, int64_t, int, unsigned char*, unsigned char*, int,
+                                                  int, cudaStream_t);
+template cudaError_t launch_state_op<float>(int, unsigned char*, const unsigned char*, int, uint64_t, float*,
+                                            cudaStream_t);
+template cudaError_t launch_state_op<double>(int, unsigned char*, const unsigned char*, int, uint64_t, double*,
+                                             cudaStream_t);
 
 template cudaError_t launch_sum<float>(const float*, int64_t, int, unsigned char*, float*, int, int, cudaStream_t,
                                        const unsigned*);

@@ -346,6 +346,61 @@ repro_status compare_impl(const T* x, size_t n, int mode, T* result, cudaStream_
 
 }  // namespace
 
+// ------------------------------------------------------------ binned states
+constexpr size_t STATE_HDR = 32;
+
+bool state_ptr_ok(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
+
+template <typename T>
+repro_status state_init_impl(void* state, int K, cudaStream_t stream) {
+  if (K < 2 || K > Lim<T>::MAXK || !state_ptr_ok(state)) return REPRO_ERR_INVALID_ARG;
+  repro_status st = validate_env(stream);
+  if (st != REPRO_OK) return st;
+  CK(launch_state_op<T>(0, (unsigned char*)state, nullptr, K, 0, nullptr, stream));
+  return REPRO_OK;
+}
+
+template <typename T>
+repro_status state_deposit_impl(void* state, const T* x, size_t n, int K, cudaStream_t stream) {
+  repro_status st = check_sum_args(x, n, K);
+  if (st != REPRO_OK) return st;
+  if (!state_ptr_ok(state)) return REPRO_ERR_INVALID_ARG;
+  if (n == 0) return REPRO_OK;
+  st = validate_env(stream);
+  if (st != REPRO_OK) return st;
+  const int block = 256;
+  if ((uint64_t)n <= SMALL_SUM_MAX) {
+    CK(launch_sum_single<T>(x, (int64_t)n, K, nullptr, block, stream, (unsigned char*)state));
+    return REPRO_OK;
+  }
+  const int grid = sum_grid((int64_t)n, block, 4 * (int)(16 / sizeof(T)), sum_blocks_per_sm<T>(K, block), nullptr);
+  Scratch ws;
+  ws.s = stream;
+  CK(ws_alloc(&ws.p, sum_workspace_bytes(K, grid), stream));
+  CK(cudaMemsetAsync(ws.p, 0, 256, stream));
+  CK(launch_state_deposit<T>(x, (int64_t)n, K, (unsigned char*)ws.p, (unsigned char*)state, grid, block, stream));
+  return REPRO_OK;
+}
+
+template <typename T>
+repro_status state_merge_impl(void* dst, const void* src, int K, cudaStream_t stream) {
+  if (K < 2 || K > Lim<T>::MAXK || !state_ptr_ok(dst) || !state_ptr_ok(src)) return REPRO_ERR_INVALID_ARG;
+  repro_status st = validate_env(stream);
+  if (st != REPRO_OK) return st;
+  CK(launch_state_op<T>(1, (unsigned char*)dst, (const unsigned char*)src, K, 0, nullptr, stream));
+  return REPRO_OK;
+}
+
+template <typename T>
+repro_status state_finalize_impl(const void* state, int K, T* result_dev, cudaStream_t stream) {
+  if (K < 2 || K > Lim<T>::MAXK || !state_ptr_ok(state) || !result_dev || !aligned(result_dev))
+    return REPRO_ERR_INVALID_ARG;
+  repro_status st = validate_env(stream);
+  if (st != REPRO_OK) return st;
+  CK(launch_state_op<T>(2, nullptr, (const unsigned char*)state, K, Lim<T>::COUNT, result_dev, stream));
+  return REPRO_OK;
+}
+
 extern "C" {
 
 const char* repro_strerror(repro_status s) {
@@ -447,5 +502,30 @@ repro_status repro_sum_neumaier_f64(const double* x, size_t n, double* r, cudaSt
   return compare_impl<double>(x, n, 3, r, s);
 }
 int repro_compensated_chunk(void) { return COMPENSATED_CHUNK; }
+
+size_t repro_state_bytes(int K) {
+  if (K < 2 || K > MAXK_F64) return 0;
+  return STATE_HDR + 16 * (size_t)K;
+}
+repro_status repro_state_init_f32(void* state, int K, cudaStream_t s) { return state_init_impl<float>(state, K, s); }
+repro_status repro_state_init_f64(void* state, int K, cudaStream_t s) { return state_init_impl<double>(state, K, s); }
+repro_status repro_state_deposit_f32(void* state, const float* x, size_t n, int K, cudaStream_t s) {
+  return state_deposit_impl<float>(state, x, n, K, s);
+}
+repro_status repro_state_deposit_f64(void* state, const double* x, size_t n, int K, cudaStream_t s) {
+  return state_deposit_impl<double>(state, x, n, K, s);
+}
+repro_status repro_state_merge_f32(void* dst, const void* src, int K, cudaStream_t s) {
+  return state_merge_impl<float>(dst, src, K, s);
+}
+repro_status repro_state_merge_f64(void* dst, const void* src, int K, cudaStream_t s) {
+  return state_merge_impl<double>(dst, src, K, s);
+}
+repro_status repro_state_finalize_f32(const void* state, int K, float* result_dev, cudaStream_t s) {
+  return state_finalize_impl<float>(state, K, result_dev, s);
+}
+repro_status repro_state_finalize_f64(const void* state, int K, double* result_dev, cudaStream_t s) {
+  return state_finalize_impl<double>(state, K, result_dev, s);
+}
 
 }  // extern "C"

@@ -12,7 +12,19 @@ cudaError_t launch_sum(const T* x, int64_t n, int K, unsigned char* ws, T* resul
                        cudaStream_t s, const unsigned* gate = nullptr);
 // One block, no workspace: the single-block sum for small inputs.
 template <typename T>
-cudaError_t launch_sum_single(const T* x, int64_t n, int K, T* result, int block, cudaStream_t s);
+cudaError_t launch_sum_single(const T* x, int64_t n, int K, T* result, int block, cudaStream_t s,
+                              unsigned char* state = nullptr);
+
+// Binned states (32-byte header + K 128-bit folds in device memory).
+// Deposit: the grid sum of x merged into *state (workspace as for
+// launch_sum).  op 0: init dst; 1: merge src into dst; 2: finalize src to
+// *result (canonical NaN past `capacity` elements or on a K/type mismatch).
+template <typename T>
+cudaError_t launch_state_deposit(const T* x, int64_t n, int K, unsigned char* ws, unsigned char* state, int grid,
+                                 int block, cudaStream_t s);
+template <typename T>
+cudaError_t launch_state_op(int op, unsigned char* dst, const unsigned char* src, int K, uint64_t capacity,
+                            T* result, cudaStream_t s);
 size_t sum_workspace_bytes(int K, int grid);
 template <typename T>
 int sum_blocks_per_sm(int K, int block);

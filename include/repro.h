@@ -118,6 +118,39 @@ repro_status repro_sum_f64_async(const double* x, size_t n, int K, cudaStream_t 
    probe) and waits for it; make it before any stream capture. */
 repro_status repro_sum_f32_noalloc(const float* x, size_t n, int K, cudaStream_t stream, float* result_dev);
 
+/* ---- binned states ("How It Works": deposit and merge; "API Reference":
+   chunked sums) ------------------------------------------------------------ */
+/* A binned state holds everything deposited into it as {bin index, K exact
+   fold sums, Inf/NaN flags, element count}.  It lives in caller-owned device
+   memory of repro_state_bytes(K) bytes, 16-byte aligned; the layout is a
+   32-byte header (int32 index, int32 flags, int32 K, int32 type 1 = float /
+   2 = double, uint64 count, 8 zero bytes) followed by K fold sums, each a
+   little-endian 128-bit integer (low 64 bits first), in units of their
+   fold's grid.  Depositing chunks and merging states in any split and any
+   order, then finalizing, gives the same bits as repro_sum of the whole
+   input: the merge aligns both states to the coarser index and adds the
+   folds exactly.  States can be copied between devices and merged there
+   (the layout has no pointers).  Calls that touch one state must be ordered
+   (one stream, or events).  All calls are stream-ordered and use the
+   same K and element type as the state's init; a different K or type, or
+   more than the capacity (repro_max_count_*) elements in total, makes
+   finalize give the canonical NaN.  Errors: REPRO_ERR_INVALID_ARG for K out
+   of range, a null or misaligned state / result / input pointer;
+   REPRO_ERR_CAPACITY for one deposit above the capacity. */
+size_t repro_state_bytes(int K);   /* 32 + 16 K; 0 for K outside 2..52 */
+repro_status repro_state_init_f32(void* state, int K, cudaStream_t stream);
+repro_status repro_state_init_f64(void* state, int K, cudaStream_t stream);
+/* state += binned x[0..n) (x device-accessible; n == 0 does nothing). */
+repro_status repro_state_deposit_f32(void* state, const float* x, size_t n, int K, cudaStream_t stream);
+repro_status repro_state_deposit_f64(void* state, const double* x, size_t n, int K, cudaStream_t stream);
+/* dst += src (dst == src doubles the state). */
+repro_status repro_state_merge_f32(void* dst, const void* src, int K, cudaStream_t stream);
+repro_status repro_state_merge_f64(void* dst, const void* src, int K, cudaStream_t stream);
+/* *result_dev (device pointer) = correctly rounded value of the state, the
+   same special-value and signed-zero rules as repro_sum. */
+repro_status repro_state_finalize_f32(const void* state, int K, float* result_dev, cudaStream_t stream);
+repro_status repro_state_finalize_f64(const void* state, int K, double* result_dev, cudaStream_t stream);
+
 /* ---- binned cumulative sums ("How It Works", cumsum paragraph; "API
    Reference": cumsum) ------------------------------------------------------ */
 /* out[i] = reproducible sum of in[0..i] (each prefix with its own bin

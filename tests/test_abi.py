@@ -77,6 +77,34 @@ def test_argument_errors_before_pointer_access(L):
     assert L.repro_segsum_f32(bogus, 4, 4, 1, 22, bogus, None) == 1
 
 
+def test_state_calls_check_arguments_first(L):
+    P = ctypes.c_void_p
+    assert L.repro_state_bytes(3) == 32 + 48
+    assert L.repro_state_bytes(52) == 32 + 16 * 52
+    assert L.repro_state_bytes(1) == 0 and L.repro_state_bytes(53) == 0
+    good = P(0x100)   # aligned, never dereferenced: every case below fails first
+    odd = P(0x108)    # not 16-byte aligned
+    for t in ("f32", "f64"):
+        init = getattr(L, "repro_state_init_" + t)
+        dep = getattr(L, "repro_state_deposit_" + t)
+        merge = getattr(L, "repro_state_merge_" + t)
+        fin = getattr(L, "repro_state_finalize_" + t)
+        assert init(good, 1, None) == 1
+        assert init(None, 3, None) == 1
+        assert init(odd, 3, None) == 1
+        assert dep(good, None, 10, 3, None) == 1
+        assert dep(odd, good, 10, 3, None) == 1
+        assert dep(good, good, 10, 0, None) == 1
+        cap = 4294966785 if t == "f32" else 9223372036854773761
+        assert dep(good, None, cap, 3, None) == 2
+        assert merge(good, None, 3, None) == 1
+        assert merge(odd, good, 3, None) == 1
+        assert fin(good, 3, None, None) == 1
+        assert fin(odd, 3, good, None) == 1
+    assert L.repro_state_init_f32(good, 22, None) == 1     # float folds: K <= 21
+    assert L.repro_state_init_f64(good, 53, None) == 1
+
+
 def test_strerror(L):
     for s in range(7):
         assert L.repro_strerror(s)

@@ -1,0 +1,128 @@
+"""Binned states: deposits of any split of the input, merged in any order
+and finalized, equal the oracle's sum of the whole input bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from compensated_bit_reproducible_gb300 import api, inputs
+from tests.gpu_util import dev, same_bits, to_dev
+
+pytestmark = pytest.mark.gpu
+F32, F64 = np.float32, np.float64
+TD = {F32: torch.float32, F64: torch.float64}
+
+
+def data(dt, n, seed):
+    return inputs.normal_f32(n, seed=seed, spikes=True) if dt == F32 else inputs.wide_f64(n, seed=seed)
+
+
+def split_points(n, rng, big):
+    """Random cut points: tiny chunks, empty ones, and (if big) chunks above
+    the one-block size, so both deposit paths run."""
+    cuts = set(rng.integers(0, n, 12).tolist()) | {0, n}
+    if big:
+        cuts |= {min(n, 20000), min(n, 60000)}
+    cuts |= {c + 1 for c in list(cuts) if c + 1 < n}   # one-element chunks
+    return sorted(cuts)
+
+
+def deposit_all(x, K, cuts, state=None):
+    t = to_dev(x)
+    st = state if state is not None else api.state_new(t.dtype, K)
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        api.state_deposit(st, t[a:b], K)
+    api.state_deposit(st, t[:0], K)   # empty deposit: no effect
+    return st
+
+
+def final(st, dt, K):
+    return api.state_finalize(st, TD[dt], K).cpu().numpy()[0]
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+@pytest.mark.parametrize("K", [2, 3, 6, 9])
+def test_random_splits_equal_the_whole(dt, K):
+    dev()
+    rng = np.random.default_rng(K)
+    x = data(dt, 100_003, 50 + K)
+    want = oracle.adn_sum(x, K, "fp")
+    for rep in range(3):
+        st = deposit_all(x, K, split_points(x.size, rng, big=True))
+        assert same_bits(final(st, dt, K), want), rep
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_shards_merged_in_any_order(dt):
+    """Four 'ranks' each deposit a contiguous shard; merging the four states
+    in different tree shapes and orders gives the whole input's sum."""
+    dev()
+    rng = np.random.default_rng(3)
+    x = data(dt, 80_000, 61)
+    want = oracle.adn_sum(x, 3, "fp")
+    q = np.array_split(np.arange(x.size), 4)
+    for order in ([0, 1, 2, 3], [3, 2, 1, 0], [2, 0, 3, 1]):
+        sts = [deposit_all(x[idx], 3, [0, idx.size]) for idx in q]
+        api.state_merge(sts[order[0]], sts[order[1]], TD[dt], 3)
+        api.state_merge(sts[order[2]], sts[order[3]], TD[dt], 3)
+        api.state_merge(sts[order[2]], sts[order[0]], TD[dt], 3)
+        assert same_bits(final(sts[order[2]], dt, 3), want), order
+    # a copy of a state (bytes moved elsewhere) merges like the original
+    s = deposit_all(x, 3, [0, x.size])
+    c = s.clone()
+    api.state_merge(c, s, TD[dt], 3)
+    assert same_bits(final(c, dt, 3), oracle.adn_sum(np.concatenate([x, x]), 3, "fp"))
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_index_raise_between_deposits(dt):
+    dev()
+    small = data(dt, 30_000, 70) * (dt(1e-9) if dt == F32 else 1e-30)
+    large = data(dt, 30_000, 71)
+    for first, second in ((small, large), (large, small)):
+        x = np.concatenate([first, second])
+        st = deposit_all(first, 3, [0, first.size])
+        deposit_all(second, 3, [0, 9, second.size], state=st)
+        assert same_bits(final(st, dt, 3), oracle.adn_sum(x, 3, "fp"))
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_specials_across_deposits(dt):
+    dev()
+    b = data(dt, 9000, 72)
+    pinf, ninf, nan = b.copy(), b.copy(), b.copy()
+    pinf[5] = np.inf
+    ninf[7] = -np.inf
+    nan[11] = np.nan
+    for parts, expect in (([b, pinf, b], "pinf"), ([ninf, b], "ninf"), ([pinf, b, ninf], "nan"), ([b, nan], "nan")):
+        st = api.state_new(TD[dt], 3)
+        for p in parts:
+            api.state_deposit(st, to_dev(p), 3)
+        got = final(st, dt, 3)
+        want = oracle.adn_sum(np.concatenate(parts), 3, "fp")
+        assert same_bits(got, want), expect
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_empty_and_zero_states(dt):
+    dev()
+    st = api.state_new(TD[dt], 3)
+    got = final(st, dt, 3)
+    assert got == 0 and not np.signbit(got)
+    api.state_deposit(st, to_dev(-np.zeros(1000, dt)), 3)
+    got = final(st, dt, 3)
+    assert got == 0 and not np.signbit(got)
+
+
+def test_mismatched_k_or_type_finalizes_to_nan():
+    dev()
+    x = to_dev(data(F64, 1000, 73))
+    st = api.state_new(torch.float64, 3)
+    api.state_deposit(st, x, 4)          # K differs from the init
+    assert np.isnan(final(st, F64, 3))
+    a = api.state_new(torch.float32, 3)
+    b = api.state_new(torch.float64, 3)
+    api.state_merge(a, b, torch.float32, 3)   # a double state merged as float
+    assert np.isnan(final(a, F32, 3))
+    c = api.state_new(torch.float64, 3)
+    assert np.isnan(final(c, F64, 2))   # finalized with another K
