@@ -326,6 +326,8 @@ def run_comparisons(api, torch, x32, x64, A, stream):
         torch.cuda.synchronize()
         return a.elapsed_time(b) / reps
 
+    A64 = A.double()
+    AC = A.view(torch.complex64)   # [4096, 2048] complex pairs of the same floats
     st32 = api.state_new(torch.float32, 3)
     st64 = api.state_new(torch.float64, 3)
     r32 = torch.empty(1, dtype=torch.float32, device=x32.device)
@@ -350,6 +352,18 @@ def run_comparisons(api, torch, x32, x64, A, stream):
         ("torch_cumsum_f32_1e8", lambda: torch.cumsum(x32, 0), N_SUM),
         ("torch_cumsum_f64_1e8", lambda: torch.cumsum(x64, 0), N_SUM),
         ("twoterm_var_f32_4096x4096", lambda: api.twoterm_var(A, axis=1, ddof=1), ROWS * COLS),
+        ("var_variant2_plain_no_twoterm_f32_4096x4096",
+         lambda: api.stable_var(A, axis=1, ddof=1, with_mean=False, variant=2), ROWS * COLS),
+        ("var_variant3_plain_f32_4096x4096",
+         lambda: api.stable_var(A, axis=1, ddof=1, with_mean=False, variant=3), ROWS * COLS),
+        ("var_variant4_reference_twosum_f32_4096x4096",
+         lambda: api.stable_var(A, axis=1, ddof=1, with_mean=False, variant=4), ROWS * COLS),
+        ("var_variant5_no_twoterm_f32_4096x4096",
+         lambda: api.stable_var(A, axis=1, ddof=1, with_mean=False, variant=5), ROWS * COLS),
+        ("var_variant6_kahan_f32_4096x4096",
+         lambda: api.stable_var(A, axis=1, ddof=1, with_mean=False, variant=6), ROWS * COLS),
+        ("var_f64_4096x4096", lambda: api.stable_var(A64, axis=1, ddof=1, with_mean=False), ROWS * COLS),
+        ("var_c64_4096x2048", lambda: api.stable_var(AC, axis=1, ddof=1, with_mean=False), ROWS * COLS // 2),
         ("torch_var_f32_4096x4096", lambda: torch.var(A, dim=1), ROWS * COLS),
     ):
         ms = timed(fn)

@@ -62,6 +62,9 @@ def lib():
             "repro_segsum_f32": (I, [P, I64, I64, I, I, P, P]),
             "stable_var_f32": (I, [P, I64, I64, I, I, P, P, P]),
             "twoterm_var_f32": (I, [P, I64, I64, I, I, P, P]),
+            "stable_var_f64": (I, [P, I64, I64, I, I, P, P, P]),
+            "stable_var_c64": (I, [P, I64, I64, I, I, P, P, P]),
+            "stable_var_f32_variant": (I, [P, I64, I64, I, I, I, P, P, P]),
             "repro_compensated_chunk": (I, []),
             "repro_state_bytes": (S, [I]),
         }
@@ -178,17 +181,32 @@ def repro_segsum(x: torch.Tensor, axis: int = 1, K: int = 3, out: torch.Tensor |
 
 # ------------------------------------------------------------------ variance
 def stable_var(x: torch.Tensor, axis: int = 1, ddof: int = 0, out=None, mean_out=None, with_mean: bool = True,
-               stream=None):
-    """Float32 variance kernel: (var, mean) per slice along `axis`."""
-    assert x.is_cuda and x.dtype == torch.float32 and x.dim() == 2 and x.is_contiguous()
+               stream=None, variant: int = 0):
+    """Variance kernel: (var, mean) per slice along `axis` of a 2-D float32,
+    float64 or complex64 tensor.  `variant` (float32 only) selects one of the
+    section 4 step changes (0 = the kernel)."""
+    assert x.is_cuda and x.dim() == 2 and x.is_contiguous()
     rows, cols = x.shape
     ns = rows if axis == 1 else cols
+    vdt = {torch.float32: torch.float32, torch.float64: torch.float64, torch.complex64: torch.float32}[x.dtype]
     if out is None:
-        out = torch.empty(ns, dtype=torch.float32, device=x.device)
+        out = torch.empty(ns, dtype=vdt, device=x.device)
     if with_mean and mean_out is None:
-        mean_out = torch.empty(ns, dtype=torch.float32, device=x.device)
+        mean_out = torch.empty(ns, dtype=x.dtype, device=x.device)
     mp = _ptr(mean_out) if with_mean else ctypes.c_void_p(0)
-    _check(lib().stable_var_f32(_ptr(x), rows, cols, axis, ddof, _ptr(out), mp, _stream(stream)), "stable_var_f32")
+    st = _stream(stream)
+    if x.dtype == torch.float32:
+        if variant:
+            rc = lib().stable_var_f32_variant(_ptr(x), rows, cols, axis, ddof, variant, _ptr(out), mp, st)
+            _check(rc, "stable_var_f32_variant")
+        else:
+            _check(lib().stable_var_f32(_ptr(x), rows, cols, axis, ddof, _ptr(out), mp, st), "stable_var_f32")
+    elif x.dtype == torch.float64:
+        assert variant == 0
+        _check(lib().stable_var_f64(_ptr(x), rows, cols, axis, ddof, _ptr(out), mp, st), "stable_var_f64")
+    else:
+        assert variant == 0
+        _check(lib().stable_var_c64(_ptr(x), rows, cols, axis, ddof, _ptr(out), mp, st), "stable_var_c64")
     return out, mean_out
 
 

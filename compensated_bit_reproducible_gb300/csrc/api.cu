@@ -316,17 +316,50 @@ repro_status cumsum_impl(const T* in, T* out, size_t n, int K, cudaStream_t stre
   return REPRO_OK;
 }
 
-repro_status var_impl(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out, float* mean,
-                      int twoterm, cudaStream_t stream) {
+// Shape checks shared by the variance calls; n must be exact in the element
+// type (2^24 for float32, 2^53 for float64).
+repro_status var_shape_ok(int64_t rows, int64_t cols, int axis, int ddof, int64_t nmax) {
   if (axis != 0 && axis != 1) return REPRO_ERR_INVALID_ARG;
   if (rows <= 0 || cols <= 0) return REPRO_ERR_INVALID_ARG;
   int64_t n = axis == 1 ? cols : rows;
   if (ddof < 0 || ddof >= n) return REPRO_ERR_INVALID_ARG;
-  if (n > (1ll << 24)) return REPRO_ERR_INVALID_ARG;   // n must be exact in float32
-  if (!x || !out || !aligned(x) || !aligned(out) || (mean && !aligned(mean))) return REPRO_ERR_INVALID_ARG;
-  repro_status st = validate_env(stream);
+  if (n > nmax) return REPRO_ERR_INVALID_ARG;
+  return REPRO_OK;
+}
+
+repro_status var_impl(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out, float* mean,
+                      int variant, cudaStream_t stream) {
+  repro_status st = var_shape_ok(rows, cols, axis, ddof, 1ll << 24);
   if (st != REPRO_OK) return st;
-  CK(launch_var(x, rows, cols, axis, ddof, out, mean, twoterm, nullptr, stream));
+  if (variant < 0 || variant > 6) return REPRO_ERR_INVALID_ARG;
+  if (!x || !out || !aligned(x) || !aligned(out) || (mean && !aligned(mean))) return REPRO_ERR_INVALID_ARG;
+  st = validate_env(stream);
+  if (st != REPRO_OK) return st;
+  CK(launch_var(x, rows, cols, axis, ddof, out, mean, variant, nullptr, stream));
+  return REPRO_OK;
+}
+
+repro_status var_f64_impl(const double* x, int64_t rows, int64_t cols, int axis, int ddof, double* out,
+                          double* mean, cudaStream_t stream) {
+  repro_status st = var_shape_ok(rows, cols, axis, ddof, 1ll << 53);
+  if (st != REPRO_OK) return st;
+  if (!x || !out || !aligned(x) || !aligned(out) || (mean && !aligned(mean))) return REPRO_ERR_INVALID_ARG;
+  st = validate_env(stream);
+  if (st != REPRO_OK) return st;
+  CK(launch_var_f64(x, rows, cols, axis, ddof, out, mean, stream));
+  return REPRO_OK;
+}
+
+repro_status var_c64_impl(const float* z, int64_t rows, int64_t cols, int axis, int ddof, float* out, float* mean,
+                          cudaStream_t stream) {
+  repro_status st = var_shape_ok(rows, cols, axis, ddof, 1ll << 24);
+  if (st != REPRO_OK) return st;
+  // complex64: 8-byte pairs
+  if (!z || !out || ((uintptr_t)z & 7u) || !aligned(out) || (mean && ((uintptr_t)mean & 7u)))
+    return REPRO_ERR_INVALID_ARG;
+  st = validate_env(stream);
+  if (st != REPRO_OK) return st;
+  CK(launch_var_c64(z, rows, cols, axis, ddof, out, mean, stream));
   return REPRO_OK;
 }
 
@@ -475,6 +508,18 @@ repro_status stable_var_f32(const float* x, int64_t rows, int64_t cols, int axis
 repro_status twoterm_var_f32(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out,
                              cudaStream_t s) {
   return var_impl(x, rows, cols, axis, ddof, out, nullptr, 1, s);
+}
+repro_status stable_var_f32_variant(const float* x, int64_t rows, int64_t cols, int axis, int ddof, int variant,
+                                    float* out, float* mean_out, cudaStream_t s) {
+  return var_impl(x, rows, cols, axis, ddof, out, mean_out, variant, s);
+}
+repro_status stable_var_f64(const double* x, int64_t rows, int64_t cols, int axis, int ddof, double* out,
+                            double* mean_out, cudaStream_t s) {
+  return var_f64_impl(x, rows, cols, axis, ddof, out, mean_out, s);
+}
+repro_status stable_var_c64(const float* z, int64_t rows, int64_t cols, int axis, int ddof, float* out,
+                            float* mean_out, cudaStream_t s) {
+  return var_c64_impl(z, rows, cols, axis, ddof, out, mean_out, s);
 }
 
 repro_status repro_sum_naive_f32(const float* x, size_t n, float* r, cudaStream_t s) {

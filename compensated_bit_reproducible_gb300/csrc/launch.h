@@ -51,7 +51,14 @@ cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, 
 
 // variance
 cudaError_t launch_var(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out, float* mean,
-                       int twoterm, unsigned char* ws, cudaStream_t s);
+                       int variant, unsigned char* ws, cudaStream_t s);
+// The kernel on float64 input (every step in float64).
+cudaError_t launch_var_f64(const double* x, int64_t rows, int64_t cols, int axis, int ddof, double* out,
+                           double* mean, cudaStream_t s);
+// Complex64 input (interleaved re, im): var(re) + var(im) per slice; mean
+// interleaved.
+cudaError_t launch_var_c64(const float* z, int64_t rows, int64_t cols, int axis, int ddof, float* out,
+                           float* mean, cudaStream_t s);
 size_t var_workspace_bytes(int64_t rows, int64_t cols, int axis);
 
 // comparison sums: mode 0 naive, 1 pairwise, 2 kahan, 3 neumaier

@@ -1,5 +1,6 @@
-// Float32 variance ("Variance in float32 with a first-element shift, a local
-// centring and a compensated tree sum", section 2), all in float32:
+// Variance ("Variance in float32 with a first-element shift, a local
+// centring and a compensated tree sum", section 2), every step in the input
+// type (float32; float64 input runs the same steps in float64):
 //   1. shift      y_i = x_i - x_0
 //   2. centring   m = sum(y) / n,  d_i = y_i - m
 //   3. TwoSum tree over d_i^2, errors carried up a second array; s2 = final
@@ -8,34 +9,79 @@
 // Every tree pairs adjacent nodes (2i, 2i+1) level by level and passes an
 // unpaired last node up unchanged.  Thread t owns the subtree of leaves
 // [t C, t C + C) (C a power of two), so the tree, and the result bits, do not
-// depend on the block size.  Also the formula of reference (section 1,
-// tf.nn.moments) on the same trees, for comparison.
+// depend on the block size.
+//
+// Variants (template V; section 4, "Which step does what"):
+//   0 the kernel;
+//   1 the formula of reference (section 1, tf.nn.moments): no shift, means
+//     as sum times RN(1/n), plain trees;
+//   2 shift + centring, plain tree, no two-term (var = s2/n);
+//   3 shift + centring, plain tree, two-term;
+//   4 no shift: the formula of reference with the TwoSum tree for d^2;
+//   5 shift + centring, TwoSum tree, no two-term;
+//   6 shift + centring, s2 by Kahan's sequential loop over d^2 in index
+//     order (one thread per slice), two-term.
+// A TwoSum node's sum is the plain rounded add, so the plain-tree variants
+// run the same tree and read only its sums.
+//
+// Complex input (section 2, last paragraph) is the real and the imaginary
+// parts through the float32 kernel, read with an element stride of 2; the
+// second pass adds its variance to the first's.
 #include <cuda_runtime.h>
 #include <cstdint>
 #include "launch.h"
 
 namespace repro {
 
-struct TS {   // TwoSum tree node: sum s, carried error c
-  float s, c;
+template <typename T> __device__ __forceinline__ T add_rn(T a, T b);
+template <typename T> __device__ __forceinline__ T sub_rn(T a, T b);
+template <typename T> __device__ __forceinline__ T mul_rn(T a, T b);
+template <typename T> __device__ __forceinline__ T div_rn(T a, T b);
+template <> __device__ __forceinline__ float add_rn(float a, float b) { return __fadd_rn(a, b); }
+template <> __device__ __forceinline__ float sub_rn(float a, float b) { return __fsub_rn(a, b); }
+template <> __device__ __forceinline__ float mul_rn(float a, float b) { return __fmul_rn(a, b); }
+template <> __device__ __forceinline__ float div_rn(float a, float b) { return __fdiv_rn(a, b); }
+template <> __device__ __forceinline__ double add_rn(double a, double b) { return __dadd_rn(a, b); }
+template <> __device__ __forceinline__ double sub_rn(double a, double b) { return __dsub_rn(a, b); }
+template <> __device__ __forceinline__ double mul_rn(double a, double b) { return __dmul_rn(a, b); }
+template <> __device__ __forceinline__ double div_rn(double a, double b) { return __ddiv_rn(a, b); }
+
+template <int V> struct Steps {
+  static constexpr bool REF = V == 1 || V == 4;   // the reference formula's means and final step
+  static constexpr bool SHIFT = !REF;
+  static constexpr int COMP = (V == 1 || V == 2 || V == 3) ? 0 : (V == 6 ? 2 : 1);   // plain, TwoSum, Kahan
+  static constexpr bool TWOTERM = !(V == 2 || V == 5);
 };
 
-__device__ __forceinline__ TS ts_combine(TS l, TS r) {
+template <typename T>
+struct TS {   // TwoSum tree node: sum s, carried error c
+  T s, c;
+};
+
+template <typename T>
+__device__ __forceinline__ TS<T> ts_combine(TS<T> l, TS<T> r) {
   // TwoSum (six operations) and the carry of the two children
-  float s = __fadd_rn(l.s, r.s);
-  float bb = __fsub_rn(s, l.s);
-  float e = __fadd_rn(__fsub_rn(l.s, __fsub_rn(s, bb)), __fsub_rn(r.s, bb));
-  float c = __fadd_rn(__fadd_rn(l.c, r.c), e);
-  return TS{s, c};
+  T s = add_rn(l.s, r.s);
+  T bb = sub_rn(s, l.s);
+  T e = add_rn(sub_rn(l.s, sub_rn(s, bb)), sub_rn(r.s, bb));
+  T c = add_rn(add_rn(l.c, r.c), e);
+  return TS<T>{s, c};
 }
 
 // Node of the pass-2 trees: compensated d^2 tree and plain d tree together.
+template <typename T>
 struct N2 {
-  TS q;
-  float d;
+  TS<T> q;
+  T d;
 };
-__device__ __forceinline__ N2 n2_combine(N2 l, N2 r) { return N2{ts_combine(l.q, r.q), __fadd_rn(l.d, r.d)}; }
-__device__ __forceinline__ float f_combine(float l, float r) { return __fadd_rn(l, r); }
+template <typename T>
+__device__ __forceinline__ N2<T> n2_combine(N2<T> l, N2<T> r) {
+  return N2<T>{ts_combine(l.q, r.q), add_rn(l.d, r.d)};
+}
+template <typename T>
+__device__ __forceinline__ T f_combine(T l, T r) {
+  return add_rn(l, r);
+}
 
 // Streaming subtree over a valid prefix of `m` leaves (m <= C, C <= 2^LMAX):
 // a binary-counter stack holds complete subtrees; the root of the C-leaf tree
@@ -76,13 +122,12 @@ struct Stack {
   }
 };
 
-template <typename Node> __device__ __forceinline__ Node shfl_down_node(Node v, int d);
-template <> __device__ __forceinline__ float shfl_down_node<float>(float v, int d) {
+template <typename T> __device__ __forceinline__ T shfl_down_node(T v, int d) {
   return __shfl_down_sync(0xffffffffu, v, d);
 }
-template <> __device__ __forceinline__ N2 shfl_down_node<N2>(N2 v, int d) {
-  return N2{TS{__shfl_down_sync(0xffffffffu, v.q.s, d), __shfl_down_sync(0xffffffffu, v.q.c, d)},
-            __shfl_down_sync(0xffffffffu, v.d, d)};
+template <typename T> __device__ __forceinline__ N2<T> shfl_down_node(N2<T> v, int d) {
+  return N2<T>{TS<T>{__shfl_down_sync(0xffffffffu, v.q.s, d), __shfl_down_sync(0xffffffffu, v.q.c, d)},
+               __shfl_down_sync(0xffffffffu, v.d, d)};
 }
 
 // Combine the per-thread subtree roots of one slice, in tree order.  Threads
@@ -96,7 +141,7 @@ __device__ Node tree_combine_block(Node v, bool have, int P, Node* sm, bool* smv
   // within a warp: levels 1, 2, 4, 8, 16
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
-    Node o = shfl_down_node<Node>(v, d);
+    Node o = shfl_down_node(v, d);
     bool oh = __shfl_down_sync(0xffffffffu, have, d);
     if ((lane & (2 * d - 1)) == 0 && lane + d < 32) {
       if (have && oh) v = comb(v, o);
@@ -120,91 +165,136 @@ __device__ Node tree_combine_block(Node v, bool have, int P, Node* sm, bool* smv
   return v;
 }
 
-__device__ __forceinline__ float max_nan0(float v) {
+template <typename T>
+__device__ __forceinline__ T max_nan0(T v) {
   if (v != v) return v;
-  return v > 0.0f ? v : 0.0f;
+  return v > (T)0 ? v : (T)0;
+}
+
+// Output of one slice, where every pass-2 quantity is known: variance
+// (rescaled, added to *out when `acc`) and mean.
+struct VarOut {
+  int acc;           // add the variance to the value already in out[s]
+  int64_t mstride;   // mean_out[s * mstride]
+};
+
+template <typename T, int V>
+__device__ __forceinline__ void finish_slice(const N2<T>& tot, T kahan_s2, T x0, T mu, int64_t n, int ddof,
+                                             T* out, T* mean_out, int64_t s, VarOut io) {
+  typedef Steps<V> St;
+  const T nf = (T)n;
+  T var, mean;
+  if constexpr (St::REF) {
+    T inv = div_rn((T)1, nf);
+    T md = mul_rn(tot.d, inv);
+    T s2 = St::COMP == 1 ? add_rn(tot.q.s, tot.q.c) : tot.q.s;
+    var = max_nan0(sub_rn(mul_rn(s2, inv), mul_rn(md, md)));
+    mean = mu;
+  } else {
+    T s2 = St::COMP == 1 ? add_rn(tot.q.s, tot.q.c) : (St::COMP == 0 ? tot.q.s : kahan_s2);
+    T t = div_rn(tot.d, nf);
+    T v = St::TWOTERM ? sub_rn(div_rn(s2, nf), mul_rn(t, t)) : div_rn(s2, nf);
+    var = max_nan0(v);
+    mean = add_rn(x0, mu);
+  }
+  if (ddof != 0) var = mul_rn(var, div_rn(nf, (T)(n - ddof)));
+  out[s] = io.acc ? add_rn(out[s], var) : var;
+  if (mean_out) mean_out[s * io.mstride] = mean;
+}
+
+// Kahan's loop over d_i^2 in index order (variant 6), one thread.
+template <typename T>
+__device__ T kahan_sq(const T* x, int64_t n, int64_t stride, T x0, T mu) {
+  T s = (T)0, c = (T)0;
+  for (int64_t i = 0; i < n; ++i) {
+    T d = sub_rn(sub_rn(x[i * stride], x0), mu);
+    T y = sub_rn(mul_rn(d, d), c);
+    T t = add_rn(s, y);
+    c = sub_rn(sub_rn(t, s), y);
+    s = t;
+  }
+  return s;
+}
+
+template <typename T, int V>
+__device__ __forceinline__ T leaf1(T xi, T x0) {
+  return Steps<V>::SHIFT ? sub_rn(xi, x0) : xi;
+}
+template <typename T, int V>
+__device__ __forceinline__ T leaf_d(T xi, T x0, T mu) {
+  typedef Steps<V> St;
+  if constexpr (St::SHIFT) return sub_rn(sub_rn(xi, x0), mu);
+  else return sub_rn(xi, mu);
+}
+template <typename T, int V>
+__device__ __forceinline__ T mean_of(T sum1, int64_t n) {
+  const T nf = (T)n;
+  return Steps<V>::REF ? mul_rn(sum1, div_rn((T)1, nf)) : div_rn(sum1, nf);
 }
 
 // Row kernel (axis 1): one block per row, thread t owns leaves [t C, t C + C).
-// MODE 0: the variance kernel; MODE 1: the formula of reference.
-template <int MODE>
-__global__ void __launch_bounds__(1024) var_rows_kernel(const float* __restrict__ x, int64_t rows, int64_t cols,
-                                                        int ddof, float* __restrict__ out, float* __restrict__ mean_out,
-                                                        int64_t C) {
-  __shared__ float smf[32];
-  __shared__ N2 sm2[32];
+// Element i of row r is x[(r cols + i) es].
+template <typename T, int V>
+__global__ void __launch_bounds__(1024) var_rows_kernel(const T* __restrict__ x, int64_t rows, int64_t cols,
+                                                        int64_t es, int ddof, T* __restrict__ out,
+                                                        T* __restrict__ mean_out, VarOut io, int64_t C) {
+  typedef Steps<V> St;
+  __shared__ T smf[32];
+  __shared__ N2<T> sm2[32];
   __shared__ bool smv[32];
-  __shared__ float bc[2];
+  __shared__ T bc[2];
   const int64_t n = cols;
-  const float nf = (float)n;
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    const float* row = x + r * cols;
-    const float x0 = row[0];
+    const T* row = x + r * cols * es;
+    const T x0 = row[0];
     int64_t b = (int64_t)threadIdx.x * C;
     int64_t m = n - b;
     m = m < 0 ? 0 : (m > C ? C : m);
-    // pass 1: sum of y (kernel) or of x (reference)
-    Stack<float, 40> st1;
-    st1.reset();
-    for (int64_t i = 0; i < m; ++i) {
-      float leaf = (MODE == 0) ? __fsub_rn(row[b + i], x0) : row[b + i];
-      st1.push(leaf, f_combine);
+    T mu = (T)0;
+    {
+      // pass 1: sum of y (shift) or of x (reference)
+      Stack<T, 40> st1;
+      st1.reset();
+      for (int64_t i = 0; i < m; ++i) st1.push(leaf1<T, V>(row[(b + i) * es], x0), f_combine<T>);
+      T v1 = (T)0;
+      bool h1 = st1.root(v1, f_combine<T>);
+      T sum1 = tree_combine_block<T>(v1, h1, blockDim.x, smf, smv, f_combine<T>);
+      if (threadIdx.x == 0) bc[0] = mean_of<T, V>(sum1, n);
+      __syncthreads();
+      mu = bc[0];
     }
-    float v1 = 0.0f;
-    bool h1 = st1.root(v1, f_combine);
-    float sum1 = tree_combine_block<float>(v1, h1, blockDim.x, smf, smv, f_combine);
-    if (threadIdx.x == 0)
-      bc[0] = (MODE == 0) ? __fdiv_rn(sum1, nf) : __fmul_rn(sum1, __fdiv_rn(1.0f, nf));
-    __syncthreads();
-    const float mu = bc[0];
-    // pass 2: d = y - m (kernel) or x - m (reference); compensated tree of d^2
-    // (kernel) or plain tree of d^2 (reference), plain tree of d
-    Stack<N2, 40> st2;
+    // pass 2: d, the d^2 tree (TwoSum nodes) and the d tree
+    Stack<N2<T>, 40> st2;
     st2.reset();
     for (int64_t i = 0; i < m; ++i) {
-      float xi = row[b + i];
-      float d = (MODE == 0) ? __fsub_rn(__fsub_rn(xi, x0), mu) : __fsub_rn(xi, mu);
-      st2.push(N2{TS{__fmul_rn(d, d), 0.0f}, d}, n2_combine);
+      T d = leaf_d<T, V>(row[(b + i) * es], x0, mu);
+      st2.push(N2<T>{TS<T>{mul_rn(d, d), (T)0}, d}, n2_combine<T>);
     }
-    N2 v2;
-    bool h2 = st2.root(v2, n2_combine);
-    N2 tot = tree_combine_block<N2>(v2, h2, blockDim.x, sm2, smv, n2_combine);
+    N2<T> v2;
+    bool h2 = st2.root(v2, n2_combine<T>);
+    N2<T> tot = tree_combine_block<N2<T>>(v2, h2, blockDim.x, sm2, smv, n2_combine<T>);
     if (threadIdx.x == 0) {
-      float var;
-      if (MODE == 0) {
-        float s2 = __fadd_rn(tot.q.s, tot.q.c);
-        float t = __fdiv_rn(tot.d, nf);
-        var = max_nan0(__fsub_rn(__fdiv_rn(s2, nf), __fmul_rn(t, t)));
-      } else {
-        float inv = __fdiv_rn(1.0f, nf);
-        float md = __fmul_rn(tot.d, inv);
-        var = max_nan0(__fsub_rn(__fmul_rn(tot.q.s, inv), __fmul_rn(md, md)));
-      }
-      if (ddof != 0) var = __fmul_rn(var, __fdiv_rn(nf, (float)(n - ddof)));
-      out[r] = var;
-      if (mean_out) mean_out[r] = (MODE == 0) ? __fadd_rn(x0, mu) : mu;
+      T ks = St::COMP == 2 ? kahan_sq<T>(row, n, es, x0, mu) : (T)0;
+      finish_slice<T, V>(tot, ks, x0, mu, n, ddof, out, mean_out, r, io);
     }
     __syncthreads();
   }
 }
 
-// The reference formula's d^2 tree must be a plain tree: a TwoSum node whose
-// carry is ignored has the same sum s as a plain add, so the MODE 1 kernel
-// reads tot.q.s only.
-
 // Column kernel (axis 0): a block covers 32 adjacent columns (threadIdx.x)
-// and G row groups (threadIdx.y); group g owns rows [g C, g C + C).
-template <int MODE>
-__global__ void __launch_bounds__(256) var_cols_kernel(const float* __restrict__ x, int64_t rows, int64_t cols,
-                                                       int ddof, float* __restrict__ out, float* __restrict__ mean_out,
-                                                       int64_t C) {
-  __shared__ float smf[8][32];
-  __shared__ N2 sm2[8][32];
+// and G row groups (threadIdx.y); group g owns rows [g C, g C + C).  Element
+// (i, c) is x[(i cols + c) es].
+template <typename T, int V>
+__global__ void __launch_bounds__(256) var_cols_kernel(const T* __restrict__ x, int64_t rows, int64_t cols,
+                                                       int64_t es, int ddof, T* __restrict__ out,
+                                                       T* __restrict__ mean_out, VarOut io, int64_t C) {
+  typedef Steps<V> St;
+  __shared__ T smf[8][32];
+  __shared__ N2<T> sm2[8][32];
   __shared__ bool smv[8][32];
-  __shared__ float bc[32];
+  __shared__ T bc[32];
   const int G = blockDim.y;
   const int64_t n = rows;
-  const float nf = (float)n;
   const int64_t c = (int64_t)blockIdx.x * 32 + threadIdx.x;
   const bool col_ok = c < cols;
   const int g = threadIdx.y;
@@ -212,42 +302,40 @@ __global__ void __launch_bounds__(256) var_cols_kernel(const float* __restrict__
   int64_t m = n - b;
   m = m < 0 ? 0 : (m > C ? C : m);
   if (!col_ok) m = 0;
-  const float x0 = col_ok ? x[c] : 0.0f;
-  Stack<float, 40> st1;
-  st1.reset();
-  for (int64_t i = 0; i < m; ++i) {
-    float xi = x[(b + i) * cols + c];
-    st1.push((MODE == 0) ? __fsub_rn(xi, x0) : xi, f_combine);
-  }
-  float v1 = 0.0f;
-  bool h1 = st1.root(v1, f_combine);
-  smf[g][threadIdx.x] = v1;
-  smv[g][threadIdx.x] = h1;
-  __syncthreads();
-  if (g == 0) {
-    for (int step = 1; step < G; step <<= 1)
-      for (int w = 0; w + step < G; w += 2 * step) {
-        if (smv[w][threadIdx.x] && smv[w + step][threadIdx.x])
-          smf[w][threadIdx.x] = __fadd_rn(smf[w][threadIdx.x], smf[w + step][threadIdx.x]);
-        else if (!smv[w][threadIdx.x] && smv[w + step][threadIdx.x]) {
-          smf[w][threadIdx.x] = smf[w + step][threadIdx.x];
-          smv[w][threadIdx.x] = true;
+  const T x0 = col_ok ? x[c * es] : (T)0;
+  T mu = (T)0;
+  {
+    Stack<T, 40> st1;
+    st1.reset();
+    for (int64_t i = 0; i < m; ++i) st1.push(leaf1<T, V>(x[((b + i) * cols + c) * es], x0), f_combine<T>);
+    T v1 = (T)0;
+    bool h1 = st1.root(v1, f_combine<T>);
+    smf[g][threadIdx.x] = v1;
+    smv[g][threadIdx.x] = h1;
+    __syncthreads();
+    if (g == 0) {
+      for (int step = 1; step < G; step <<= 1)
+        for (int w = 0; w + step < G; w += 2 * step) {
+          if (smv[w][threadIdx.x] && smv[w + step][threadIdx.x])
+            smf[w][threadIdx.x] = add_rn(smf[w][threadIdx.x], smf[w + step][threadIdx.x]);
+          else if (!smv[w][threadIdx.x] && smv[w + step][threadIdx.x]) {
+            smf[w][threadIdx.x] = smf[w + step][threadIdx.x];
+            smv[w][threadIdx.x] = true;
+          }
         }
-      }
-    float s = smf[0][threadIdx.x];
-    bc[threadIdx.x] = (MODE == 0) ? __fdiv_rn(s, nf) : __fmul_rn(s, __fdiv_rn(1.0f, nf));
+      bc[threadIdx.x] = mean_of<T, V>(smf[0][threadIdx.x], n);
+    }
+    __syncthreads();
+    mu = bc[threadIdx.x];
   }
-  __syncthreads();
-  const float mu = bc[threadIdx.x];
-  Stack<N2, 40> st2;
+  Stack<N2<T>, 40> st2;
   st2.reset();
   for (int64_t i = 0; i < m; ++i) {
-    float xi = x[(b + i) * cols + c];
-    float d = (MODE == 0) ? __fsub_rn(__fsub_rn(xi, x0), mu) : __fsub_rn(xi, mu);
-    st2.push(N2{TS{__fmul_rn(d, d), 0.0f}, d}, n2_combine);
+    T d = leaf_d<T, V>(x[((b + i) * cols + c) * es], x0, mu);
+    st2.push(N2<T>{TS<T>{mul_rn(d, d), (T)0}, d}, n2_combine<T>);
   }
-  N2 v2;
-  bool h2 = st2.root(v2, n2_combine);
+  N2<T> v2;
+  bool h2 = st2.root(v2, n2_combine<T>);
   sm2[g][threadIdx.x] = v2;
   smv[g][threadIdx.x] = h2;
   __syncthreads();
@@ -261,20 +349,8 @@ __global__ void __launch_bounds__(256) var_cols_kernel(const float* __restrict__
           smv[w][threadIdx.x] = true;
         }
       }
-    N2 tot = sm2[0][threadIdx.x];
-    float var;
-    if (MODE == 0) {
-      float s2 = __fadd_rn(tot.q.s, tot.q.c);
-      float t = __fdiv_rn(tot.d, nf);
-      var = max_nan0(__fsub_rn(__fdiv_rn(s2, nf), __fmul_rn(t, t)));
-    } else {
-      float inv = __fdiv_rn(1.0f, nf);
-      float md = __fmul_rn(tot.d, inv);
-      var = max_nan0(__fsub_rn(__fmul_rn(tot.q.s, inv), __fmul_rn(md, md)));
-    }
-    if (ddof != 0) var = __fmul_rn(var, __fdiv_rn(nf, (float)(n - ddof)));
-    out[c] = var;
-    if (mean_out) mean_out[c] = (MODE == 0) ? __fadd_rn(x0, mu) : mu;
+    T ks = St::COMP == 2 ? kahan_sq<T>(x + c * es, n, cols * es, x0, mu) : (T)0;
+    finish_slice<T, V>(sm2[0][threadIdx.x], ks, x0, mu, n, ddof, out, mean_out, c, io);
   }
 }
 
@@ -297,78 +373,85 @@ __device__ __forceinline__ bool reg_tree(Node* a, int m, F comb) {
   return m > 0;
 }
 
-template <int C, int MODE>
-__global__ void __launch_bounds__(256) var_rows_reg(const float* __restrict__ x, int64_t rows, int64_t cols, int ddof,
-                                                    float* __restrict__ out, float* __restrict__ mean_out) {
-  __shared__ float smf[32];
-  __shared__ N2 sm2[32];
+template <typename T> struct Vec16;
+template <> struct Vec16<float> {
+  typedef float4 type;
+  static constexpr int W = 4;
+  __device__ __forceinline__ static void put(const float4& q, float* v) {
+    v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+  }
+};
+template <> struct Vec16<double> {
+  typedef double2 type;
+  static constexpr int W = 2;
+  __device__ __forceinline__ static void put(const double2& q, double* v) {
+    v[0] = q.x; v[1] = q.y;
+  }
+};
+
+template <typename T, int C, int V>
+__global__ void __launch_bounds__(256) var_rows_reg(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t es,
+                                                    int ddof, T* __restrict__ out, T* __restrict__ mean_out,
+                                                    VarOut io) {
+  typedef Steps<V> St;
+  typedef Vec16<T> VT;
+  __shared__ T smf[32];
+  __shared__ N2<T> sm2[32];
   __shared__ bool smv[32];
-  __shared__ float bc[1];
+  __shared__ T bc[1];
   const int n = (int)cols;
-  const float nf = (float)n;
   const int b = threadIdx.x * C;
   int m = n - b;
   m = m < 0 ? 0 : (m > C ? C : m);
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    const float* row = x + r * cols;
-    const float x0 = __ldg(row);
-    float v[C];
-    if (C % 4 == 0 && m == C && ((((uintptr_t)(row + b)) & 15) == 0)) {
+    const T* row = x + r * cols * es;
+    const T x0 = __ldg(row);
+    T v[C];
+    if (C % VT::W == 0 && es == 1 && m == C && ((((uintptr_t)(row + b)) & 15) == 0)) {
 #pragma unroll
-      for (int u = 0; u < C / 4; ++u) {
-        float4 q = __ldcs((const float4*)(row + b) + u);
-        v[4 * u] = q.x; v[4 * u + 1] = q.y; v[4 * u + 2] = q.z; v[4 * u + 3] = q.w;
-      }
+      for (int u = 0; u < C / VT::W; ++u) VT::put(__ldcs((const typename VT::type*)(row + b) + u), v + VT::W * u);
     } else {
 #pragma unroll
-      for (int i = 0; i < C; ++i) v[i] = (i < m) ? row[b + i] : 0.0f;
+      for (int i = 0; i < C; ++i) v[i] = (i < m) ? row[(b + i) * es] : (T)0;
     }
-    // pass 1
-    float t1[C];
+    T mu = (T)0;
+    {
+      // pass 1
+      T t1[C];
 #pragma unroll
-    for (int i = 0; i < C; ++i) t1[i] = (MODE == 0) ? __fsub_rn(v[i], x0) : v[i];
-    bool h1 = reg_tree<float, C>(t1, m, f_combine);
-    float sum1 = tree_combine_block<float>(t1[0], h1, blockDim.x, smf, smv, f_combine);
-    if (threadIdx.x == 0) bc[0] = (MODE == 0) ? __fdiv_rn(sum1, nf) : __fmul_rn(sum1, __fdiv_rn(1.0f, nf));
-    __syncthreads();
-    const float mu = bc[0];
+      for (int i = 0; i < C; ++i) t1[i] = leaf1<T, V>(v[i], x0);
+      bool h1 = reg_tree<T, C>(t1, m, f_combine<T>);
+      T sum1 = tree_combine_block<T>(t1[0], h1, blockDim.x, smf, smv, f_combine<T>);
+      if (threadIdx.x == 0) bc[0] = mean_of<T, V>(sum1, n);
+      __syncthreads();
+      mu = bc[0];
+    }
     // pass 2
-    N2 t2[C];
+    N2<T> t2[C];
 #pragma unroll
     for (int i = 0; i < C; ++i) {
-      float d = (MODE == 0) ? __fsub_rn(__fsub_rn(v[i], x0), mu) : __fsub_rn(v[i], mu);
-      t2[i] = N2{TS{__fmul_rn(d, d), 0.0f}, d};
+      T d = leaf_d<T, V>(v[i], x0, mu);
+      t2[i] = N2<T>{TS<T>{mul_rn(d, d), (T)0}, d};
     }
-    bool h2 = reg_tree<N2, C>(t2, m, n2_combine);
-    N2 tot = tree_combine_block<N2>(t2[0], h2, blockDim.x, sm2, smv, n2_combine);
+    bool h2 = reg_tree<N2<T>, C>(t2, m, n2_combine<T>);
+    N2<T> tot = tree_combine_block<N2<T>>(t2[0], h2, blockDim.x, sm2, smv, n2_combine<T>);
     if (threadIdx.x == 0) {
-      float var;
-      if (MODE == 0) {
-        float s2 = __fadd_rn(tot.q.s, tot.q.c);
-        float t = __fdiv_rn(tot.d, nf);
-        var = max_nan0(__fsub_rn(__fdiv_rn(s2, nf), __fmul_rn(t, t)));
-      } else {
-        float inv = __fdiv_rn(1.0f, nf);
-        float md = __fmul_rn(tot.d, inv);
-        var = max_nan0(__fsub_rn(__fmul_rn(tot.q.s, inv), __fmul_rn(md, md)));
-      }
-      if (ddof != 0) var = __fmul_rn(var, __fdiv_rn(nf, (float)(n - ddof)));
-      out[r] = var;
-      if (mean_out) mean_out[r] = (MODE == 0) ? __fadd_rn(x0, mu) : mu;
+      T ks = St::COMP == 2 ? kahan_sq<T>(row, n, es, x0, mu) : (T)0;
+      finish_slice<T, V>(tot, ks, x0, mu, n, ddof, out, mean_out, r, io);
     }
     __syncthreads();
   }
 }
 
-template <int MODE>
-static void launch_rows_reg(int64_t C, const float* x, int64_t rows, int64_t cols, int ddof, float* out, float* mean,
-                            unsigned grid, cudaStream_t s) {
+template <typename T, int V>
+static void launch_rows_reg(int64_t C, const T* x, int64_t rows, int64_t cols, int64_t es, int ddof, T* out,
+                            T* mean, VarOut io, unsigned grid, cudaStream_t s) {
   switch (C) {
-    case 1: var_rows_reg<1, MODE><<<grid, 256, 0, s>>>(x, rows, cols, ddof, out, mean); break;
-    case 2: var_rows_reg<2, MODE><<<grid, 256, 0, s>>>(x, rows, cols, ddof, out, mean); break;
-    case 4: var_rows_reg<4, MODE><<<grid, 256, 0, s>>>(x, rows, cols, ddof, out, mean); break;
-    case 8: var_rows_reg<8, MODE><<<grid, 256, 0, s>>>(x, rows, cols, ddof, out, mean); break;
-    default: var_rows_reg<16, MODE><<<grid, 256, 0, s>>>(x, rows, cols, ddof, out, mean); break;
+    case 1: var_rows_reg<T, 1, V><<<grid, 256, 0, s>>>(x, rows, cols, es, ddof, out, mean, io); break;
+    case 2: var_rows_reg<T, 2, V><<<grid, 256, 0, s>>>(x, rows, cols, es, ddof, out, mean, io); break;
+    case 4: var_rows_reg<T, 4, V><<<grid, 256, 0, s>>>(x, rows, cols, es, ddof, out, mean, io); break;
+    case 8: var_rows_reg<T, 8, V><<<grid, 256, 0, s>>>(x, rows, cols, es, ddof, out, mean, io); break;
+    default: var_rows_reg<T, 16, V><<<grid, 256, 0, s>>>(x, rows, cols, es, ddof, out, mean, io); break;
   }
 }
 
@@ -378,25 +461,17 @@ static int64_t pow2_ceil(int64_t v) {
   return p;
 }
 
-size_t var_workspace_bytes(int64_t, int64_t, int) { return 0; }
-
-cudaError_t launch_var(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out, float* mean,
-                       int twoterm, unsigned char*, cudaStream_t s) {
+template <typename T, int V>
+static cudaError_t launch_var_v(const T* x, int64_t rows, int64_t cols, int axis, int ddof, int64_t es, T* out,
+                                T* mean, VarOut io, cudaStream_t s) {
   if (axis == 1) {
     int block = 256;
     int64_t np = pow2_ceil(cols);
     int64_t C = np / block;
     if (C < 1) C = 1;
     int64_t grid = rows < 65535 * 16 ? rows : 65535 * 16;
-    if (C <= 16) {
-      if (twoterm) launch_rows_reg<1>(C, x, rows, cols, ddof, out, mean, (unsigned)grid, s);
-      else launch_rows_reg<0>(C, x, rows, cols, ddof, out, mean, (unsigned)grid, s);
-      return cudaGetLastError();
-    }
-    if (twoterm)
-      var_rows_kernel<1><<<(unsigned)grid, block, 0, s>>>(x, rows, cols, ddof, out, mean, C);
-    else
-      var_rows_kernel<0><<<(unsigned)grid, block, 0, s>>>(x, rows, cols, ddof, out, mean, C);
+    if (C <= 16) launch_rows_reg<T, V>(C, x, rows, cols, es, ddof, out, mean, io, (unsigned)grid, s);
+    else var_rows_kernel<T, V><<<(unsigned)grid, block, 0, s>>>(x, rows, cols, es, ddof, out, mean, io, C);
   } else {
     int G = 8;
     int64_t np = pow2_ceil(rows);
@@ -404,12 +479,39 @@ cudaError_t launch_var(const float* x, int64_t rows, int64_t cols, int axis, int
     if (C < 1) C = 1;
     dim3 block(32, G);
     unsigned grid = (unsigned)((cols + 31) / 32);
-    if (twoterm)
-      var_cols_kernel<1><<<grid, block, 0, s>>>(x, rows, cols, ddof, out, mean, C);
-    else
-      var_cols_kernel<0><<<grid, block, 0, s>>>(x, rows, cols, ddof, out, mean, C);
+    var_cols_kernel<T, V><<<grid, block, 0, s>>>(x, rows, cols, es, ddof, out, mean, io, C);
   }
   return cudaGetLastError();
+}
+
+size_t var_workspace_bytes(int64_t, int64_t, int) { return 0; }
+
+cudaError_t launch_var(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out, float* mean,
+                       int variant, unsigned char*, cudaStream_t s) {
+  const VarOut io{0, 1};
+  switch (variant) {
+    case 0: return launch_var_v<float, 0>(x, rows, cols, axis, ddof, 1, out, mean, io, s);
+    case 1: return launch_var_v<float, 1>(x, rows, cols, axis, ddof, 1, out, mean, io, s);
+    case 2: return launch_var_v<float, 2>(x, rows, cols, axis, ddof, 1, out, mean, io, s);
+    case 3: return launch_var_v<float, 3>(x, rows, cols, axis, ddof, 1, out, mean, io, s);
+    case 4: return launch_var_v<float, 4>(x, rows, cols, axis, ddof, 1, out, mean, io, s);
+    case 5: return launch_var_v<float, 5>(x, rows, cols, axis, ddof, 1, out, mean, io, s);
+    case 6: return launch_var_v<float, 6>(x, rows, cols, axis, ddof, 1, out, mean, io, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_var_f64(const double* x, int64_t rows, int64_t cols, int axis, int ddof, double* out,
+                           double* mean, cudaStream_t s) {
+  return launch_var_v<double, 0>(x, rows, cols, axis, ddof, 1, out, mean, VarOut{0, 1}, s);
+}
+
+cudaError_t launch_var_c64(const float* z, int64_t rows, int64_t cols, int axis, int ddof, float* out,
+                           float* mean, cudaStream_t s) {
+  // real parts (mean to the even floats), then imaginary parts added on
+  cudaError_t e = launch_var_v<float, 0>(z, rows, cols, axis, ddof, 2, out, mean, VarOut{0, 2}, s);
+  if (e != cudaSuccess) return e;
+  return launch_var_v<float, 0>(z + 1, rows, cols, axis, ddof, 2, out, mean ? mean + 1 : nullptr, VarOut{1, 2}, s);
 }
 
 }  // namespace repro

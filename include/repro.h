@@ -184,6 +184,35 @@ repro_status repro_segsum_f32(const float* x, int64_t rows, int64_t cols, int ax
    mean_out (nullable) the means.  Device pointers; stream-ordered. */
 repro_status stable_var_f32(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out,
                             float* mean_out, cudaStream_t stream);
+/* The same kernel on float64 input, every step in float64 (variance page,
+   section 2: "all in the input dtype"; section 5 lists float64 as not
+   measured).  n <= 2^53; otherwise as stable_var_f32. */
+repro_status stable_var_f64(const double* x, int64_t rows, int64_t cols, int axis, int ddof, double* out,
+                            double* mean_out, cudaStream_t stream);
+/* Complex64 input (section 2, last paragraph): z is a row-major [rows, cols]
+   complex64 array (interleaved real, imaginary float32 pairs, 8-byte
+   aligned).  Per slice, out = RN(var(re) + var(im)) with each part by the
+   float32 kernel (ddof applied to each part), i.e. E|z - mean(z)|^2;
+   mean_out (nullable, complex64, 8-byte aligned) gets (mean(re), mean(im)).
+   Otherwise as stable_var_f32. */
+repro_status stable_var_c64(const float* z, int64_t rows, int64_t cols, int axis, int ddof, float* out,
+                            float* mean_out, cudaStream_t stream);
+/* The kernel with steps changed, as in the variance page's section 4
+   ("Which step does what"); variant:
+     0  the kernel (= stable_var_f32);
+     1  the formula of reference (= twoterm_var_f32; mean_out gets mean(x));
+     2  shift + centring, plain tree for d^2, no two-term: var = s2/n;
+     3  shift + centring, plain tree for d^2, two-term;
+     4  no shift: the formula of reference with the TwoSum tree for d^2
+        (var = max(RN(s2 RN(1/n)) - md^2, 0)); mean_out gets mean(x);
+     5  shift + centring, TwoSum tree, no two-term;
+     6  shift + centring, s2 by Kahan's sequential loop over d^2 in index
+        order (one thread per slice: slow by design), two-term.
+   Every tree and rounding step is the kernel's; the result is bit-identical
+   to the oracle's restatement of each variant.  variant outside 0..6 gives
+   REPRO_ERR_INVALID_ARG. */
+repro_status stable_var_f32_variant(const float* x, int64_t rows, int64_t cols, int axis, int ddof, int variant,
+                                    float* out, float* mean_out, cudaStream_t stream);
 
 /* ---- comparison modes ("Reduction order and compensation solve related but
    different problems"; "Kahan's Summation Formula") ---------------------- */

@@ -106,6 +106,33 @@ void orc_var_f64(const float* x, int64_t rows, int64_t cols, int axis, int ddof,
 void orc_segsum_f32(const float* x, int64_t rows, int64_t cols, int axis, int K, float* out);
 /* Complex variance: var(re) + var(im), each by the float32 kernel. */
 void orc_var_kernel_c64(const float* re, const float* im, int64_t n, int ddof, float* var_out);
+/* The same per slice of a complex64 [rows, cols] array (interleaved re, im);
+   mean_out (interleaved, may be NULL) gets (mean(re), mean(im)). */
+void orc_var_kernel_c64_2d(const float* z, int64_t rows, int64_t cols, int axis, int ddof,
+                           float* var_out, float* mean_out);
+/* Section 4 variants of the float32 kernel ("Which step does what"):
+     0 the kernel: shift + centring, TwoSum tree, two-term;
+     2 shift + centring, plain tree, no two-term (var = s2/n);
+     3 shift + centring, plain tree, two-term;
+     4 no shift: the formula of reference (means as the tree sum times
+       RN(1/n), d = x - mean, two-term) with the TwoSum tree for d^2 (the
+       reading that matches its row: at most equal to the reference on 4/4
+       datasets, NaN for [1e38]*3 on the GPU); mean = the reference's mean;
+     5 shift + centring, TwoSum tree, no two-term;
+     6 shift + centring, s2 by Kahan's sequential loop over d^2 in index
+       order, two-term (only step 3 changes: "one step changed at a time").
+   Variant 1 is the formula of reference (orc_var_twoterm_f32, with its
+   mean).  Pins: exact
+   variance on small-integer data; the [1e38]*3 column of section 4 (0 with
+   the shift, NaN for variant 4); identical values give 0 with the shift;
+   float64 closeness; variant 0 equals orc_var_kernel_f32 bit for bit. */
+void orc_var_variant_f32(const float* x, int64_t rows, int64_t cols, int axis, int ddof, int variant,
+                         float* var_out, float* mean_out);
+/* The kernel on float64 input, every step in float64.  Pins: exact
+   variance on small-integer data, identical values (including [1e307]*3)
+   give 0, closeness to the exact rational variance. */
+void orc_var_kernel_f64(const double* x, int64_t rows, int64_t cols, int axis, int ddof,
+                        double* var_out, double* mean_out);
 
 #ifdef __cplusplus
 }

@@ -91,6 +91,9 @@ def _L():
             "orc_var_f64": (None, [P, i64, i64, ci, ci, P, P]),
             "orc_segsum_f32": (None, [P, i64, i64, ci, ci, P]),
             "orc_var_kernel_c64": (None, [P, P, i64, ci, P]),
+            "orc_var_kernel_c64_2d": (None, [P, i64, i64, ci, ci, P, P]),
+            "orc_var_variant_f32": (None, [P, i64, i64, ci, ci, ci, P, P]),
+            "orc_var_kernel_f64": (None, [P, i64, i64, ci, ci, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -270,3 +273,41 @@ def var_kernel_complex(z, ddof: int = 0):
     out = np.zeros(1, dtype=np.float32)
     _L().orc_var_kernel_c64(pr, pi, re.size, ddof, out.ctypes.data_as(ctypes.c_void_p))
     return out[0]
+
+
+def var_variant(x2d, variant: int, axis: int = 1, ddof: int = 0):
+    """Section 4 variants of the float32 kernel (see orc_var_variant_f32)."""
+    a, p = _arr(x2d, np.float32)
+    rows, cols = a.shape
+    ns = rows if axis == 1 else cols
+    v = np.empty(ns, dtype=np.float32)
+    m = np.empty(ns, dtype=np.float32)
+    _L().orc_var_variant_f32(p, rows, cols, axis, ddof, variant, v.ctypes.data_as(ctypes.c_void_p),
+                             m.ctypes.data_as(ctypes.c_void_p))
+    return v, m
+
+
+def var_kernel_f64(x2d, axis: int = 1, ddof: int = 0):
+    """The kernel on float64 input, every step in float64."""
+    a, p = _arr(x2d, np.float64)
+    rows, cols = a.shape
+    ns = rows if axis == 1 else cols
+    v = np.empty(ns, dtype=np.float64)
+    m = np.empty(ns, dtype=np.float64)
+    _L().orc_var_kernel_f64(p, rows, cols, axis, ddof, v.ctypes.data_as(ctypes.c_void_p),
+                            m.ctypes.data_as(ctypes.c_void_p))
+    return v, m
+
+
+def var_kernel_c64_2d(z2d, axis: int = 1, ddof: int = 0):
+    """Complex64 [rows, cols]: var(re) + var(im) per slice, and the complex mean."""
+    zz = np.ascontiguousarray(np.asarray(z2d, dtype=np.complex64))
+    rows, cols = zz.shape
+    f = zz.view(np.float32)
+    p = f.ctypes.data_as(ctypes.c_void_p)
+    ns = rows if axis == 1 else cols
+    v = np.empty(ns, dtype=np.float32)
+    m = np.empty(ns, dtype=np.complex64)
+    _L().orc_var_kernel_c64_2d(p, rows, cols, axis, ddof, v.ctypes.data_as(ctypes.c_void_p),
+                               m.ctypes.data_as(ctypes.c_void_p))
+    return v, m

@@ -450,3 +450,119 @@ def test_shift_is_exact_within_factor_two(orc):
     v, m = orc.var_kernel(x, 0)
     _, m64 = orc.var_f64(x, 0)
     assert np.all(np.abs(m - m64) <= np.spacing(np.float32(1e6)))
+
+
+# ------------------------------------------------- variance extras (oracle)
+VARIANTS = (0, 1, 2, 3, 4, 5, 6)
+
+
+def arr_same(a, b):
+    a, b = np.asarray(a), np.asarray(b)
+    return a.dtype == b.dtype and a.shape == b.shape and a.tobytes() == b.tobytes()
+
+
+def test_variants_closed_form(orc):
+    """Data with an integer mean and small integer deviations: every
+    rounding step of every variant is exact, so each gives the exact
+    population variance 5.25 and mean 5 (section 4 changes steps, not the
+    value)."""
+    x = np.array([[3, 7, 1, 5, 9, 5, 4, 6]], np.float32)
+    for v in VARIANTS:
+        var, mean = orc.var_variant(x, v, 1)
+        assert var[0] == 5.25 and mean[0] == 5.0, v
+    # the same slice along axis 0
+    var, mean = orc.var_variant(np.ascontiguousarray(x.T), 6, 0)
+    assert var[0] == 5.25 and mean[0] == 5.0
+
+
+def test_variants_identical_values(orc):
+    """Section 4, [1e38]*3 column (GPU): 0 for every variant with the shift,
+    NaN for the formula of reference and the variant without the shift.
+    Section 3 rows: identical values give exactly 0 with the shift."""
+    x = np.full((1, 3), np.float32(1e38))
+    for v in (0, 2, 3, 5, 6):
+        assert orc.var_variant(x, v, 1)[0][0] == 0.0, v
+    for v in (1, 4):
+        assert np.isnan(orc.var_variant(x, v, 1)[0][0]), v
+    for val in (1e10, 7.5e10, 1e15):
+        y = np.full((1, 3), np.float32(val))
+        for v in (0, 2, 3, 5, 6):
+            assert orc.var_variant(y, v, 1)[0][0] == 0.0, (val, v)
+
+
+def test_variants_zero_and_one_are_the_kernel_and_the_reference(orc):
+    for name, x, axis in inputs.var_datasets(0):
+        for ddof in (0, 1):
+            k, m = orc.var_kernel(x, axis, ddof)
+            v0, m0 = orc.var_variant(x, 0, axis, ddof)
+            assert arr_same(k, v0) and arr_same(m, m0), name
+            v1, _ = orc.var_variant(x, 1, axis, ddof)
+            assert arr_same(v1, orc.var_twoterm(x, axis, ddof)), name
+
+
+def test_variants_accuracy(orc):
+    """Every variant stays within 2e-6 relative of the float64 two-pass value
+    on the note's datasets (the plain trees lose at most about log2(n) ulps);
+    the two-term correction and the shift do not change it by more."""
+    for name, x, axis in inputs.var_datasets(0):
+        ref64, _ = orc.var_f64(x, axis)
+        for v in VARIANTS:
+            var, _ = orc.var_variant(x, v, axis)
+            err = np.max(np.abs(var - ref64) / ref64)
+            assert err <= 2e-6, (name, v, err)
+
+
+def test_kahan_variant_uses_the_sequential_loop(orc):
+    """Variant 6 differs from the kernel only in s2: recomputing s2 with the
+    comparison-mode Kahan loop over the same d^2 reproduces it."""
+    rng = np.random.default_rng(4)
+    x = (rng.standard_normal((1, 777)) * 3 + 1e4).astype(np.float32)
+    var, mean = orc.var_variant(x, 6, 1)
+    r = x[0]
+    y = (r - r[0]).astype(np.float32)
+    m = np.float32(orc.sum_mode(y, "pairwise") / np.float32(r.size))
+    d = (y - m).astype(np.float32)
+    s2 = orc.sum_mode((d * d).astype(np.float32), "kahan")
+    s1 = orc.sum_mode(d, "pairwise")
+    t = np.float32(s1 / np.float32(r.size))
+    want = np.float32(np.float32(s2 / np.float32(r.size)) - np.float32(t * t))
+    assert var[0] == max(want, np.float32(0)) and mean[0] == np.float32(r[0] + m)
+
+
+def test_f64_kernel_closed_forms_and_exactness(orc):
+    x = np.array([[3, 7, 1, 5, 9, 5, 4, 6]], np.float64)
+    v, m = orc.var_kernel_f64(x, 1)
+    assert v[0] == 5.25 and m[0] == 5.0
+    for val in (1.0, 1e10, 1e300, 1e307):
+        v, m = orc.var_kernel_f64(np.full((1, 3), val), 1)
+        assert v[0] == 0.0 and m[0] == val
+    from fractions import Fraction
+    rng = np.random.default_rng(5)
+    x = rng.normal(1e6, 1.0, (4, 1000))
+    v, m = orc.var_kernel_f64(x, 1, ddof=1)
+    for r in range(4):
+        fr = [Fraction(float(t)) for t in x[r]]
+        mu = sum(fr) / len(fr)
+        exact = sum((t - mu) ** 2 for t in fr) / (len(fr) - 1)
+        assert abs(Fraction(float(v[r])) - exact) / exact < Fraction(1, 10 ** 13), r
+        assert abs(Fraction(float(m[r])) - mu) <= Fraction(1, 2 ** 31)
+
+
+def test_complex_2d_matches_parts_and_the_page(orc):
+    g = load_kv("variance_complex.txt")
+    z = np.array([complex(t) for t in g["values"].split()], dtype=np.complex64)
+    v, m = orc.var_kernel_c64_2d(z.reshape(1, -1), 1)
+    assert v[0] == float(g["var"])
+    v0, _ = orc.var_kernel_c64_2d(z.reshape(-1, 1).copy(), 0)
+    assert v0[0] == float(g["var"])
+    # [7.5e10+7.5e10j]*3 gives 0 (section 3 table)
+    v, m = orc.var_kernel_c64_2d(np.full((1, 3), 7.5e10 + 7.5e10j, np.complex64), 1)
+    assert v[0] == 0.0 and m[0] == np.complex64(7.5e10 + 7.5e10j)
+    rng = np.random.default_rng(6)
+    zz = (rng.standard_normal((5, 37)) + 1j * rng.standard_normal((5, 37)) * 3 + 100).astype(np.complex64)
+    for axis in (0, 1):
+        v, m = orc.var_kernel_c64_2d(zz, axis, 1)
+        vr, mr = orc.var_kernel(np.ascontiguousarray(zz.real), axis, 1)
+        vi, mi = orc.var_kernel(np.ascontiguousarray(zz.imag), axis, 1)
+        assert arr_same(v, (vr + vi).astype(np.float32))
+        assert arr_same(m.real.copy(), mr) and arr_same(m.imag.copy(), mi)
