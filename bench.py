@@ -287,7 +287,7 @@ def run_e2e(args, api, torch, h32, h64, hA, dev, stream):
         v, m = api.stable_var(dA, axis=1, ddof=1)
         ov.copy_(v, non_blocking=True)
         om.copy_(m, non_blocking=True)
-        res["s32"] = api.repro_sum(p32, 3)            # host pointer: the library copies it
+        res["s32"] = api.repro_sum(p32, 3)            # pinned host memory: the kernel reads it in place
         oseg.copy_(api.repro_segsum(dA, axis=1, K=3), non_blocking=True)
         d32.copy_(p32, non_blocking=True)
         api.repro_cumsum(d32, out=d32, K=3)

@@ -158,9 +158,11 @@ def repro_sum_noalloc(x: torch.Tensor, out: torch.Tensor, K: int = 3, stream=Non
 
 def repro_cumsum(x: torch.Tensor, out: torch.Tensor | None = None, K: int = 3, block: int = 0,
                  stream=None) -> torch.Tensor:
-    """Binned cumulative sum; out may be x itself (in place)."""
+    """Binned cumulative sum; out may be x itself (in place).  x and out may
+    be CUDA tensors or CPU tensors (plain host memory is copied by the
+    library and the call then waits for the result)."""
     sfx = _sfx(x)
-    assert x.is_cuda and x.is_contiguous()
+    assert x.is_contiguous()
     if out is None:
         out = torch.empty_like(x)
     assert out.dtype == x.dtype and out.is_contiguous() and out.numel() == x.numel()

@@ -308,11 +308,37 @@ repro_status cumsum_impl(const T* in, T* out, size_t n, int K, cudaStream_t stre
   if (in != out && a0 < b1 && b0 < a1) return REPRO_ERR_OVERLAP;
   repro_status st = validate_env(stream);
   if (st != REPRO_OK) return st;
+  // plain host memory ("Pointer type handling"): the input is copied to
+  // temporary device memory, the output computed there and copied back, and
+  // the call waits for it; device, managed and pinned pointers are used as
+  // they are
+  const bool hin = is_host_only(in), hout = is_host_only(out);
+  Scratch tin, tout;
+  tin.s = tout.s = stream;
+  const T* din = in;
+  T* dout = out;
+  if (hin) {
+    CK(ws_alloc(&tin.p, n * sizeof(T), stream));
+    CK(cudaMemcpyAsync(tin.p, in, n * sizeof(T), cudaMemcpyHostToDevice, stream));
+    din = (const T*)tin.p;
+  }
+  if (hout) {
+    if (in == out) {
+      dout = (T*)tin.p;   // in place on the copy
+    } else {
+      CK(ws_alloc(&tout.p, n * sizeof(T), stream));
+      dout = (T*)tout.p;
+    }
+  }
   Scratch ws;
   ws.s = stream;
   const size_t wsb = cumsum_workspace_bytes<T>((int64_t)n, K);
   if (wsb) CK(ws_alloc(&ws.p, wsb, stream));   // none for a single tile
-  CK(launch_cumsum<T>(in, out, (int64_t)n, K, (unsigned char*)ws.p, l ? l->block : 0, stream));
+  CK(launch_cumsum<T>(din, dout, (int64_t)n, K, (unsigned char*)ws.p, l ? l->block : 0, stream));
+  if (hout) {
+    CK(cudaMemcpyAsync(out, dout, n * sizeof(T), cudaMemcpyDeviceToHost, stream));
+    CK(cudaStreamSynchronize(stream));
+  }
   return REPRO_OK;
 }
 

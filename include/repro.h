@@ -155,8 +155,12 @@ repro_status repro_state_finalize_f64(const void* state, int K, double* result_d
    Reference": cumsum) ------------------------------------------------------ */
 /* out[i] = reproducible sum of in[0..i] (each prefix with its own bin
    index, so out[n-1] equals repro_sum of the whole input).  in == out (exact
-   in place) is allowed; any other overlap gives REPRO_ERR_OVERLAP.  Device or
-   managed pointers; stream-ordered (returns once enqueued). */
+   in place) is allowed; any other overlap gives REPRO_ERR_OVERLAP.  Device,
+   managed or pinned host pointers are used as they are and the call is
+   stream-ordered (returns once enqueued).  Plain host memory ("Pointer type
+   handling"): a host input is copied to temporary device memory, a host
+   output is computed there and copied back, and the call then returns only
+   when out holds the result. */
 repro_status repro_cumsum_f32(const float* in, float* out, size_t n, int K, cudaStream_t stream);
 repro_status repro_cumsum_f64(const double* in, double* out, size_t n, int K, cudaStream_t stream);
 repro_status repro_cumsum_f32_ex(const float* in, float* out, size_t n, int K, cudaStream_t stream,

@@ -103,3 +103,26 @@ def test_full_size_sampled(dt, K):
     pos = np.unique(np.concatenate([rng.integers(0, n, 400), [0, 4095, 4096, 4097, n // 2, n - 1]]))
     want = oracle.adn_cumsum_at(x, pos, K)
     assert same_bits(got[pos], want), first_diff(got[pos], want)
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+@pytest.mark.parametrize("n", [1000, 200_003])
+def test_host_pointers(dt, n):
+    """Plain host memory in and/or out (copied by the library; the call
+    waits), in place on the host, and pinned host memory used directly."""
+    dev()
+    x = inputs.normal_f32(n, seed=9, spikes=True).astype(dt) if dt == F32 else inputs.wide_f64(n, seed=9)
+    want = oracle.adn_cumsum(x, 3)
+    h = torch.from_numpy(x.copy())
+    assert same_bits(api.repro_cumsum(h, K=3).numpy(), want)                      # host -> host
+    o = torch.empty(n, dtype=h.dtype, device="cuda")
+    assert same_bits(api.repro_cumsum(h, out=o, K=3).cpu().numpy(), want)         # host -> device
+    ho = torch.empty(n, dtype=h.dtype)
+    assert same_bits(api.repro_cumsum(to_dev(x), out=ho, K=3).numpy(), want)      # device -> host
+    api.repro_cumsum(h, out=h, K=3)                                               # in place on the host
+    assert same_bits(h.numpy(), want)
+    p = torch.from_numpy(x.copy()).pin_memory()
+    po = torch.empty(n, dtype=p.dtype).pin_memory()
+    api.repro_cumsum(p, out=po, K=3)                                              # pinned: stream-ordered
+    torch.cuda.synchronize()
+    assert same_bits(po.numpy(), want)
