@@ -991,16 +991,45 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_replay(const T* in, T* out, int64
         }
       }
     } else {
-      // |running total| < 2^71: 96-bit words
-      fx::I96 a{(uint32_t)t.w0, (uint32_t)(t.w0 >> 32), (uint32_t)t.w1};
+      // Each rounded value is below 2^38, so a lane starting below 2^62 in
+      // magnitude keeps its running total in 64 bits (the usual case);
+      // otherwise 96-bit words (|running total| < 2^71).
+      const int64_t a0 = (int64_t)t.w0;
+      const uint64_t sx = (uint64_t)(a0 >> 63);
+      if (t.w1 == sx && t.w2 == sx && (a0 >> 62) == (a0 >> 63)) {
+        uint32_t lo = (uint32_t)t.w0, hi = (uint32_t)(t.w0 >> 32);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (b + i < cnt) {
-          const uint32_t bits = __float_as_uint(buf[sb + i]);
-          uint32_t rl, rh;
-          fx::round_f32w(bits, fk, rl, rh);
-          a = fx::i96_add_signed(a, rl, rh, (uint32_t)((int32_t)bits >> 31));
-          buf[sb + i] = fx::i96_to_float(a, bf);
+        for (int i = 0; i < 16; ++i) {
+          if (b + i < cnt) {
+            const uint32_t bits = __float_as_uint(buf[sb + i]);
+            uint32_t rl, rh;
+            fx::round_f32w(bits, fk, rl, rh);
+            const uint32_t sm = (uint32_t)((int32_t)bits >> 31);
+            // a + (R xor sm) + (sm & 1): the +1 of a negation as the first carry
+            asm("{\n\t.reg .u32 c;\n\t"
+                "add.cc.u32 c, %2, 0xFFFFFFFF;\n\t"
+                "addc.cc.u32 %0, %0, %3;\n\t"
+                "addc.u32 %1, %1, %4;\n\t}"
+                : "+r"(lo), "+r"(hi)
+                : "r"(sm & 1u), "r"(rl ^ sm), "r"(rh ^ sm));
+            const int64_t a = (int64_t)(((uint64_t)hi << 32) | lo);
+            uint32_t fb;
+            if (!fx::i64_to_float_normal(a, bf, &fb))
+              fb = __float_as_uint(fx::i96_to_float(fx::I96{lo, hi, (uint32_t)((int32_t)hi >> 31)}, bf));
+            buf[sb + i] = __uint_as_float(fb);
+          }
+        }
+      } else {
+        fx::I96 a{(uint32_t)t.w0, (uint32_t)(t.w0 >> 32), (uint32_t)t.w1};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (b + i < cnt) {
+            const uint32_t bits = __float_as_uint(buf[sb + i]);
+            uint32_t rl, rh;
+            fx::round_f32w(bits, fk, rl, rh);
+            a = fx::i96_add_signed(a, rl, rh, (uint32_t)((int32_t)bits >> 31));
+            buf[sb + i] = fx::i96_to_float(a, bf);
+          }
         }
       }
     }

@@ -112,3 +112,19 @@ def test_many_chunks_in_and_out_of_place_repeatable(dt):
     assert same_bits(cumsum(x, inplace=True), want)
     for _ in range(3):
         assert same_bits(cumsum(x), got)
+
+
+def test_float_totals_beyond_64_bits():
+    """Float: identical values just below the top of their bin (each rounded
+    value about 2^38 grid units) push the running total past 2^62 units after
+    2^24 elements, so later lanes take the 96-bit path instead of 64 bits.
+    Sampled prefixes on both sides of the switch equal the oracle's."""
+    dev()
+    n = (1 << 24) + 300_000
+    x = np.full(n, np.float32(4095.9), np.float32)
+    x[::7] = np.float32(4095.5)
+    got = cumsum(x)
+    pos = np.array([0, 1, 4095, 4096, 1 << 20, (1 << 24) - 1, 1 << 24, (1 << 24) + 1,
+                    (1 << 24) + 4096, (1 << 24) + 150_001, n - 1])
+    want = oracle.adn_cumsum_at(x, pos, 3)
+    assert same_bits(got[pos], want), first_diff(got[pos], want)
