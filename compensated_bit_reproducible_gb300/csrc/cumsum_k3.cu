@@ -98,6 +98,41 @@ __device__ __forceinline__ bool t192_to_double_normal(uint64_t t0, uint64_t t1, 
   return true;
 }
 
+// The same for a signed 128-bit T (t1:t0): one word level fewer.
+__device__ __forceinline__ bool t128_to_double_normal(uint64_t t0, uint64_t t1, int lsb, double* out) {
+  const uint32_t x0 = (uint32_t)t0, x1 = (uint32_t)(t0 >> 32), x2 = (uint32_t)t1, x3 = (uint32_t)(t1 >> 32);
+  const uint32_t s = (uint32_t)((int32_t)x3 >> 31);
+  const bool za = (x3 == s) & (x2 == s);
+  uint32_t W3 = za ? x1 : x3;
+  uint32_t W2 = za ? x0 : x2;
+  uint32_t W1 = za ? 0u : x1;
+  uint32_t W0 = za ? 0u : x0;
+  int e = za ? -64 : 0;
+  if (W3 == s) {
+    W3 = W2;
+    W2 = W1;
+    W1 = W0;
+    W0 = 0u;
+    e -= 32;
+  }
+  const uint32_t lz = (uint32_t)__clz((int)(W3 ^ s));   // 32 only for T = 0 or -1
+  const int E = e + 127 - (int)lz + lsb;
+  if (lz == 32u || (unsigned)(E + 1022) > 2045u) return false;
+  const uint32_t h = fx::funnel_l(W2, W3, lz);
+  const uint32_t l = fx::funnel_l(W1, W2, lz);
+  const uint32_t below = fx::shl_clamp32(W1, (int)lz) | W0;
+  const uint32_t st = ((l & 0x3FFu) | below) != 0u ? 1u : 0u;
+  const uint32_t odd = (l >> 11) & 1u;
+  const uint64_t w = (((uint64_t)h) << 32) | ((l & ~0x3FFu) | st);
+  const uint64_t v = w + 0x3FFu + odd;
+  const uint64_t q = (v >> 11) | ((uint64_t)(v < w) << 53);
+  const uint64_t S = (uint64_t)(int64_t)(int32_t)s;
+  const uint64_t m = (q ^ S) + (S & ((1ull << 53) + 1));
+  *out = __longlong_as_double(
+      (long long)((S & 0x8000000000000000ull) + ((uint64_t)(E + 1022) << 52) + m));
+  return true;
+}
+
 // double: T is a signed 192-bit integer (t2:t1:t0) times 2^lsb.
 __device__ __forceinline__ double round_t192_d(int64_t t2, uint64_t t1, uint64_t t0, int lsb) {
   double r;
@@ -979,15 +1014,52 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_replay(const T* in, T* out, int64
     }
     __syncwarp();
     if constexpr (sizeof(T) == 8) {
+      // Each rounded value is below 2^120 grid units, so a lane starting
+      // below 2^126 in magnitude keeps its running total in 128 bits (the
+      // usual case); otherwise 192.
+      const uint64_t sx = (uint64_t)((int64_t)t.w1 >> 63);
+      if (t.w2 == sx && ((int64_t)t.w1 >> 62) == ((int64_t)t.w1 >> 63)) {
+        uint64_t t0 = t.w0, t1 = t.w1;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (b + i < cnt) {
-          const double v = buf[sb + i];
-          const uint32_t hi = (uint32_t)__double2hiint(v);
-          uint64_t rl, rh;
-          fx::round_f64(hi, (uint32_t)__double2loint(v), kc, rl, rh);
-          t = i192_add_signed(t, rl, rh, (uint64_t)((int64_t)(int32_t)hi >> 31));
-          buf[sb + i] = round_t192_d((int64_t)t.w2, t.w1, t.w0, bf);
+        for (int i = 0; i < 16; ++i) {
+          if (b + i < cnt) {
+            const double v = buf[sb + i];
+            const uint32_t hi = (uint32_t)__double2hiint(v);
+            uint64_t rl, rh;
+            fx::round_f64(hi, (uint32_t)__double2loint(v), kc, rl, rh);
+            const uint32_t sm = (uint32_t)((int32_t)hi >> 31);
+            const uint64_t S = (uint64_t)(int64_t)(int32_t)sm;
+            const uint64_t xl = rl ^ S, xh = rh ^ S;
+            uint32_t r0, r1, r2, r3;
+            // t + (R xor sgn) + (sgn & 1): the +1 of a negation as the first carry
+            asm("{\n\t.reg .u32 c;\n\t"
+                "add.cc.u32 c, %4, 0xFFFFFFFF;\n\t"
+                "addc.cc.u32 %0, %5, %9;\n\t"
+                "addc.cc.u32 %1, %6, %10;\n\t"
+                "addc.cc.u32 %2, %7, %11;\n\t"
+                "addc.u32 %3, %8, %12;\n\t}"
+                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                : "r"(sm & 1u), "r"((uint32_t)t0), "r"((uint32_t)(t0 >> 32)), "r"((uint32_t)t1),
+                  "r"((uint32_t)(t1 >> 32)), "r"((uint32_t)xl), "r"((uint32_t)(xl >> 32)), "r"((uint32_t)xh),
+                  "r"((uint32_t)(xh >> 32)));
+            t0 = ((uint64_t)r1 << 32) | r0;
+            t1 = ((uint64_t)r3 << 32) | r2;
+            double r;
+            if (!t128_to_double_normal(t0, t1, bf, &r)) r = round_t192_d((int64_t)t1 >> 63, t1, t0, bf);
+            buf[sb + i] = r;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (b + i < cnt) {
+            const double v = buf[sb + i];
+            const uint32_t hi = (uint32_t)__double2hiint(v);
+            uint64_t rl, rh;
+            fx::round_f64(hi, (uint32_t)__double2loint(v), kc, rl, rh);
+            t = i192_add_signed(t, rl, rh, (uint64_t)((int64_t)(int32_t)hi >> 31));
+            buf[sb + i] = round_t192_d((int64_t)t.w2, t.w1, t.w0, bf);
+          }
         }
       }
     } else {

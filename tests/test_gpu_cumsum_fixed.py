@@ -128,3 +128,17 @@ def test_float_totals_beyond_64_bits():
                     (1 << 24) + 4096, (1 << 24) + 150_001, n - 1])
     want = oracle.adn_cumsum_at(x, pos, 3)
     assert same_bits(got[pos], want), first_diff(got[pos], want)
+
+
+def test_double_totals_beyond_128_bits():
+    """Double: runs of +v and -v with v just below the top of its bin (each
+    rounded value about 2^119 grid units) move the running total back and
+    forth across 2^126 units, so lanes take both the 128-bit and the 192-bit
+    path.  Every prefix equals the oracle's."""
+    dev()
+    n = 200_003
+    v = 0.999 * 2.0 ** 25
+    i = np.arange(n)
+    x = np.where((i // 1000) % 2 == 0, v, -v)
+    x[::13] *= 0.75
+    check(x)
