@@ -875,14 +875,29 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
     }
     const size_t li = (size_t)ch * 32 + lane;
     if constexpr (sizeof(T) == 8) {
-      fx::I192 own{0, 0, 0};
+      // 16 rounded values below 2^120 grid units: the lane sum fits 128 bits
+      uint32_t o0 = 0, o1 = 0, o2 = 0, o3 = 0;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const uint32_t hi = (uint32_t)__double2hiint(v[i]);
         uint64_t rl, rh;
         fx::round_f64(hi, (uint32_t)__double2loint(v[i]), kc, rl, rh);
-        own = i192_add_signed(own, rl, rh, (uint64_t)((int64_t)(int32_t)hi >> 31));
+        const uint32_t sm = (uint32_t)((int32_t)hi >> 31);
+        const uint64_t S = (uint64_t)(int64_t)(int32_t)sm;
+        const uint64_t xl = rl ^ S, xh = rh ^ S;
+        // own + (R xor sgn) + (sgn & 1): the +1 of a negation as the first carry
+        asm("{\n\t.reg .u32 c;\n\t"
+            "add.cc.u32 c, %4, 0xFFFFFFFF;\n\t"
+            "addc.cc.u32 %0, %0, %5;\n\t"
+            "addc.cc.u32 %1, %1, %6;\n\t"
+            "addc.cc.u32 %2, %2, %7;\n\t"
+            "addc.u32 %3, %3, %8;\n\t}"
+            : "+r"(o0), "+r"(o1), "+r"(o2), "+r"(o3)
+            : "r"(sm & 1u), "r"((uint32_t)xl), "r"((uint32_t)(xl >> 32)), "r"((uint32_t)xh),
+              "r"((uint32_t)(xh >> 32)));
       }
+      const uint64_t ol = ((uint64_t)o1 << 32) | o0, oh = ((uint64_t)o3 << 32) | o2;
+      const fx::I192 own{ol, oh, (uint64_t)((int64_t)oh >> 63)};
       const fx::I192 exc = i192_warp_exclusive(own, &tot);
       const size_t plane = (size_t)nch * 32;
       uint64_t* lp = (uint64_t*)lanep;
