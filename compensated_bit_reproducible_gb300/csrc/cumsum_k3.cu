@@ -989,6 +989,106 @@ __global__ void __launch_bounds__(1024) cf_scan(const fx::I192* __restrict__ cto
   }
 }
 
+// One lane's replay of its 16 elements (the first cnt - b of them when not
+// FULL): running total t from the lane's prefix, a conversion after every
+// element, results written back over the staged inputs.
+template <typename T, bool FULL>
+__device__ __forceinline__ void cf_replay_lanes(T* buf, int sb, int b, int cnt, fx::I192 t, const fx::FxConst& kc,
+                                                const fx::F32Const& fk, int bf) {
+  if constexpr (sizeof(T) == 8) {
+    // Each rounded value is below 2^120 grid units, so a lane starting
+    // below 2^126 in magnitude keeps its running total in 128 bits (the
+    // usual case); otherwise 192.
+    const uint64_t sx = (uint64_t)((int64_t)t.w1 >> 63);
+    if (t.w2 == sx && ((int64_t)t.w1 >> 62) == ((int64_t)t.w1 >> 63)) {
+      uint64_t t0 = t.w0, t1 = t.w1;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (FULL || b + i < cnt) {
+          const double v = buf[sb + i];
+          const uint32_t hi = (uint32_t)__double2hiint(v);
+          uint64_t rl, rh;
+          fx::round_f64(hi, (uint32_t)__double2loint(v), kc, rl, rh);
+          const uint32_t sm = (uint32_t)((int32_t)hi >> 31);
+          const uint64_t S = (uint64_t)(int64_t)(int32_t)sm;
+          const uint64_t xl = rl ^ S, xh = rh ^ S;
+          uint32_t r0, r1, r2, r3;
+          // t + (R xor sgn) + (sgn & 1): the +1 of a negation as the first carry
+          asm("{\n\t.reg .u32 c;\n\t"
+              "add.cc.u32 c, %4, 0xFFFFFFFF;\n\t"
+              "addc.cc.u32 %0, %5, %9;\n\t"
+              "addc.cc.u32 %1, %6, %10;\n\t"
+              "addc.cc.u32 %2, %7, %11;\n\t"
+              "addc.u32 %3, %8, %12;\n\t}"
+              : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+              : "r"(sm & 1u), "r"((uint32_t)t0), "r"((uint32_t)(t0 >> 32)), "r"((uint32_t)t1),
+                "r"((uint32_t)(t1 >> 32)), "r"((uint32_t)xl), "r"((uint32_t)(xl >> 32)), "r"((uint32_t)xh),
+                "r"((uint32_t)(xh >> 32)));
+          t0 = ((uint64_t)r1 << 32) | r0;
+          t1 = ((uint64_t)r3 << 32) | r2;
+          double r;
+          if (!t128_to_double_normal(t0, t1, bf, &r)) r = round_t192_d((int64_t)t1 >> 63, t1, t0, bf);
+          buf[sb + i] = r;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (FULL || b + i < cnt) {
+          const double v = buf[sb + i];
+          const uint32_t hi = (uint32_t)__double2hiint(v);
+          uint64_t rl, rh;
+          fx::round_f64(hi, (uint32_t)__double2loint(v), kc, rl, rh);
+          t = i192_add_signed(t, rl, rh, (uint64_t)((int64_t)(int32_t)hi >> 31));
+          buf[sb + i] = round_t192_d((int64_t)t.w2, t.w1, t.w0, bf);
+        }
+      }
+    }
+  } else {
+    // Each rounded value is below 2^38, so a lane starting below 2^62 in
+    // magnitude keeps its running total in 64 bits (the usual case);
+    // otherwise 96-bit words (|running total| < 2^71).
+    const int64_t a0 = (int64_t)t.w0;
+    const uint64_t sx = (uint64_t)(a0 >> 63);
+    if (t.w1 == sx && t.w2 == sx && (a0 >> 62) == (a0 >> 63)) {
+      uint32_t lo = (uint32_t)t.w0, hi = (uint32_t)(t.w0 >> 32);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (FULL || b + i < cnt) {
+          const uint32_t bits = __float_as_uint(buf[sb + i]);
+          uint32_t rl, rh;
+          fx::round_f32w(bits, fk, rl, rh);
+          const uint32_t sm = (uint32_t)((int32_t)bits >> 31);
+          // a + (R xor sm) + (sm & 1): the +1 of a negation as the first carry
+          asm("{\n\t.reg .u32 c;\n\t"
+              "add.cc.u32 c, %2, 0xFFFFFFFF;\n\t"
+              "addc.cc.u32 %0, %0, %3;\n\t"
+              "addc.u32 %1, %1, %4;\n\t}"
+              : "+r"(lo), "+r"(hi)
+              : "r"(sm & 1u), "r"(rl ^ sm), "r"(rh ^ sm));
+          const int64_t a = (int64_t)(((uint64_t)hi << 32) | lo);
+          uint32_t fb;
+          if (!fx::i64_to_float_normal(a, bf, &fb))
+            fb = __float_as_uint(fx::i96_to_float(fx::I96{lo, hi, (uint32_t)((int32_t)hi >> 31)}, bf));
+          buf[sb + i] = __uint_as_float(fb);
+        }
+      }
+    } else {
+      fx::I96 a{(uint32_t)t.w0, (uint32_t)(t.w0 >> 32), (uint32_t)t.w1};
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        if (FULL || b + i < cnt) {
+          const uint32_t bits = __float_as_uint(buf[sb + i]);
+          uint32_t rl, rh;
+          fx::round_f32w(bits, fk, rl, rh);
+          a = fx::i96_add_signed(a, rl, rh, (uint32_t)((int32_t)bits >> 31));
+          buf[sb + i] = fx::i96_to_float(a, bf);
+        }
+      }
+    }
+  }
+}
+
 // Pass 3.  Each warp replays whole chunks staged in shared memory (coalesced
 // global traffic); lane l starts from chunk prefix + its lane prefix and
 // converts after every one of its 16 elements.
@@ -1028,97 +1128,13 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_replay(const T* in, T* out, int64
       t = fx::i192_add(t, i192_from_i64(((const int64_t*)lanep)[li]));
     }
     __syncwarp();
-    if constexpr (sizeof(T) == 8) {
-      // Each rounded value is below 2^120 grid units, so a lane starting
-      // below 2^126 in magnitude keeps its running total in 128 bits (the
-      // usual case); otherwise 192.
-      const uint64_t sx = (uint64_t)((int64_t)t.w1 >> 63);
-      if (t.w2 == sx && ((int64_t)t.w1 >> 62) == ((int64_t)t.w1 >> 63)) {
-        uint64_t t0 = t.w0, t1 = t.w1;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (b + i < cnt) {
-            const double v = buf[sb + i];
-            const uint32_t hi = (uint32_t)__double2hiint(v);
-            uint64_t rl, rh;
-            fx::round_f64(hi, (uint32_t)__double2loint(v), kc, rl, rh);
-            const uint32_t sm = (uint32_t)((int32_t)hi >> 31);
-            const uint64_t S = (uint64_t)(int64_t)(int32_t)sm;
-            const uint64_t xl = rl ^ S, xh = rh ^ S;
-            uint32_t r0, r1, r2, r3;
-            // t + (R xor sgn) + (sgn & 1): the +1 of a negation as the first carry
-            asm("{\n\t.reg .u32 c;\n\t"
-                "add.cc.u32 c, %4, 0xFFFFFFFF;\n\t"
-                "addc.cc.u32 %0, %5, %9;\n\t"
-                "addc.cc.u32 %1, %6, %10;\n\t"
-                "addc.cc.u32 %2, %7, %11;\n\t"
-                "addc.u32 %3, %8, %12;\n\t}"
-                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                : "r"(sm & 1u), "r"((uint32_t)t0), "r"((uint32_t)(t0 >> 32)), "r"((uint32_t)t1),
-                  "r"((uint32_t)(t1 >> 32)), "r"((uint32_t)xl), "r"((uint32_t)(xl >> 32)), "r"((uint32_t)xh),
-                  "r"((uint32_t)(xh >> 32)));
-            t0 = ((uint64_t)r1 << 32) | r0;
-            t1 = ((uint64_t)r3 << 32) | r2;
-            double r;
-            if (!t128_to_double_normal(t0, t1, bf, &r)) r = round_t192_d((int64_t)t1 >> 63, t1, t0, bf);
-            buf[sb + i] = r;
-          }
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (b + i < cnt) {
-            const double v = buf[sb + i];
-            const uint32_t hi = (uint32_t)__double2hiint(v);
-            uint64_t rl, rh;
-            fx::round_f64(hi, (uint32_t)__double2loint(v), kc, rl, rh);
-            t = i192_add_signed(t, rl, rh, (uint64_t)((int64_t)(int32_t)hi >> 31));
-            buf[sb + i] = round_t192_d((int64_t)t.w2, t.w1, t.w0, bf);
-          }
-        }
-      }
+    // float: full chunks without the per-element bound (measured faster);
+    // double: one predicated body (the specialised copy costs registers)
+    if constexpr (sizeof(T) == 4) {
+      if (cnt == CF_CHUNK) cf_replay_lanes<T, true>(buf, sb, b, cnt, t, kc, fk, bf);
+      else cf_replay_lanes<T, false>(buf, sb, b, cnt, t, kc, fk, bf);
     } else {
-      // Each rounded value is below 2^38, so a lane starting below 2^62 in
-      // magnitude keeps its running total in 64 bits (the usual case);
-      // otherwise 96-bit words (|running total| < 2^71).
-      const int64_t a0 = (int64_t)t.w0;
-      const uint64_t sx = (uint64_t)(a0 >> 63);
-      if (t.w1 == sx && t.w2 == sx && (a0 >> 62) == (a0 >> 63)) {
-        uint32_t lo = (uint32_t)t.w0, hi = (uint32_t)(t.w0 >> 32);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (b + i < cnt) {
-            const uint32_t bits = __float_as_uint(buf[sb + i]);
-            uint32_t rl, rh;
-            fx::round_f32w(bits, fk, rl, rh);
-            const uint32_t sm = (uint32_t)((int32_t)bits >> 31);
-            // a + (R xor sm) + (sm & 1): the +1 of a negation as the first carry
-            asm("{\n\t.reg .u32 c;\n\t"
-                "add.cc.u32 c, %2, 0xFFFFFFFF;\n\t"
-                "addc.cc.u32 %0, %0, %3;\n\t"
-                "addc.u32 %1, %1, %4;\n\t}"
-                : "+r"(lo), "+r"(hi)
-                : "r"(sm & 1u), "r"(rl ^ sm), "r"(rh ^ sm));
-            const int64_t a = (int64_t)(((uint64_t)hi << 32) | lo);
-            uint32_t fb;
-            if (!fx::i64_to_float_normal(a, bf, &fb))
-              fb = __float_as_uint(fx::i96_to_float(fx::I96{lo, hi, (uint32_t)((int32_t)hi >> 31)}, bf));
-            buf[sb + i] = __uint_as_float(fb);
-          }
-        }
-      } else {
-        fx::I96 a{(uint32_t)t.w0, (uint32_t)(t.w0 >> 32), (uint32_t)t.w1};
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (b + i < cnt) {
-            const uint32_t bits = __float_as_uint(buf[sb + i]);
-            uint32_t rl, rh;
-            fx::round_f32w(bits, fk, rl, rh);
-            a = fx::i96_add_signed(a, rl, rh, (uint32_t)((int32_t)bits >> 31));
-            buf[sb + i] = fx::i96_to_float(a, bf);
-          }
-        }
-      }
+      cf_replay_lanes<T, false>(buf, sb, b, cnt, t, kc, fk, bf);
     }
     __syncwarp();
     T* g = out + c0;
