@@ -267,8 +267,10 @@ def load_traffic(kernel_row: str):
 
 def run_e2e(args, api, torch, h32, h64, hA, dev, stream):
     """Same step through the C ABI from pinned host buffers: every input is
-    copied host->device and every result device->host inside the timed
-    region."""
+    copied host->device once and every result device->host inside the timed
+    region.  Input copies run on one stream, in the order the rows use them,
+    and result copies on another, each after an event on the compute stream,
+    so copies in both directions overlap the rows' kernels."""
     p32 = torch.from_numpy(h32).pin_memory()
     p64 = torch.from_numpy(h64).pin_memory()
     pA = torch.from_numpy(hA).pin_memory()
@@ -277,25 +279,53 @@ def run_e2e(args, api, torch, h32, h64, hA, dev, stream):
     ov = torch.empty(ROWS, dtype=torch.float32).pin_memory()
     om = torch.empty(ROWS, dtype=torch.float32).pin_memory()
     oseg = torch.empty(ROWS, dtype=torch.float32).pin_memory()
+    os32 = torch.empty(1, dtype=torch.float32).pin_memory()
+    os64 = torch.empty(1, dtype=torch.float64).pin_memory()
     d32 = torch.empty(N_SUM, dtype=torch.float32, device=dev)
     d64 = torch.empty(N_SUM, dtype=torch.float64, device=dev)
+    c32 = torch.empty(N_SUM, dtype=torch.float32, device=dev)
+    c64 = torch.empty(N_SUM, dtype=torch.float64, device=dev)
     dA = torch.empty(ROWS, COLS, dtype=torch.float32, device=dev)
-    res = {}
+    s32 = torch.empty(1, dtype=torch.float32, device=dev)
+    s64 = torch.empty(1, dtype=torch.float64, device=dev)
+    seg = torch.empty(ROWS, dtype=torch.float32, device=dev)
+    copy_stream = torch.cuda.Stream(device=dev)
+    h2d_stream = torch.cuda.Stream(device=dev)
+
+    def back(dst, src):
+        # device->host on the copy stream once `src` is complete
+        ev = torch.cuda.Event()
+        ev.record(stream)
+        copy_stream.wait_event(ev)
+        with torch.cuda.stream(copy_stream):
+            dst.copy_(src, non_blocking=True)
 
     def one():
-        dA.copy_(pA, non_blocking=True)
-        v, m = api.stable_var(dA, axis=1, ddof=1)
-        ov.copy_(v, non_blocking=True)
-        om.copy_(m, non_blocking=True)
-        res["s32"] = api.repro_sum(p32, 3)            # pinned host memory: the kernel reads it in place
-        oseg.copy_(api.repro_segsum(dA, axis=1, K=3), non_blocking=True)
-        d32.copy_(p32, non_blocking=True)
-        api.repro_cumsum(d32, out=d32, K=3)
-        oc32.copy_(d32, non_blocking=True)
-        res["s64"] = api.repro_sum(p64, 3)
-        d64.copy_(p64, non_blocking=True)
-        api.repro_cumsum(d64, out=d64, K=3)
-        oc64.copy_(d64, non_blocking=True)
+        # inputs host->device on their own stream, in the order the rows use them
+        evs = []
+        with torch.cuda.stream(h2d_stream):
+            for dst, src in ((dA, pA), (d32, p32), (d64, p64)):
+                dst.copy_(src, non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(h2d_stream)
+                evs.append(ev)
+        with torch.cuda.stream(stream):
+            stream.wait_event(evs[0])
+            v, m = api.stable_var(dA, axis=1, ddof=1)
+            back(ov, v)
+            back(om, m)
+            api.repro_segsum(dA, axis=1, K=3, out=seg)
+            back(oseg, seg)
+            stream.wait_event(evs[1])
+            api.repro_sum_async(d32, s32, 3)
+            back(os32, s32)
+            api.repro_cumsum(d32, out=c32, K=3)
+            back(oc32, c32)
+            stream.wait_event(evs[2])
+            api.repro_sum_async(d64, s64, 3)
+            back(os64, s64)
+            api.repro_cumsum(d64, out=c64, K=3)
+            back(oc64, c64)
         torch.cuda.synchronize()
 
     one()
@@ -305,7 +335,7 @@ def run_e2e(args, api, torch, h32, h64, hA, dev, stream):
         one()
     dt = (time.perf_counter() - t) / n
     elems = sum(nn for _, nn, _ in ROWS_SPEC)
-    h2d = 4 * N_SUM * 2 + 8 * N_SUM * 2 + 4 * ROWS * COLS
+    h2d = 4 * N_SUM + 8 * N_SUM + 4 * ROWS * COLS
     d2h = 4 * N_SUM + 8 * N_SUM + 4 + 8 + 3 * 4 * ROWS
     return {"value": round(elems / dt / 1e9, 3), "unit": "GElements/s", "ms_per_step": round(dt * 1e3, 3),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
