@@ -310,6 +310,52 @@ __global__ void __launch_bounds__(1024) segsum_rows_kernel(const float* __restri
   }
 }
 
+// One warp per row (rows up to SEG_WARP_MAX columns): the lanes accumulate
+// strided parts of the row and merge exactly inside the warp (block-wide
+// minimum index replaced by the warp's, fold sums reduced by shuffles), so a
+// row needs no shared memory or block barrier and many rows are in flight
+// per SM.  Same bits as the block kernel: the merge is exact.
+template <int KT, int U>
+__global__ void __launch_bounds__(256) segsum_rows_warp(const float* __restrict__ x, int64_t rows, int64_t cols,
+                                                        int K, float* __restrict__ out) {
+  typedef AccF<KT> Acc;
+  constexpr int N = Acc::N;
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t GW = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t r = gw; r < rows; r += GW) {
+    Acc acc;
+    acc.init(K);
+    accumulate_range<float, Acc, U>(acc, x + r * cols, cols, lane, 32);
+    acc.finish();
+    const int Iw = __reduce_min_sync(0xffffffffu, acc.I);
+    const int fl = (int)__reduce_or_sync(0xffffffffu, (unsigned)acc.flags);
+    const int d = acc.I - Iw;
+    W128 F[N];
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      W128 v = W128{0, 0};
+      if (k < K) {
+        v = w_from(fold_at<N, int64_t>(acc.L, K, k - d));
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) v = w_add(v, shfl_xor_w(v, m));
+      }
+      F[k] = v;
+    }
+    if (lane == 0) {
+      if constexpr (KT != 0) {
+        out[r] = convert_fast<float, KT>(Iw, fl, F);
+      } else {
+        State<N> st;
+        st.I = Iw;
+        st.flags = fl;
+        for (int k = 0; k < N; ++k) st.F[k] = F[k];
+        out[r] = convert_state<float, N>(st, K);
+      }
+    }
+  }
+}
+
 // One thread per column, rows walked in order (coalesced across columns).
 template <int KT>
 __global__ void __launch_bounds__(256) segsum_cols_kernel(const float* __restrict__ x, int64_t rows,
@@ -462,9 +508,18 @@ template int sum_blocks_per_sm<double>(int, int);
 
 size_t sum_workspace_bytes(int K, int grid) { return 256 + (size_t)grid * (16 + 16 * (size_t)K) + 64; }
 
+// Rows up to this many columns use one warp per row.
+constexpr int64_t SEG_WARP_MAX = 1 << 16;
+
 cudaError_t launch_segsum(const float* x, int64_t rows, int64_t cols, int axis, int K, float* out, int grid,
                           int block, cudaStream_t s) {
-  if (axis == 1) {
+  if (axis == 1 && cols <= SEG_WARP_MAX && (K == 2 || K == 3)) {
+    // one warp per row, eight rows per block
+    const int64_t g = (rows + 7) / 8;
+    const unsigned wg = (unsigned)(g < 65535 * 16 ? g : 65535 * 16);
+    if (K == 3) segsum_rows_warp<3, 4><<<wg, 256, 0, s>>>(x, rows, cols, K, out);
+    else segsum_rows_warp<2, 4><<<wg, 256, 0, s>>>(x, rows, cols, K, out);
+  } else if (axis == 1) {
     switch (K) {
       case 3: segsum_rows_kernel<3, 4><<<grid, block, 0, s>>>(x, rows, cols, K, out); break;
       case 2: segsum_rows_kernel<2, 4><<<grid, block, 0, s>>>(x, rows, cols, K, out); break;

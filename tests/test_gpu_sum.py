@@ -180,6 +180,27 @@ def test_segmented_rows_and_cols():
         assert same_bits(got, oracle.segsum(x, axis=1, K=K))
 
 
+def test_segmented_warp_and_block_rows_and_specials():
+    """Rows up to 65536 columns take one warp per row, longer rows one block:
+    both equal the oracle, also with Inf/NaN and tiny or huge rows."""
+    dev()
+    for rows, cols in ((3, 65536), (2, 65537), (2, 70001)):
+        x = inputs.offset_rows(rows, cols, seed=cols)
+        got = api.repro_segsum(to_dev(x), axis=1, K=3).cpu().numpy()
+        assert same_bits(got, oracle.segsum(x, axis=1, K=3)), (rows, cols)
+    x = inputs.offset_rows(8, 1000, seed=4)
+    x[1, 5] = np.nan
+    x[2, 7] = np.inf
+    x[3, 9] = np.inf
+    x[3, 10] = -np.inf
+    x[4, :] = 0.0
+    x[5, :] = np.float32(1e-45)
+    x[6, ::2] = np.float32(3e38)
+    for K in (2, 3):
+        got = api.repro_segsum(to_dev(x), axis=1, K=K).cpu().numpy()
+        assert same_bits(got, oracle.segsum(x, axis=1, K=K)), K
+
+
 @pytest.mark.slow
 def test_segmented_full_size_sampled_rows():
     """[4096, 4096] rows (offset + noise and the heavy-tailed variant): all
