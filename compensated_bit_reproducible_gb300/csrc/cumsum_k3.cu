@@ -815,6 +815,52 @@ __device__ __forceinline__ void cf_stage(T* buf, const T* g, int cnt, int lane) 
   }
 }
 
+// Double totals: each thread deposits its elements' rounded values into
+// 64-bit word cells in shared memory (cell k + 8 s: word position k of
+// M' 2^u for the sign s, the rounding of the binned sum's fixed-index
+// deposit), the cells accumulating over all of the thread's chunks.  The
+// value of the cells is sum_s (-1)^s sum_{k = 2..6} cell 2^(32 (k - 2)) in
+// units of g_f (positions 0, 1 lie below the grid; 7 only beyond the guessed
+// bin, which fails the guess), so a lane's sum over its 16 elements is the
+// difference of the values after and before them.
+constexpr int CT_CELLS = 16;
+template <typename T>
+__host__ __device__ constexpr int ct_cell_bytes() {
+  return sizeof(T) == 8 ? CT_CELLS * C3_BLOCK * 8 : 0;
+}
+
+__device__ __forceinline__ void ct_deposit(uint32_t hi, uint32_t lo, const fx::FxConst& k, uint32_t c8, uint64_t* A) {
+  const uint32_t eb = fx::mad32(hi, k.one + k.one, 0u) >> 21;   // biased exponent
+  const int us = (int)fx::mad32(eb, k.one, k.Cp);               // shift of M
+  const uint32_t u = (uint32_t)max(us, 0);
+  const uint32_t c = min(u >> 5, 5u);
+  const uint32_t mh = (hi & 0xFFFFFu) | 0x100000u;
+  const uint32_t hl = fx::shl_clamp32(1u, (int)fx::mad32(u, k.negone, k.c63));
+  const uint32_t hh = fx::shl_clamp32(1u, (int)fx::mad32(u, k.negone, k.c31));
+  const uint32_t b = min(mh & fx::mad32(hl, k.c256, 0u), 1u);   // rounding bit of fold K-2
+  const uint64_t Mp = ((((uint64_t)mh) << 32) | lo) + ((((uint64_t)hh) << 32) | hl) - (uint64_t)b;
+  const uint32_t lo2 = (uint32_t)Mp, mh2 = (uint32_t)(Mp >> 32);
+  const uint32_t w0 = fx::funnel_l(0u, lo2, u);
+  const uint32_t w1 = fx::funnel_l(lo2, mh2, u);
+  const uint32_t w2 = fx::funnel_l(mh2, 0u, u);
+  uint64_t* p = A + fx::mad32(fx::mad32(hi >> 31, c8, c), (uint32_t)C3_BLOCK, 0u);
+  p[0] = fx::madw(w0, k.one, p[0]);
+  p[C3_BLOCK] = fx::madw(w1, k.one, p[C3_BLOCK]);
+  p[2 * C3_BLOCK] = fx::madw(w2, k.one, p[2 * C3_BLOCK]);
+}
+
+__device__ __forceinline__ fx::I192 ct_value(const uint64_t* A) {
+  fx::I192 t{0, 0, 0};
+#pragma unroll
+  for (int s = 0; s < 2; ++s)
+#pragma unroll
+    for (int w = 2; w < 7; ++w) {
+      const fx::I192 v = fx::i192_from_shifted(W128{A[(w + 8 * s) * C3_BLOCK], 0}, w - 2);
+      t = fx::i192_add(t, s ? fx::i192_neg(v) : v);
+    }
+  return t;
+}
+
 // Pass 1.  Persistent blocks; each warp takes whole chunks: staged in shared
 // memory, lane l sums its 16 contiguous elements (double: one rounding each;
 // float: the binned sum's floating-point primaries at the fixed index, whose
@@ -830,6 +876,7 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
   typedef Geom<T> G;
   __shared__ T sm[CF_WARPS * CF_PAD];
   __shared__ unsigned s_emax;
+  extern __shared__ __align__(16) unsigned char ct_smem[];   // double: the word cells
   int eb_max;
   const int L = fx::guess_index<T>(in, n, 3, &s_emax, &eb_max);
   const int bf = beta<T>(L + 2);
@@ -851,6 +898,13 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
   if constexpr (sizeof(T) == 4) {
     facc.init(3);
     if (L < facc.I) facc.raise(L);
+  }
+  uint64_t* A = (uint64_t*)ct_smem + threadIdx.x;   // double: this thread's cells
+  fx::I192 prev{0, 0, 0};                             // double: value of the cells so far
+  const uint32_t c8 = 8u * one;
+  if constexpr (sizeof(T) == 8) {
+#pragma unroll
+    for (int k = 0; k < CT_CELLS; ++k) A[k * C3_BLOCK] = 0;
   }
   const int64_t gw = (int64_t)blockIdx.x * CF_WARPS + warp, GW = (int64_t)gridDim.x * CF_WARPS;
   for (int64_t ch = gw; ch < nch; ch += GW) {
@@ -875,29 +929,13 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
     }
     const size_t li = (size_t)ch * 32 + lane;
     if constexpr (sizeof(T) == 8) {
-      // 16 rounded values below 2^120 grid units: the lane sum fits 128 bits
-      uint32_t o0 = 0, o1 = 0, o2 = 0, o3 = 0;
+      // padding elements are zero and deposit nothing
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t hi = (uint32_t)__double2hiint(v[i]);
-        uint64_t rl, rh;
-        fx::round_f64(hi, (uint32_t)__double2loint(v[i]), kc, rl, rh);
-        const uint32_t sm = (uint32_t)((int32_t)hi >> 31);
-        const uint64_t S = (uint64_t)(int64_t)(int32_t)sm;
-        const uint64_t xl = rl ^ S, xh = rh ^ S;
-        // own + (R xor sgn) + (sgn & 1): the +1 of a negation as the first carry
-        asm("{\n\t.reg .u32 c;\n\t"
-            "add.cc.u32 c, %4, 0xFFFFFFFF;\n\t"
-            "addc.cc.u32 %0, %0, %5;\n\t"
-            "addc.cc.u32 %1, %1, %6;\n\t"
-            "addc.cc.u32 %2, %2, %7;\n\t"
-            "addc.u32 %3, %3, %8;\n\t}"
-            : "+r"(o0), "+r"(o1), "+r"(o2), "+r"(o3)
-            : "r"(sm & 1u), "r"((uint32_t)xl), "r"((uint32_t)(xl >> 32)), "r"((uint32_t)xh),
-              "r"((uint32_t)(xh >> 32)));
-      }
-      const uint64_t ol = ((uint64_t)o1 << 32) | o0, oh = ((uint64_t)o3 << 32) | o2;
-      const fx::I192 own{ol, oh, (uint64_t)((int64_t)oh >> 63)};
+      for (int i = 0; i < 16; ++i)
+        ct_deposit((uint32_t)__double2hiint(v[i]), (uint32_t)__double2loint(v[i]), kc, c8, A);
+      const fx::I192 val = ct_value(A);
+      const fx::I192 own = fx::i192_add(val, fx::i192_neg(prev));
+      prev = val;
       const fx::I192 exc = i192_warp_exclusive(own, &tot);
       const size_t plane = (size_t)nch * 32;
       uint64_t* lp = (uint64_t*)lanep;
@@ -1185,6 +1223,24 @@ static int cf_sm_count() {
   return cached[dev];
 }
 
+// cf_totals<double> takes its word cells as dynamic shared memory beyond the
+// default limit: allow it once per device.
+template <typename T>
+static cudaError_t ct_prepare() {
+  if constexpr (sizeof(T) == 4) {
+    return cudaSuccess;
+  } else {
+    static bool done[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(cf_totals<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, ct_cell_bytes<T>());
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
+    return e;
+  }
+}
+
 template <typename K, typename... A>
 static cudaError_t launch_gated(K kernel, int64_t grid, int block, size_t smem, cudaStream_t s, bool pdl, A... args) {
   cudaLaunchConfig_t cfg = {};
@@ -1249,8 +1305,10 @@ cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, 
     fx::I192* btot = lpre + nc;
     fx::I192* bpre = btot + ncb;
     if ((e = cudaMemsetAsync(ctl, 0, 256, s)) != cudaSuccess) return e;
+    if ((e = ct_prepare<T>()) != cudaSuccess) return e;
     int bt = 0, br = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bt, cf_totals<T>, C3_BLOCK, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bt, cf_totals<T>, C3_BLOCK, ct_cell_bytes<T>()) !=
+            cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&br, cf_replay<T>, C3_BLOCK, 0) != cudaSuccess) {
       cudaGetLastError();
       bt = br = 1;
@@ -1258,7 +1316,7 @@ cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, 
     const int64_t sms = cf_sm_count();
     const int64_t wb = (nc + CF_WARPS - 1) / CF_WARPS;   // blocks that have a chunk
     const int64_t gt = max((int64_t)1, min(wb, sms * max(bt, 1))), gr = max((int64_t)1, min(wb, sms * max(br, 1)));
-    cf_totals<T><<<(unsigned)gt, C3_BLOCK, 0, s>>>(in, n, nc, 1u, ctl, lanep, ctot);
+    cf_totals<T><<<(unsigned)gt, C3_BLOCK, ct_cell_bytes<T>(), s>>>(in, n, nc, 1u, ctl, lanep, ctot);
     cf_scan<<<(unsigned)ncb, 1024, 0, s>>>(ctot, nc, ctl, lpre, btot, bpre);
     cf_replay<T><<<(unsigned)gr, C3_BLOCK, 0, s>>>(in, out, n, nc, 1u, ctl, lanep, lpre, bpre);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
