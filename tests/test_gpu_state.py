@@ -126,3 +126,18 @@ def test_mismatched_k_or_type_finalizes_to_nan():
     assert np.isnan(final(a, F32, 3))
     c = api.state_new(torch.float64, 3)
     assert np.isnan(final(c, F64, 2))   # finalized with another K
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_state_bytes_through_host_memory(dt):
+    """A state copied to host memory and back (as it would travel to another
+    GPU) merges like the original: the layout holds no pointers."""
+    dev()
+    x = data(dt, 50_000, 80)
+    a = deposit_all(x[:20_000], 3, [0, 20_000])
+    b = deposit_all(x[20_000:], 3, [0, 30_000])
+    host = b.cpu().numpy().copy()
+    assert host.size == api.state_bytes(3)
+    b2 = torch.from_numpy(host).to(a.device)
+    api.state_merge(a, b2, TD[dt], 3)
+    assert same_bits(final(a, dt, 3), oracle.adn_sum(x, 3, "fp"))
