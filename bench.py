@@ -357,6 +357,7 @@ def run_comparisons(api, torch, x32, x64, A, stream):
         return a.elapsed_time(b) / reps
 
     A64 = A.double()
+    c64k6 = torch.empty_like(x64)
     AC = A.view(torch.complex64)   # [4096, 2048] complex pairs of the same floats
     st32 = api.state_new(torch.float32, 3)
     st64 = api.state_new(torch.float64, 3)
@@ -372,6 +373,8 @@ def run_comparisons(api, torch, x32, x64, A, stream):
 
     out = {}
     for name, fn, n in (
+        ("sum_f64_k6_1e8", lambda: api.repro_sum_async(x64, r64, 6), N_SUM),
+        ("cumsum_f64_k6_1e8", lambda: api.repro_cumsum(x64, out=c64k6, K=6), N_SUM),
         ("state_8_chunks_f32_1e8", lambda: chunked(x32, st32, r32), N_SUM),
         ("state_8_chunks_f64_1e8", lambda: chunked(x64, st64, r64), N_SUM),
         ("naive_sum_f32_1e8", lambda: api.compare_sum(x32, "naive"), N_SUM),
