@@ -314,9 +314,10 @@ __global__ void __launch_bounds__(1024) segsum_rows_kernel(const float* __restri
 // strided parts of the row and merge exactly inside the warp (block-wide
 // minimum index replaced by the warp's, fold sums reduced by shuffles), so a
 // row needs no shared memory or block barrier and many rows are in flight
-// per SM.  Same bits as the block kernel: the merge is exact.
+// per SM (64 registers: 32 warps per SM, so 4096 rows fit one wave).  Same
+// bits as the block kernel: the merge is exact.
 template <int KT, int U>
-__global__ void __launch_bounds__(256) segsum_rows_warp(const float* __restrict__ x, int64_t rows, int64_t cols,
+__global__ void __launch_bounds__(256, 4) segsum_rows_warp(const float* __restrict__ x, int64_t rows, int64_t cols,
                                                         int K, float* __restrict__ out) {
   typedef AccF<KT> Acc;
   constexpr int N = Acc::N;
@@ -517,8 +518,8 @@ cudaError_t launch_segsum(const float* x, int64_t rows, int64_t cols, int axis, 
     // one warp per row, eight rows per block
     const int64_t g = (rows + 7) / 8;
     const unsigned wg = (unsigned)(g < 65535 * 16 ? g : 65535 * 16);
-    if (K == 3) segsum_rows_warp<3, 4><<<wg, 256, 0, s>>>(x, rows, cols, K, out);
-    else segsum_rows_warp<2, 4><<<wg, 256, 0, s>>>(x, rows, cols, K, out);
+    if (K == 3) segsum_rows_warp<3, 2><<<wg, 256, 0, s>>>(x, rows, cols, K, out);
+    else segsum_rows_warp<2, 2><<<wg, 256, 0, s>>>(x, rows, cols, K, out);
   } else if (axis == 1) {
     switch (K) {
       case 3: segsum_rows_kernel<3, 4><<<grid, block, 0, s>>>(x, rows, cols, K, out); break;

@@ -130,6 +130,14 @@ template <typename T> __device__ __forceinline__ N2<T> shfl_down_node(N2<T> v, i
                __shfl_down_sync(0xffffffffu, v.d, d)};
 }
 
+template <typename T> __device__ __forceinline__ T shfl_node(T v, int src) {
+  return __shfl_sync(0xffffffffu, v, src);
+}
+template <typename T> __device__ __forceinline__ N2<T> shfl_node(N2<T> v, int src) {
+  return N2<T>{TS<T>{__shfl_sync(0xffffffffu, v.q.s, src), __shfl_sync(0xffffffffu, v.q.c, src)},
+               __shfl_sync(0xffffffffu, v.d, src)};
+}
+
 // Combine the per-thread subtree roots of one slice, in tree order.  Threads
 // are numbered by `pos` (0..P-1, P = number of participating threads, a
 // multiple of 32 when P > 32, laid out so that pos p and p+1 are adjacent
@@ -163,6 +171,34 @@ __device__ Node tree_combine_block(Node v, bool have, int P, Node* sm, bool* smv
   }
   __syncthreads();
   return v;
+}
+
+// tree_combine_block when every one of the P threads holds a subtree; the
+// root is returned in every thread.  One barrier: the warp roots go to
+// shared memory and each warp combines them with shuffles (lanes 0..nw-1
+// hold roots 0..nw-1).  The caller must pass a barrier between the read of
+// `sm` here and its next write (alternating two arrays does that).
+template <typename Node, typename F>
+__device__ __forceinline__ Node tree_combine_block_all(Node v, int P, Node* sm, F comb) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    Node o = shfl_down_node(v, d);
+    if ((lane & (2 * d - 1)) == 0) v = comb(v, o);
+  }
+  const int nw = P >> 5;
+  if (nw > 1) {
+    if (lane == 0) sm[warp] = v;
+    __syncthreads();
+    v = sm[lane < nw ? lane : 0];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      if (d >= nw) break;
+      Node o = shfl_down_node(v, d);
+      if ((lane & (2 * d - 1)) == 0 && lane + d < nw) v = comb(v, o);
+    }
+  }
+  return shfl_node(v, 0);
 }
 
 template <typename T>
@@ -373,6 +409,16 @@ __device__ __forceinline__ bool reg_tree(Node* a, int m, F comb) {
   return m > 0;
 }
 
+// The same tree when all C leaves are present: no per-node presence tests.
+template <typename Node, int C, typename F>
+__device__ __forceinline__ void reg_tree_full(Node* a, F comb) {
+#pragma unroll
+  for (int w = C; w > 1; w >>= 1) {
+#pragma unroll
+    for (int i = 0; i < w / 2; ++i) a[i] = comb(a[2 * i], a[2 * i + 1]);
+  }
+}
+
 template <typename T> struct Vec16;
 template <> struct Vec16<float> {
   typedef float4 type;
@@ -403,6 +449,8 @@ __global__ void __launch_bounds__(256) var_rows_reg(const T* __restrict__ x, int
   const int b = threadIdx.x * C;
   int m = n - b;
   m = m < 0 ? 0 : (m > C ? C : m);
+  // every thread of the block holds C leaves (the row fills the block)
+  const bool all = n >= (int)blockDim.x * C;
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
     const T* row = x + r * cols * es;
     const T x0 = __ldg(row);
@@ -420,11 +468,17 @@ __global__ void __launch_bounds__(256) var_rows_reg(const T* __restrict__ x, int
       T t1[C];
 #pragma unroll
       for (int i = 0; i < C; ++i) t1[i] = leaf1<T, V>(v[i], x0);
-      bool h1 = reg_tree<T, C>(t1, m, f_combine<T>);
-      T sum1 = tree_combine_block<T>(t1[0], h1, blockDim.x, smf, smv, f_combine<T>);
-      if (threadIdx.x == 0) bc[0] = mean_of<T, V>(sum1, n);
-      __syncthreads();
-      mu = bc[0];
+      if (all) {
+        // every thread gets the root and computes the same mean
+        reg_tree_full<T, C>(t1, f_combine<T>);
+        mu = mean_of<T, V>(tree_combine_block_all<T>(t1[0], blockDim.x, smf, f_combine<T>), n);
+      } else {
+        bool h1 = reg_tree<T, C>(t1, m, f_combine<T>);
+        T sum1 = tree_combine_block<T>(t1[0], h1, blockDim.x, smf, smv, f_combine<T>);
+        if (threadIdx.x == 0) bc[0] = mean_of<T, V>(sum1, n);
+        __syncthreads();
+        mu = bc[0];
+      }
     }
     // pass 2
     N2<T> t2[C];
@@ -433,13 +487,21 @@ __global__ void __launch_bounds__(256) var_rows_reg(const T* __restrict__ x, int
       T d = leaf_d<T, V>(v[i], x0, mu);
       t2[i] = N2<T>{TS<T>{mul_rn(d, d), (T)0}, d};
     }
-    bool h2 = reg_tree<N2<T>, C>(t2, m, n2_combine<T>);
-    N2<T> tot = tree_combine_block<N2<T>>(t2[0], h2, blockDim.x, sm2, smv, n2_combine<T>);
+    N2<T> tot;
+    if (all) {
+      // one barrier per pass: smf and sm2 alternate, so each is rewritten
+      // only after the other pass's barrier
+      reg_tree_full<N2<T>, C>(t2, n2_combine<T>);
+      tot = tree_combine_block_all<N2<T>>(t2[0], blockDim.x, sm2, n2_combine<T>);
+    } else {
+      bool h2 = reg_tree<N2<T>, C>(t2, m, n2_combine<T>);
+      tot = tree_combine_block<N2<T>>(t2[0], h2, blockDim.x, sm2, smv, n2_combine<T>);
+    }
     if (threadIdx.x == 0) {
       T ks = St::COMP == 2 ? kahan_sq<T>(row, n, es, x0, mu) : (T)0;
       finish_slice<T, V>(tot, ks, x0, mu, n, ddof, out, mean_out, r, io);
     }
-    __syncthreads();
+    if (!all) __syncthreads();
   }
 }
 

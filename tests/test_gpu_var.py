@@ -62,6 +62,20 @@ def test_ragged_shapes(rows, cols, axis):
         assert same_bits(tt, oracle.var_twoterm(x, axis, ddof))
 
 
+@pytest.mark.parametrize("rows,cols", [(3000, 37), (2600, 300), (1900, 1000), (1400, 2000), (1300, 4096),
+                                       (1217, 4093), (1500, 256), (1300, 512), (1250, 1024), (1230, 2048)])
+def test_more_rows_than_resident_blocks(rows, cols):
+    """Row counts above one wave of resident blocks, for every per-thread
+    leaf count C (1 to 16), rows that fill the block exactly (every thread
+    holds C leaves) and rows with a ragged last thread."""
+    dev()
+    x = inputs.offset_rows(rows, cols, seed=rows + cols, heavy=(cols % 2 == 1))
+    v, m = gpu_var(x, 1, 1)
+    wv, wm = oracle.var_kernel(x, 1, 1)
+    assert same_bits(v, wv), first_diff(v, wv)
+    assert same_bits(m, wm)
+
+
 def test_nonfinite_inputs():
     dev()
     x = inputs.offset_rows(6, 513, seed=1)
