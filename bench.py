@@ -270,7 +270,9 @@ def run_e2e(args, api, torch, h32, h64, hA, dev, stream):
     copied host->device once and every result device->host inside the timed
     region.  Input copies run on one stream, in the order the rows use them,
     and result copies on another, each after an event on the compute stream,
-    so copies in both directions overlap the rows' kernels."""
+    so copies in both directions overlap the rows' kernels.  The host link
+    (about 208 GB/s in, 191 GB/s out, measured with pinned copies) bounds
+    this number, not the kernels."""
     p32 = torch.from_numpy(h32).pin_memory()
     p64 = torch.from_numpy(h64).pin_memory()
     pA = torch.from_numpy(hA).pin_memory()
@@ -301,31 +303,33 @@ def run_e2e(args, api, torch, h32, h64, hA, dev, stream):
             dst.copy_(src, non_blocking=True)
 
     def one():
-        # inputs host->device on their own stream, in the order the rows use them
+        # inputs host->device on their own stream, in the order the rows use
+        # them: the double array first, so that its 800 MB cumulative sum
+        # goes back over the link while the other inputs still come in
         evs = []
         with torch.cuda.stream(h2d_stream):
-            for dst, src in ((dA, pA), (d32, p32), (d64, p64)):
+            for dst, src in ((d64, p64), (dA, pA), (d32, p32)):
                 dst.copy_(src, non_blocking=True)
                 ev = torch.cuda.Event()
                 ev.record(h2d_stream)
                 evs.append(ev)
         with torch.cuda.stream(stream):
             stream.wait_event(evs[0])
+            api.repro_sum_async(d64, s64, 3)
+            back(os64, s64)
+            api.repro_cumsum(d64, out=c64, K=3)
+            back(oc64, c64)
+            stream.wait_event(evs[1])
             v, m = api.stable_var(dA, axis=1, ddof=1)
             back(ov, v)
             back(om, m)
             api.repro_segsum(dA, axis=1, K=3, out=seg)
             back(oseg, seg)
-            stream.wait_event(evs[1])
+            stream.wait_event(evs[2])
             api.repro_sum_async(d32, s32, 3)
             back(os32, s32)
             api.repro_cumsum(d32, out=c32, K=3)
             back(oc32, c32)
-            stream.wait_event(evs[2])
-            api.repro_sum_async(d64, s64, 3)
-            back(os64, s64)
-            api.repro_cumsum(d64, out=c64, K=3)
-            back(oc64, c64)
         torch.cuda.synchronize()
 
     one()

@@ -173,19 +173,21 @@ __device__ Node tree_combine_block(Node v, bool have, int P, Node* sm, bool* smv
   return v;
 }
 
-// tree_combine_block when every one of the P threads holds a subtree; the
-// root is returned in every thread.  One barrier: the warp roots go to
-// shared memory and each warp combines them with shuffles (lanes 0..nw-1
-// hold roots 0..nw-1).  The caller must pass a barrier between the read of
-// `sm` here and its next write (alternating two arrays does that).
+// tree_combine_block when every one of the P threads holds a subtree (P a
+// power of two); the root is returned in every thread.  At the level that
+// pairs nodes d apart, lane L (L a multiple of 2d) combines with lane L + d;
+// the other lanes combine too, unconditionally, and their values are never
+// read by a lane that carries the tree: lane L + d at level d is a multiple
+// of d, so it was a left node, combined correctly, at every lower level.
+// One barrier: the warp roots go to shared memory and each warp combines
+// them the same way (lanes 0..nw-1 hold roots 0..nw-1).  The caller must
+// pass a barrier between the read of `sm` here and its next write
+// (alternating two arrays does that).
 template <typename Node, typename F>
 __device__ __forceinline__ Node tree_combine_block_all(Node v, int P, Node* sm, F comb) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    Node o = shfl_down_node(v, d);
-    if ((lane & (2 * d - 1)) == 0) v = comb(v, o);
-  }
+  for (int d = 1; d < 32; d <<= 1) v = comb(v, shfl_down_node(v, d));
   const int nw = P >> 5;
   if (nw > 1) {
     if (lane == 0) sm[warp] = v;
@@ -194,8 +196,7 @@ __device__ __forceinline__ Node tree_combine_block_all(Node v, int P, Node* sm, 
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       if (d >= nw) break;
-      Node o = shfl_down_node(v, d);
-      if ((lane & (2 * d - 1)) == 0 && lane + d < nw) v = comb(v, o);
+      v = comb(v, shfl_down_node(v, d));
     }
   }
   return shfl_node(v, 0);
@@ -214,14 +215,32 @@ struct VarOut {
   int64_t mstride;   // mean_out[s * mstride]
 };
 
+// The slice length in the input type, its reciprocal (the reference
+// formula's means) and the factor n / (n - ddof): formed once per kernel,
+// outside the slice loops.
+template <typename T>
+struct Count {
+  T nf, inv, scale;
+  int ddof;
+};
+template <typename T>
+__device__ __forceinline__ Count<T> make_count(int64_t n, int ddof) {
+  Count<T> c;
+  c.nf = (T)n;
+  c.inv = div_rn((T)1, c.nf);
+  c.ddof = ddof;
+  c.scale = ddof != 0 ? div_rn(c.nf, (T)(n - ddof)) : (T)1;
+  return c;
+}
+
 template <typename T, int V>
-__device__ __forceinline__ void finish_slice(const N2<T>& tot, T kahan_s2, T x0, T mu, int64_t n, int ddof,
+__device__ __forceinline__ void finish_slice(const N2<T>& tot, T kahan_s2, T x0, T mu, const Count<T>& cnt,
                                              T* out, T* mean_out, int64_t s, VarOut io) {
   typedef Steps<V> St;
-  const T nf = (T)n;
+  const T nf = cnt.nf;
   T var, mean;
   if constexpr (St::REF) {
-    T inv = div_rn((T)1, nf);
+    T inv = cnt.inv;
     T md = mul_rn(tot.d, inv);
     T s2 = St::COMP == 1 ? add_rn(tot.q.s, tot.q.c) : tot.q.s;
     var = max_nan0(sub_rn(mul_rn(s2, inv), mul_rn(md, md)));
@@ -233,7 +252,7 @@ __device__ __forceinline__ void finish_slice(const N2<T>& tot, T kahan_s2, T x0,
     var = max_nan0(v);
     mean = add_rn(x0, mu);
   }
-  if (ddof != 0) var = mul_rn(var, div_rn(nf, (T)(n - ddof)));
+  if (cnt.ddof != 0) var = mul_rn(var, cnt.scale);
   out[s] = io.acc ? add_rn(out[s], var) : var;
   if (mean_out) mean_out[s * io.mstride] = mean;
 }
@@ -263,9 +282,8 @@ __device__ __forceinline__ T leaf_d(T xi, T x0, T mu) {
   else return sub_rn(xi, mu);
 }
 template <typename T, int V>
-__device__ __forceinline__ T mean_of(T sum1, int64_t n) {
-  const T nf = (T)n;
-  return Steps<V>::REF ? mul_rn(sum1, div_rn((T)1, nf)) : div_rn(sum1, nf);
+__device__ __forceinline__ T mean_of(T sum1, const Count<T>& cnt) {
+  return Steps<V>::REF ? mul_rn(sum1, cnt.inv) : div_rn(sum1, cnt.nf);
 }
 
 // Row kernel (axis 1): one block per row, thread t owns leaves [t C, t C + C).
@@ -280,6 +298,7 @@ __global__ void __launch_bounds__(1024) var_rows_kernel(const T* __restrict__ x,
   __shared__ bool smv[32];
   __shared__ T bc[2];
   const int64_t n = cols;
+  const Count<T> cnt = make_count<T>(n, ddof);
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
     const T* row = x + r * cols * es;
     const T x0 = row[0];
@@ -295,7 +314,7 @@ __global__ void __launch_bounds__(1024) var_rows_kernel(const T* __restrict__ x,
       T v1 = (T)0;
       bool h1 = st1.root(v1, f_combine<T>);
       T sum1 = tree_combine_block<T>(v1, h1, blockDim.x, smf, smv, f_combine<T>);
-      if (threadIdx.x == 0) bc[0] = mean_of<T, V>(sum1, n);
+      if (threadIdx.x == 0) bc[0] = mean_of<T, V>(sum1, cnt);
       __syncthreads();
       mu = bc[0];
     }
@@ -311,7 +330,7 @@ __global__ void __launch_bounds__(1024) var_rows_kernel(const T* __restrict__ x,
     N2<T> tot = tree_combine_block<N2<T>>(v2, h2, blockDim.x, sm2, smv, n2_combine<T>);
     if (threadIdx.x == 0) {
       T ks = St::COMP == 2 ? kahan_sq<T>(row, n, es, x0, mu) : (T)0;
-      finish_slice<T, V>(tot, ks, x0, mu, n, ddof, out, mean_out, r, io);
+      finish_slice<T, V>(tot, ks, x0, mu, cnt, out, mean_out, r, io);
     }
     __syncthreads();
   }
@@ -331,6 +350,7 @@ __global__ void __launch_bounds__(256) var_cols_kernel(const T* __restrict__ x, 
   __shared__ T bc[32];
   const int G = blockDim.y;
   const int64_t n = rows;
+  const Count<T> cnt = make_count<T>(n, ddof);
   const int64_t c = (int64_t)blockIdx.x * 32 + threadIdx.x;
   const bool col_ok = c < cols;
   const int g = threadIdx.y;
@@ -359,7 +379,7 @@ __global__ void __launch_bounds__(256) var_cols_kernel(const T* __restrict__ x, 
             smv[w][threadIdx.x] = true;
           }
         }
-      bc[threadIdx.x] = mean_of<T, V>(smf[0][threadIdx.x], n);
+      bc[threadIdx.x] = mean_of<T, V>(smf[0][threadIdx.x], cnt);
     }
     __syncthreads();
     mu = bc[threadIdx.x];
@@ -386,7 +406,7 @@ __global__ void __launch_bounds__(256) var_cols_kernel(const T* __restrict__ x, 
         }
       }
     T ks = St::COMP == 2 ? kahan_sq<T>(x + c * es, n, cols * es, x0, mu) : (T)0;
-    finish_slice<T, V>(sm2[0][threadIdx.x], ks, x0, mu, n, ddof, out, mean_out, c, io);
+    finish_slice<T, V>(sm2[0][threadIdx.x], ks, x0, mu, cnt, out, mean_out, c, io);
   }
 }
 
@@ -446,6 +466,7 @@ __global__ void __launch_bounds__(256) var_rows_reg(const T* __restrict__ x, int
   __shared__ bool smv[32];
   __shared__ T bc[1];
   const int n = (int)cols;
+  const Count<T> cnt = make_count<T>(n, ddof);
   const int b = threadIdx.x * C;
   int m = n - b;
   m = m < 0 ? 0 : (m > C ? C : m);
@@ -471,11 +492,11 @@ __global__ void __launch_bounds__(256) var_rows_reg(const T* __restrict__ x, int
       if (all) {
         // every thread gets the root and computes the same mean
         reg_tree_full<T, C>(t1, f_combine<T>);
-        mu = mean_of<T, V>(tree_combine_block_all<T>(t1[0], blockDim.x, smf, f_combine<T>), n);
+        mu = mean_of<T, V>(tree_combine_block_all<T>(t1[0], blockDim.x, smf, f_combine<T>), cnt);
       } else {
         bool h1 = reg_tree<T, C>(t1, m, f_combine<T>);
         T sum1 = tree_combine_block<T>(t1[0], h1, blockDim.x, smf, smv, f_combine<T>);
-        if (threadIdx.x == 0) bc[0] = mean_of<T, V>(sum1, n);
+        if (threadIdx.x == 0) bc[0] = mean_of<T, V>(sum1, cnt);
         __syncthreads();
         mu = bc[0];
       }
@@ -499,7 +520,7 @@ __global__ void __launch_bounds__(256) var_rows_reg(const T* __restrict__ x, int
     }
     if (threadIdx.x == 0) {
       T ks = St::COMP == 2 ? kahan_sq<T>(row, n, es, x0, mu) : (T)0;
-      finish_slice<T, V>(tot, ks, x0, mu, n, ddof, out, mean_out, r, io);
+      finish_slice<T, V>(tot, ks, x0, mu, cnt, out, mean_out, r, io);
     }
     if (!all) __syncthreads();
   }
