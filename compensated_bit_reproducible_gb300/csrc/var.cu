@@ -215,22 +215,17 @@ struct VarOut {
   int64_t mstride;   // mean_out[s * mstride]
 };
 
-// The slice length in the input type, its reciprocal (the reference
-// formula's means) and the factor n / (n - ddof): formed once per kernel,
-// outside the slice loops.
+// The slice length n and n - ddof converted to the input type once per
+// kernel, outside the slice loops (the divisions stay with the thread that
+// needs them: in double they run on the slow FP64 pipe).
 template <typename T>
 struct Count {
-  T nf, inv, scale;
+  T nf, nd;
   int ddof;
 };
 template <typename T>
 __device__ __forceinline__ Count<T> make_count(int64_t n, int ddof) {
-  Count<T> c;
-  c.nf = (T)n;
-  c.inv = div_rn((T)1, c.nf);
-  c.ddof = ddof;
-  c.scale = ddof != 0 ? div_rn(c.nf, (T)(n - ddof)) : (T)1;
-  return c;
+  return Count<T>{(T)n, (T)(n - ddof), ddof};
 }
 
 template <typename T, int V>
@@ -240,7 +235,7 @@ __device__ __forceinline__ void finish_slice(const N2<T>& tot, T kahan_s2, T x0,
   const T nf = cnt.nf;
   T var, mean;
   if constexpr (St::REF) {
-    T inv = cnt.inv;
+    T inv = div_rn((T)1, nf);
     T md = mul_rn(tot.d, inv);
     T s2 = St::COMP == 1 ? add_rn(tot.q.s, tot.q.c) : tot.q.s;
     var = max_nan0(sub_rn(mul_rn(s2, inv), mul_rn(md, md)));
@@ -252,7 +247,7 @@ __device__ __forceinline__ void finish_slice(const N2<T>& tot, T kahan_s2, T x0,
     var = max_nan0(v);
     mean = add_rn(x0, mu);
   }
-  if (cnt.ddof != 0) var = mul_rn(var, cnt.scale);
+  if (cnt.ddof != 0) var = mul_rn(var, div_rn(nf, cnt.nd));
   out[s] = io.acc ? add_rn(out[s], var) : var;
   if (mean_out) mean_out[s * io.mstride] = mean;
 }
@@ -283,7 +278,7 @@ __device__ __forceinline__ T leaf_d(T xi, T x0, T mu) {
 }
 template <typename T, int V>
 __device__ __forceinline__ T mean_of(T sum1, const Count<T>& cnt) {
-  return Steps<V>::REF ? mul_rn(sum1, cnt.inv) : div_rn(sum1, cnt.nf);
+  return Steps<V>::REF ? mul_rn(sum1, div_rn((T)1, cnt.nf)) : div_rn(sum1, cnt.nf);
 }
 
 // Row kernel (axis 1): one block per row, thread t owns leaves [t C, t C + C).
@@ -455,8 +450,10 @@ template <> struct Vec16<double> {
   }
 };
 
+// (the Kahan variant asks for five resident blocks per SM: its time is one
+// thread's sequential loop per row, so it scales with the blocks in flight)
 template <typename T, int C, int V>
-__global__ void __launch_bounds__(256) var_rows_reg(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t es,
+__global__ void __launch_bounds__(256, Steps<V>::COMP == 2 ? 5 : 1) var_rows_reg(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t es,
                                                     int ddof, T* __restrict__ out, T* __restrict__ mean_out,
                                                     VarOut io) {
   typedef Steps<V> St;
@@ -470,8 +467,13 @@ __global__ void __launch_bounds__(256) var_rows_reg(const T* __restrict__ x, int
   const int b = threadIdx.x * C;
   int m = n - b;
   m = m < 0 ? 0 : (m > C ? C : m);
-  // every thread of the block holds C leaves (the row fills the block)
-  const bool all = n >= (int)blockDim.x * C;
+  // every thread of the block holds C leaves (the row fills the block).
+  // Float only: in the full-row path every warp runs the cross-warp levels,
+  // which for double would put eight times the FP64 work of one thread on
+  // GB300's slow FP64 pipe.  The Kahan variant, whose time is one thread's
+  // sequential loop per row, keeps the general path and its lower register
+  // count (more blocks in flight).
+  const bool all = sizeof(T) == 4 && St::COMP != 2 && n >= (int)blockDim.x * C;
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
     const T* row = x + r * cols * es;
     const T x0 = __ldg(row);
@@ -490,8 +492,8 @@ __global__ void __launch_bounds__(256) var_rows_reg(const T* __restrict__ x, int
 #pragma unroll
       for (int i = 0; i < C; ++i) t1[i] = leaf1<T, V>(v[i], x0);
       if (all) {
-        // every thread gets the root and computes the same mean
         reg_tree_full<T, C>(t1, f_combine<T>);
+        // every thread has the root and forms the same mean
         mu = mean_of<T, V>(tree_combine_block_all<T>(t1[0], blockDim.x, smf, f_combine<T>), cnt);
       } else {
         bool h1 = reg_tree<T, C>(t1, m, f_combine<T>);
