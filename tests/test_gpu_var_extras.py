@@ -11,7 +11,8 @@ from tests.golden import load_kv
 from tests.gpu_util import dev, first_diff, same_bits, to_dev
 
 pytestmark = pytest.mark.gpu
-SHAPES = [(1, 1), (3, 5), (7, 33), (4, 257), (9, 1000), (2, 4096), (3, 4097), (2, 20000), (1000, 64), (33, 7)]
+SHAPES = [(1, 1), (3, 5), (7, 33), (5, 256), (4, 257), (9, 1000), (3, 1024), (2, 4096), (3, 4097), (2, 20000),
+          (1000, 64), (33, 7)]
 
 
 def gpu(x, axis, ddof, variant=0):
