@@ -353,6 +353,10 @@ def run_comparisons(api, torch, x32, x64, A, stream):
         torch.cuda.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
+        # a device-side wait of about 2 ms first, so that every call is
+        # queued before the first event: the timed region is device time
+        # only, even for calls shorter than their host-side launch
+        torch.cuda._sleep(4_000_000)
         a.record(stream)
         for _ in range(reps):
             fn()

@@ -25,8 +25,10 @@
 // run the same tree and read only its sums.
 //
 // Complex input (section 2, last paragraph) is the real and the imaginary
-// parts through the float32 kernel, read with an element stride of 2; the
-// second pass adds its variance to the first's.
+// parts through the float32 kernel: the variance is RN(var_re + var_im).
+// Rows of up to 4096 elements (axis 1) run both parts in one pass with pair
+// nodes; other shapes read each part with an element stride of 2, the
+// second pass adding its variance to the first's.
 #include <cuda_runtime.h>
 #include <cstdint>
 #include "launch.h"
@@ -228,12 +230,12 @@ __device__ __forceinline__ Count<T> make_count(int64_t n, int ddof) {
   return Count<T>{(T)n, (T)(n - ddof), ddof};
 }
 
+// Variance and mean of one slice from its pass-2 quantities.
 template <typename T, int V>
-__device__ __forceinline__ void finish_slice(const N2<T>& tot, T kahan_s2, T x0, T mu, const Count<T>& cnt,
-                                             T* out, T* mean_out, int64_t s, VarOut io) {
+__device__ __forceinline__ void slice_stats(const N2<T>& tot, T kahan_s2, T x0, T mu, const Count<T>& cnt, T& var,
+                                            T& mean) {
   typedef Steps<V> St;
   const T nf = cnt.nf;
-  T var, mean;
   if constexpr (St::REF) {
     T inv = div_rn((T)1, nf);
     T md = mul_rn(tot.d, inv);
@@ -248,6 +250,13 @@ __device__ __forceinline__ void finish_slice(const N2<T>& tot, T kahan_s2, T x0,
     mean = add_rn(x0, mu);
   }
   if (cnt.ddof != 0) var = mul_rn(var, div_rn(nf, cnt.nd));
+}
+
+template <typename T, int V>
+__device__ __forceinline__ void finish_slice(const N2<T>& tot, T kahan_s2, T x0, T mu, const Count<T>& cnt,
+                                             T* out, T* mean_out, int64_t s, VarOut io) {
+  T var, mean;
+  slice_stats<T, V>(tot, kahan_s2, x0, mu, cnt, var, mean);
   out[s] = io.acc ? add_rn(out[s], var) : var;
   if (mean_out) mean_out[s * io.mstride] = mean;
 }
@@ -591,9 +600,133 @@ cudaError_t launch_var_f64(const double* x, int64_t rows, int64_t cols, int axis
   return launch_var_v<double, 0>(x, rows, cols, axis, ddof, 1, out, mean, VarOut{0, 1}, s);
 }
 
+// ------------------------------------------------- complex rows in one pass
+// The real and the imaginary parts of a complex64 row run side by side:
+// every tree node is a pair combined componentwise, so each part's tree is
+// the adjacent-pair tree of the float kernel and gives its bits; the row's
+// variance is RN(var_re + var_im) and its mean (mean_re, mean_im), as in two
+// strided passes.  Thread t owns complex leaves [t C, t C + C) (C <= 8).
+template <typename T>
+struct Pair {
+  T re, im;
+};
+template <typename T> __device__ __forceinline__ Pair<T> shfl_down_node(Pair<T> v, int d) {
+  return Pair<T>{shfl_down_node(v.re, d), shfl_down_node(v.im, d)};
+}
+template <typename T> __device__ __forceinline__ Pair<T> shfl_node(Pair<T> v, int src) {
+  return Pair<T>{shfl_node(v.re, src), shfl_node(v.im, src)};
+}
+__device__ __forceinline__ Pair<float> pf_combine(Pair<float> l, Pair<float> r) {
+  return Pair<float>{add_rn(l.re, r.re), add_rn(l.im, r.im)};
+}
+__device__ __forceinline__ Pair<N2<float>> pn2_combine(Pair<N2<float>> l, Pair<N2<float>> r) {
+  return Pair<N2<float>>{n2_combine(l.re, r.re), n2_combine(l.im, r.im)};
+}
+
+template <int C>
+__global__ void __launch_bounds__(512) var_rows_c64(const float* __restrict__ z, int64_t rows, int64_t cols,
+                                                    int ddof, float* __restrict__ out,
+                                                    float* __restrict__ mean_out) {
+  typedef Pair<float> P;
+  typedef Pair<N2<float>> Q;
+  __shared__ P smf[32];
+  __shared__ Q sm2[32];
+  __shared__ bool smv[32];
+  __shared__ P bc[1];
+  const int n = (int)cols;
+  const Count<float> cnt = make_count<float>(n, ddof);
+  const int b = threadIdx.x * C;
+  int m = n - b;
+  m = m < 0 ? 0 : (m > C ? C : m);
+  const bool all = n >= (int)blockDim.x * C;   // every thread holds C leaves
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const float* row = z + 2 * r * cols;
+    const float re0 = __ldg(row), im0 = __ldg(row + 1);
+    float vr[C], vi[C];
+    if (C % 2 == 0 && m == C && ((((uintptr_t)(row + 2 * b)) & 15) == 0)) {
+#pragma unroll
+      for (int u = 0; u < C / 2; ++u) {
+        const float4 q = __ldcs((const float4*)(row + 2 * b) + u);
+        vr[2 * u] = q.x;
+        vi[2 * u] = q.y;
+        vr[2 * u + 1] = q.z;
+        vi[2 * u + 1] = q.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < C; ++i) {
+        vr[i] = (i < m) ? row[2 * (b + i)] : 0.f;
+        vi[i] = (i < m) ? row[2 * (b + i) + 1] : 0.f;
+      }
+    }
+    P mu;
+    {
+      // pass 1
+      P t1[C];
+#pragma unroll
+      for (int i = 0; i < C; ++i) t1[i] = P{leaf1<float, 0>(vr[i], re0), leaf1<float, 0>(vi[i], im0)};
+      if (all) {
+        reg_tree_full<P, C>(t1, pf_combine);
+        const P s1 = tree_combine_block_all<P>(t1[0], blockDim.x, smf, pf_combine);
+        mu = P{mean_of<float, 0>(s1.re, cnt), mean_of<float, 0>(s1.im, cnt)};
+      } else {
+        bool h1 = reg_tree<P, C>(t1, m, pf_combine);
+        const P s1 = tree_combine_block<P>(t1[0], h1, blockDim.x, smf, smv, pf_combine);
+        if (threadIdx.x == 0) bc[0] = P{mean_of<float, 0>(s1.re, cnt), mean_of<float, 0>(s1.im, cnt)};
+        __syncthreads();
+        mu = bc[0];
+      }
+    }
+    // pass 2
+    Q t2[C];
+#pragma unroll
+    for (int i = 0; i < C; ++i) {
+      const float dr = leaf_d<float, 0>(vr[i], re0, mu.re), di = leaf_d<float, 0>(vi[i], im0, mu.im);
+      t2[i] = Q{N2<float>{TS<float>{mul_rn(dr, dr), 0.f}, dr}, N2<float>{TS<float>{mul_rn(di, di), 0.f}, di}};
+    }
+    Q tot;
+    if (all) {
+      // smf and sm2 alternate: each is rewritten only after the other
+      // pass's barrier
+      reg_tree_full<Q, C>(t2, pn2_combine);
+      tot = tree_combine_block_all<Q>(t2[0], blockDim.x, sm2, pn2_combine);
+    } else {
+      bool h2 = reg_tree<Q, C>(t2, m, pn2_combine);
+      tot = tree_combine_block<Q>(t2[0], h2, blockDim.x, sm2, smv, pn2_combine);
+    }
+    if (threadIdx.x == 0) {
+      float var_re, mean_re, var_im, mean_im;
+      slice_stats<float, 0>(tot.re, 0.f, re0, mu.re, cnt, var_re, mean_re);
+      slice_stats<float, 0>(tot.im, 0.f, im0, mu.im, cnt, var_im, mean_im);
+      out[r] = add_rn(var_re, var_im);
+      if (mean_out) {
+        mean_out[2 * r] = mean_re;
+        mean_out[2 * r + 1] = mean_im;
+      }
+    }
+    if (!all) __syncthreads();
+  }
+}
+
 cudaError_t launch_var_c64(const float* z, int64_t rows, int64_t cols, int axis, int ddof, float* out,
                            float* mean, cudaStream_t s) {
-  // real parts (mean to the even floats), then imaginary parts added on
+  if (axis == 1 && cols <= 4096) {
+    // one pass: 256 threads and C = 1..8 leaves each, or 512 threads at C = 8
+    const int64_t np = pow2_ceil(cols);
+    const int block = np <= 2048 ? 256 : 512;
+    int64_t C = np / block;
+    if (C < 1) C = 1;
+    const unsigned grid = (unsigned)(rows < 65535 * 16 ? rows : 65535 * 16);
+    switch (C) {
+      case 1: var_rows_c64<1><<<grid, block, 0, s>>>(z, rows, cols, ddof, out, mean); break;
+      case 2: var_rows_c64<2><<<grid, block, 0, s>>>(z, rows, cols, ddof, out, mean); break;
+      case 4: var_rows_c64<4><<<grid, block, 0, s>>>(z, rows, cols, ddof, out, mean); break;
+      default: var_rows_c64<8><<<grid, block, 0, s>>>(z, rows, cols, ddof, out, mean); break;
+    }
+    return cudaGetLastError();
+  }
+  // two strided passes: real parts (mean to the even floats), then
+  // imaginary parts added on
   cudaError_t e = launch_var_v<float, 0>(z, rows, cols, axis, ddof, 2, out, mean, VarOut{0, 2}, s);
   if (e != cudaSuccess) return e;
   return launch_var_v<float, 0>(z + 1, rows, cols, axis, ddof, 2, out, mean ? mean + 1 : nullptr, VarOut{1, 2}, s);

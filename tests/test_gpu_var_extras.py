@@ -91,6 +91,21 @@ def test_complex_bit_exact(rows, cols):
             assert m.dtype == np.complex64 and same_bits(m, wm)
 
 
+@pytest.mark.parametrize("rows,cols", [(1500, 2048), (600, 4096), (900, 3000)])
+def test_complex_rows_one_pass_many_rows(rows, cols):
+    """Rows of up to 4096 elements take both parts in one pass (pair
+    nodes; 512 threads at 4096): more rows than resident blocks, full and
+    ragged rows, a heavy-tailed imaginary part."""
+    dev()
+    rng = np.random.default_rng(rows + cols)
+    z = (rng.standard_normal((rows, cols)) + 5e4
+         + 1j * (1e-3 * rng.standard_t(3, (rows, cols)))).astype(np.complex64)
+    v, m = gpu(z, 1, 1)
+    wv, wm = oracle.var_kernel_c64_2d(z, 1, 1)
+    assert same_bits(v, wv), first_diff(v, wv)
+    assert same_bits(m, wm)
+
+
 def test_complex_page_values():
     dev()
     g = load_kv("variance_complex.txt")
