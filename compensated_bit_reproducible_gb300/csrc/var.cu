@@ -443,6 +443,106 @@ __device__ __forceinline__ void reg_tree_full(Node* a, F comb) {
   }
 }
 
+// Two float lanes in one 64-bit register (x low word, y high word).
+// add/sub.rn.f32x2 are two independent IEEE round-to-nearest operations in
+// one instruction (subnormals kept): the bits of two scalar operations.
+// Products stay scalar: a packed multiply feeding a packed add was measured
+// to be contracted into a fused multiply-add on this GPU (about 20% of
+// random operand pairs differed), even with FMA contraction disabled, while
+// scalar products packed into a packed add kept both roundings.
+typedef unsigned long long F2;
+__device__ __forceinline__ F2 pk2(float x, float y) {
+  F2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+  return r;
+}
+__device__ __forceinline__ void up2(F2 v, float& x, float& y) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
+}
+__device__ __forceinline__ F2 add2(F2 a, F2 b) {
+  F2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ F2 sub2(F2 a, F2 b) {
+  F2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ F2 f2_combine(F2 l, F2 r) { return add2(l, r); }
+
+// Two pass-2 nodes side by side: the operations of ts_combine and
+// n2_combine, in the same order, on both lanes.
+struct N2x {
+  F2 s, c, d;
+};
+__device__ __forceinline__ N2x n2x_combine(N2x l, N2x r) {
+  const F2 s = add2(l.s, r.s);
+  const F2 bb = sub2(s, l.s);
+  const F2 e = add2(sub2(l.s, sub2(s, bb)), sub2(r.s, bb));
+  return N2x{s, add2(add2(l.c, r.c), e), add2(l.d, r.d)};
+}
+
+// A thread's full subtree of C float leaves as two half-subtrees in
+// lockstep: leaves [0, C/2) in lane x, [C/2, C) in lane y, then one scalar
+// combine of the two roots (x left, y right).  That is the adjacent-pair
+// tree of the C leaves, with half the floating-point instructions.
+template <int V, int C>
+__device__ __forceinline__ float root1_packed(const float* v, float x0) {
+  constexpr int H = C / 2;
+  F2 a[H];
+  const F2 X0 = pk2(x0, x0);
+#pragma unroll
+  for (int j = 0; j < H; ++j) {
+    const F2 p = pk2(v[j], v[j + H]);
+    a[j] = Steps<V>::SHIFT ? sub2(p, X0) : p;
+  }
+  reg_tree_full<F2, H>(a, f2_combine);
+  float x, y;
+  up2(a[0], x, y);
+  return add_rn(x, y);
+}
+template <int V, int C>
+__device__ __forceinline__ N2<float> root2_packed(const float* v, float x0, float mu) {
+  constexpr int H = C / 2;
+  N2x a[H];
+  const F2 X0 = pk2(x0, x0), MU = pk2(mu, mu);
+#pragma unroll
+  for (int j = 0; j < H; ++j) {
+    const F2 p = pk2(v[j], v[j + H]);
+    const F2 d = Steps<V>::SHIFT ? sub2(sub2(p, X0), MU) : sub2(p, MU);
+    float dx, dy;
+    up2(d, dx, dy);
+    a[j] = N2x{pk2(mul_rn(dx, dx), mul_rn(dy, dy)), 0ull, d};
+  }
+  reg_tree_full<N2x, H>(a, n2x_combine);
+  float sx, sy, cx, cy, dx, dy;
+  up2(a[0].s, sx, sy);
+  up2(a[0].c, cx, cy);
+  up2(a[0].d, dx, dy);
+  return n2_combine(N2<float>{TS<float>{sx, cx}, dx}, N2<float>{TS<float>{sy, cy}, dy});
+}
+
+// Root of a thread's full subtree in pass 1 / pass 2 (t1, t2: its leaves).
+template <typename T, int V, int C>
+__device__ __forceinline__ T full_root1(const T* v, T* t1, T x0) {
+  if constexpr (sizeof(T) == 4 && C >= 2) {
+    return root1_packed<V, C>(v, x0);
+  } else {
+    reg_tree_full<T, C>(t1, f_combine<T>);
+    return t1[0];
+  }
+}
+template <typename T, int V, int C>
+__device__ __forceinline__ N2<T> full_root2(const T* v, N2<T>* t2, T x0, T mu) {
+  if constexpr (sizeof(T) == 4 && C >= 2) {
+    return root2_packed<V, C>(v, x0, mu);
+  } else {
+    reg_tree_full<N2<T>, C>(t2, n2_combine<T>);
+    return t2[0];
+  }
+}
+
 template <typename T> struct Vec16;
 template <> struct Vec16<float> {
   typedef float4 type;
@@ -462,7 +562,7 @@ template <> struct Vec16<double> {
 // (the Kahan variant asks for five resident blocks per SM: its time is one
 // thread's sequential loop per row, so it scales with the blocks in flight)
 template <typename T, int C, int V>
-__global__ void __launch_bounds__(256, Steps<V>::COMP == 2 ? 5 : 1) var_rows_reg(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t es,
+__global__ void __launch_bounds__(256, sizeof(T) == 4 ? 5 : 3) var_rows_reg(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t es,
                                                     int ddof, T* __restrict__ out, T* __restrict__ mean_out,
                                                     VarOut io) {
   typedef Steps<V> St;
@@ -501,9 +601,9 @@ __global__ void __launch_bounds__(256, Steps<V>::COMP == 2 ? 5 : 1) var_rows_reg
 #pragma unroll
       for (int i = 0; i < C; ++i) t1[i] = leaf1<T, V>(v[i], x0);
       if (all) {
-        reg_tree_full<T, C>(t1, f_combine<T>);
         // every thread has the root and forms the same mean
-        mu = mean_of<T, V>(tree_combine_block_all<T>(t1[0], blockDim.x, smf, f_combine<T>), cnt);
+        const T r1 = full_root1<T, V, C>(v, t1, x0);
+        mu = mean_of<T, V>(tree_combine_block_all<T>(r1, blockDim.x, smf, f_combine<T>), cnt);
       } else {
         bool h1 = reg_tree<T, C>(t1, m, f_combine<T>);
         T sum1 = tree_combine_block<T>(t1[0], h1, blockDim.x, smf, smv, f_combine<T>);
@@ -523,8 +623,8 @@ __global__ void __launch_bounds__(256, Steps<V>::COMP == 2 ? 5 : 1) var_rows_reg
     if (all) {
       // one barrier per pass: smf and sm2 alternate, so each is rewritten
       // only after the other pass's barrier
-      reg_tree_full<N2<T>, C>(t2, n2_combine<T>);
-      tot = tree_combine_block_all<N2<T>>(t2[0], blockDim.x, sm2, n2_combine<T>);
+      const N2<T> r2 = full_root2<T, V, C>(v, t2, x0, mu);
+      tot = tree_combine_block_all<N2<T>>(r2, blockDim.x, sm2, n2_combine<T>);
     } else {
       bool h2 = reg_tree<N2<T>, C>(t2, m, n2_combine<T>);
       tot = tree_combine_block<N2<T>>(t2[0], h2, blockDim.x, sm2, smv, n2_combine<T>);
