@@ -385,6 +385,10 @@ def run_comparisons(api, torch, x32, x64, A, stream):
         ("cumsum_f64_k6_1e8", lambda: api.repro_cumsum(x64, out=c64k6, K=6), N_SUM),
         ("state_8_chunks_f32_1e8", lambda: chunked(x32, st32, r32), N_SUM),
         ("state_8_chunks_f64_1e8", lambda: chunked(x64, st64, r64), N_SUM),
+        # the hot-path calls again, timed the same way as the others here
+        ("adn_sum_f32_1e8", lambda: api.repro_sum_async(x32, r32, 3), N_SUM),
+        ("adn_sum_f64_1e8", lambda: api.repro_sum_async(x64, r64, 3), N_SUM),
+        ("stable_var_f32_4096x4096", lambda: api.stable_var(A, axis=1, ddof=1, with_mean=False), ROWS * COLS),
         ("naive_sum_f32_1e8", lambda: api.compare_sum(x32, "naive"), N_SUM),
         ("pairwise_sum_f32_1e8", lambda: api.compare_sum(x32, "pairwise"), N_SUM),
         ("torch_sum_f32_1e8", lambda: torch.sum(x32), N_SUM),
