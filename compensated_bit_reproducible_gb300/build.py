@@ -19,7 +19,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librepro_gb300.so")
 SOURCES = ["api.cu", "adn_sum.cu", "sum_f64_fixed.cu", "adn_cumsum.cu", "cumsum_k3.cu", "var.cu", "compare.cu",
            "noalloc.cu"]
-HEADERS = ["adn.cuh", "accum.cuh", "launch.h"]
+HEADERS = ["adn.cuh", "accum.cuh", "fixed_index.cuh", "f32x2.cuh", "launch.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-fmad=false", "-prec-div=true",

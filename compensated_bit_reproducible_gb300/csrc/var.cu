@@ -31,6 +31,7 @@
 // second pass adding its variance to the first's.
 #include <cuda_runtime.h>
 #include <cstdint>
+#include "f32x2.cuh"
 #include "launch.h"
 
 namespace repro {
@@ -443,32 +444,6 @@ __device__ __forceinline__ void reg_tree_full(Node* a, F comb) {
   }
 }
 
-// Two float lanes in one 64-bit register (x low word, y high word).
-// add/sub.rn.f32x2 are two independent IEEE round-to-nearest operations in
-// one instruction (subnormals kept): the bits of two scalar operations.
-// Products stay scalar: a packed multiply feeding a packed add was measured
-// to be contracted into a fused multiply-add on this GPU (about 20% of
-// random operand pairs differed), even with FMA contraction disabled, while
-// scalar products packed into a packed add kept both roundings.
-typedef unsigned long long F2;
-__device__ __forceinline__ F2 pk2(float x, float y) {
-  F2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
-  return r;
-}
-__device__ __forceinline__ void up2(F2 v, float& x, float& y) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(x), "=f"(y) : "l"(v));
-}
-__device__ __forceinline__ F2 add2(F2 a, F2 b) {
-  F2 r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ F2 sub2(F2 a, F2 b) {
-  F2 r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
 __device__ __forceinline__ F2 f2_combine(F2 l, F2 r) { return add2(l, r); }
 
 // Two pass-2 nodes side by side: the operations of ts_combine and
