@@ -534,12 +534,14 @@ template <> struct Vec16<double> {
   }
 };
 
-// (the Kahan variant asks for five resident blocks per SM: its time is one
-// thread's sequential loop per row, so it scales with the blocks in flight)
+// Resident blocks asked for: five per SM for float (47 registers; the Kahan
+// variant's time is one thread's loop per row, so it scales with the blocks
+// in flight), three for double (72 registers, no spills).  Without an
+// explicit count the compiler gave some instances 79 or 110 registers.
 template <typename T, int C, int V>
-__global__ void __launch_bounds__(256, sizeof(T) == 4 ? 5 : 3) var_rows_reg(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t es,
-                                                    int ddof, T* __restrict__ out, T* __restrict__ mean_out,
-                                                    VarOut io) {
+__global__ void __launch_bounds__(256, sizeof(T) == 4 ? 5 : 3)
+    var_rows_reg(const T* __restrict__ x, int64_t rows, int64_t cols, int64_t es, int ddof, T* __restrict__ out,
+                 T* __restrict__ mean_out, VarOut io) {
   typedef Steps<V> St;
   typedef Vec16<T> VT;
   __shared__ T smf[32];
