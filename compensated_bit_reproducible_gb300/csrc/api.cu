@@ -219,15 +219,18 @@ repro_status sum_async_impl(const T* x, size_t n, int K, cudaStream_t stream, T*
   int grid = sum_grid((int64_t)n, block, 4 * (int)(16 / sizeof(T)), sum_blocks_per_sm<T>(K, block),
                       l);   // 4 vectors per thread per iteration, one wave of blocks
   size_t wsb = sum_workspace_bytes(K, grid);
-  // double with K = 2 or 3: the sampled fixed-index kernel runs first and the
+  // double with K = 2..6: the sampled fixed-index kernel runs first and the
   // general kernel only if that one flags its guess (workspace header bytes
   // [64, 76) are its control words)
   int fgrid = 0, fblock = 0;
   size_t foff = 0;
   if constexpr (sizeof(T) == 8) {
-    if ((K == 2 || K == 3) && n >= FIXED_MIN_N && (uint64_t)n <= FIXED_MAX_N) {
+    if (K >= 2 && K <= 6 && n >= FIXED_MIN_N && (uint64_t)n <= FIXED_MAX_N) {
       fblock = (l && l->block) ? l->block : 128;
-      fgrid = (l && l->grid > 0) ? l->grid : sum_f64_fixed_grid(K, fblock, sm_count());
+      // zero when the cells do not fit this block size (K = 6 at 1024
+      // threads): the general kernel alone runs
+      const int fcap = sum_f64_fixed_grid(K, fblock, sm_count());
+      fgrid = fcap <= 0 ? 0 : ((l && l->grid > 0) ? l->grid : fcap);
       if (fgrid > 0) {
         foff = (wsb + 255) & ~(size_t)255;
         wsb = foff + sum_f64_fixed_workspace_bytes(fgrid);

@@ -30,8 +30,19 @@ namespace repro {
 namespace fx {
 
 constexpr int SAMPLE = 256;   // elements sampled for the index guess
-constexpr int STRIDE = 7;     // sum cells per sign: 32-bit word positions 0..6 of P''
-constexpr int CELLS = 14;     // both signs
+// Sum cells per sign, one per 32-bit word position of P'', for K folds.  A
+// valid element (inside the guessed bin) has shift u <= 50 + W (K - 1) over
+// g_f, so its three words end at position (u >> 5) + 2.  K <= 3 keeps 7
+// positions (0..6); K = 6 needs 10.
+template <int K>
+struct FxGeo {
+  static constexpr int UMAX = 50 + 40 * (K - 1);
+  static constexpr int STR = K <= 3 ? 7 : (UMAX >> 5) + 3;
+  static constexpr int NPOS = STR - 2;   // kept positions 2..STR-1
+  static constexpr int CELLS = 2 * STR;  // both signs
+};
+constexpr int STRIDE = FxGeo<3>::STR;
+constexpr int CELLS = FxGeo<3>::CELLS;
 
 __device__ __forceinline__ uint32_t shl_clamp32(uint32_t v, int s) {   // s outside [0, 31] gives 0
   uint32_t r;
@@ -63,13 +74,14 @@ struct FxConst {
 
 // One deposit.  A: 64-bit cells (stride NT), B: 32-bit cells; sign s word k
 // at cell k + 7 s (B: k - 2 + 7 s, only k >= 2 is used).
+template <int STR = STRIDE>
 __device__ __forceinline__ void fx_deposit(uint32_t hi, uint32_t lo, const FxConst& k, uint64_t* A, uint32_t* B,
                                            uint32_t NT, int& umax) {
   uint32_t eb = mad32(hi, k.one + k.one, 0u) >> 21;          // biased exponent
   int us = (int)mad32(eb, k.one, k.Cp);                       // shift of M
   umax = max(umax, us);
   uint32_t u = (uint32_t)max(us, 0);   // tiny values: their words stay below position 2
-  uint32_t c = min(u >> 5, 5u);        // beyond the bin (flagged through umax): kept in bounds
+  uint32_t c = min(u >> 5, (uint32_t)(STR - 2));   // beyond the bin (flagged through umax): kept in bounds
   uint32_t mh = (hi & 0xFFFFFu) | 0x100000u;
   uint32_t hl = shl_clamp32(1u, (int)mad32(u, k.negone, k.c63));
   uint32_t hh = shl_clamp32(1u, (int)mad32(u, k.negone, k.c31));
@@ -87,13 +99,14 @@ __device__ __forceinline__ void fx_deposit(uint32_t hi, uint32_t lo, const FxCon
   pb[0] = mad32(w2, k.one, pb[0]);
 }
 
+template <int STR = STRIDE>
 __device__ __forceinline__ void fx_fold(uint64_t* A, uint32_t* B, uint32_t NT) {
 #pragma unroll
   for (int s = 0; s < 2; ++s)
 #pragma unroll
-    for (int w = 2; w < STRIDE; ++w) {
-      A[(w + STRIDE * s) * NT] += B[(w - 2 + STRIDE * s) * NT];
-      B[(w - 2 + STRIDE * s) * NT] = 0;
+    for (int w = 2; w < STR; ++w) {
+      A[(w + STR * s) * NT] += B[(w - 2 + STR * s) * NT];
+      B[(w - 2 + STR * s) * NT] = 0;
     }
 }
 
@@ -129,39 +142,102 @@ __device__ __forceinline__ I192 i192_neg(I192 a) {
   return i192_add(r, I192{1, 0, 0});
 }
 
-// Block sum of the thread cells into a signed 192-bit total (units of g_f),
-// valid in thread 0.  `scratch` (32 x 10 W128) may alias the cells: they are
-// read into registers before it is written.
-__device__ __forceinline__ I192 fx_block_total(const uint64_t* A, uint32_t NT, W128 (*red)[10]) {
+// Signed 320-bit integer: block totals for K = 4..6 (|total| < 2^280 in
+// units of g_f: an element's rounded value is below 2^(UMAX - 10) <= 2^240,
+// at most 2^36 elements).
+struct I320 {
+  uint64_t w[5];
+};
+__device__ __forceinline__ I320 i320_add(I320 a, I320 b) {
+  I320 r;
+  asm("add.cc.u64 %0, %5, %10;\n\taddc.cc.u64 %1, %6, %11;\n\taddc.cc.u64 %2, %7, %12;\n\t"
+      "addc.cc.u64 %3, %8, %13;\n\taddc.u64 %4, %9, %14;"
+      : "=l"(r.w[0]), "=l"(r.w[1]), "=l"(r.w[2]), "=l"(r.w[3]), "=l"(r.w[4])
+      : "l"(a.w[0]), "l"(a.w[1]), "l"(a.w[2]), "l"(a.w[3]), "l"(a.w[4]), "l"(b.w[0]), "l"(b.w[1]),
+        "l"(b.w[2]), "l"(b.w[3]), "l"(b.w[4]));
+  return r;
+}
+__device__ __forceinline__ I320 i320_shfl_xor(I320 v, int m) {
+  I320 r;
+#pragma unroll
+  for (int i = 0; i < 5; ++i) r.w[i] = __shfl_xor_sync(0xffffffffu, v.w[i], m);
+  return r;
+}
+// v * 2^(32 j) for a W128 v >= 0 below 2^96 (a column sum), as I320
+__device__ __forceinline__ I320 i320_from_shifted(W128 v, int j) {
+  uint32_t src[4] = {(uint32_t)v.lo, (uint32_t)(v.lo >> 32), (uint32_t)v.hi, (uint32_t)((uint64_t)v.hi >> 32)};
+  uint32_t d[10] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (i + j < 10) d[i + j] = src[i];
+  I320 r;
+#pragma unroll
+  for (int i = 0; i < 5; ++i) r.w[i] = ((uint64_t)d[2 * i + 1] << 32) | d[2 * i];
+  return r;
+}
+__device__ __forceinline__ I320 i320_neg(I320 a) {
+  I320 r;
+#pragma unroll
+  for (int i = 0; i < 5; ++i) r.w[i] = ~a.w[i];
+  return i320_add(r, I320{{1, 0, 0, 0, 0}});
+}
+
+// The same operations under one name for either width.
+__device__ __forceinline__ I192 tot_add(I192 a, I192 b) { return i192_add(a, b); }
+__device__ __forceinline__ I320 tot_add(I320 a, I320 b) { return i320_add(a, b); }
+__device__ __forceinline__ I192 tot_neg(I192 a) { return i192_neg(a); }
+__device__ __forceinline__ I320 tot_neg(I320 a) { return i320_neg(a); }
+__device__ __forceinline__ I192 tot_shfl_xor(I192 v, int m) { return i192_shfl_xor(v, m); }
+__device__ __forceinline__ I320 tot_shfl_xor(I320 v, int m) { return i320_shfl_xor(v, m); }
+__device__ __forceinline__ void tot_from_shifted(W128 v, int j, I192* r) { *r = i192_from_shifted(v, j); }
+__device__ __forceinline__ void tot_from_shifted(W128 v, int j, I320* r) { *r = i320_from_shifted(v, j); }
+__device__ __forceinline__ I192 tot_ldcg(const I192* q) { return I192{__ldcg(&q->w0), __ldcg(&q->w1), __ldcg(&q->w2)}; }
+__device__ __forceinline__ I320 tot_ldcg(const I320* q) {
+  I320 r;
+#pragma unroll
+  for (int i = 0; i < 5; ++i) r.w[i] = __ldcg(&q->w[i]);
+  return r;
+}
+
+// Block sum of the thread cells (STR positions per sign) into a signed total
+// TOT (units of g_f), valid in thread 0.  `red` (32 warps x 2 (STR - 2)
+// W128) may alias the cells: they are read into registers before it is
+// written.
+template <int STR, typename TOT>
+__device__ __forceinline__ TOT fx_block_total_t(const uint64_t* A, uint32_t NT, W128 (*red)[2 * (STR - 2)]) {
+  constexpr int NP = STR - 2, NC = 2 * NP;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (int)(NT >> 5);
-  W128 col[10];
+  W128 col[NC];
 #pragma unroll
   for (int s = 0; s < 2; ++s)
 #pragma unroll
-    for (int w = 2; w < STRIDE; ++w) col[s * 5 + (w - 2)] = W128{A[(w + STRIDE * s) * NT], 0};
+    for (int w = 2; w < STR; ++w) col[s * NP + (w - 2)] = W128{A[(w + STR * s) * NT], 0};
   __syncthreads();
 #pragma unroll
-  for (int i = 0; i < 10; ++i) {
+  for (int i = 0; i < NC; ++i) {
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) col[i] = w_add(col[i], shfl_xor_w(col[i], m));
   }
   if (lane == 0) {
 #pragma unroll
-    for (int i = 0; i < 10; ++i) red[warp][i] = col[i];
+    for (int i = 0; i < NC; ++i) red[warp][i] = col[i];
   }
   __syncthreads();
-  I192 t{0, 0, 0};
+  TOT t{};
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 10; ++i) {
+    for (int i = 0; i < NC; ++i) {
       W128 s = W128{0, 0};
       for (int w = 0; w < nw; ++w) s = w_add(s, red[w][i]);
-      I192 v = i192_from_shifted(s, i % 5);
-      t = i192_add(t, i < 5 ? v : i192_neg(v));
+      TOT v;
+      tot_from_shifted(s, i % NP, &v);
+      t = tot_add(t, i < NP ? v : tot_neg(v));
     }
   }
   return t;
 }
-
+__device__ __forceinline__ I192 fx_block_total(const uint64_t* A, uint32_t NT, W128 (*red)[10]) {
+  return fx_block_total_t<STRIDE, I192>(A, NT, red);
+}
 
 // Index guess from the largest exponent field over SAMPLE evenly spaced
 // elements (every block computes the same value).  Returns the bin index;
@@ -202,14 +278,14 @@ __device__ __forceinline__ int bin_top_exponent(int I) {
   return I == 0 ? (sizeof(T) == 8 ? 2046 : 254) : G::BIAS + beta<T>(I) + G::W - 2;
 }
 
-__device__ __forceinline__ FxConst make_const(int bf, uint32_t one) {
+__device__ __forceinline__ FxConst make_const(int bf, uint32_t one, int stride = STRIDE) {
   FxConst k;
   k.one = one;
   k.negone = 0u - one;
   k.c63 = 63u * one;
   k.c31 = 31u * one;
   k.c256 = 256u * one;
-  k.c7 = (uint32_t)STRIDE * one;
+  k.c7 = (uint32_t)stride * one;   // cells per sign
   k.Cp = (uint32_t)(-1011 - bf);
   return k;
 }

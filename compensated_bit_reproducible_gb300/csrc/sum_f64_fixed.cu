@@ -1,4 +1,4 @@
-// Double binned sum (K = 2, 3) at an index fixed before the deposit (see
+// Double binned sum (K = 2..6) at an index fixed before the deposit (see
 // fixed_index.cuh for the reading this rests on).  If any element lies
 // outside the guessed bin or is Inf/NaN, or the index is too fine for the
 // shortcuts, the kernel sets a flag and the general one-pass kernel
@@ -11,7 +11,9 @@
 // position (and sign) in shared memory, so a deposit is an add into three
 // cells and no variable-width shift of a wide accumulator.  The top word w2
 // is below 2^22 and goes to a 32-bit cell (1024 additions fit), folded into
-// the 64-bit cells every 992 deposits.
+// the 64-bit cells every 992 deposits.  K sets only how many positions
+// there are (7 for K <= 3, 10 for K = 6) and the width of the block total
+// (192 or 320 bits): an element's three words are the same for any K.
 #include "accum.cuh"
 #include "fixed_index.cuh"
 #include "launch.h"
@@ -39,17 +41,59 @@ struct FixedCtl {
 // CNT: the block size as a compile-time constant (128 or 256: registers
 // capped for 10 resp. 5 resident blocks per SM, cell offsets folded into the
 // addressing), or 0 for any block size up to 1024.
+// K >= 4: the larger cells fit seven 128-thread blocks per SM (three of 256).
 constexpr int fx_max_threads(int cnt) { return cnt ? cnt : 1024; }
-constexpr int fx_min_blocks(int cnt) { return cnt ? 1280 / (cnt ? cnt : 1) : 1; }
+constexpr int fx_min_blocks(int cnt, int K) { return cnt ? (K <= 3 ? 1280 : 896) / (cnt ? cnt : 1) : 1; }
+
+// Block totals: 192 bits for K <= 3, 320 bits for K = 4..6.
+template <int K> struct FxTot { typedef I320 type; };
+template <> struct FxTot<2> { typedef I192 type; };
+template <> struct FxTot<3> { typedef I192 type; };
+
+// Folds of a total for the conversion (any split with the right weighted sum
+// converts alike): 40-bit fields from the bottom, the rest (arithmetic) on top.
+template <int K>
+__device__ __forceinline__ void fx_folds(const I192& tot, W128* F) {
+  const uint64_t m40 = (1ull << 40) - 1;
+  F[K - 1] = W128{tot.w0 & m40, 0};
+  if (K == 3) {
+    F[1] = W128{((tot.w0 >> 40) | (tot.w1 << 24)) & m40, 0};
+    // tot >> 80 (arithmetic)
+    F[0] = W128{(tot.w1 >> 16) | (tot.w2 << 48), (int64_t)tot.w2 >> 16};
+  } else {
+    // tot >> 40 (arithmetic)
+    F[0] = W128{(tot.w0 >> 40) | (tot.w1 << 24), (int64_t)((tot.w1 >> 40) | (tot.w2 << 24))};
+  }
+}
+template <int K>
+__device__ __forceinline__ void fx_folds(const I320& tot, W128* F) {
+  const uint64_t m40 = (1ull << 40) - 1;
+#pragma unroll
+  for (int j = 0; j < K - 1; ++j) {
+    const int a = (40 * j) >> 6, b = (40 * j) & 63;
+    uint64_t v = tot.w[a] >> b;
+    if (b > 24) v |= tot.w[a + 1] << (64 - b);
+    F[K - 1 - j] = W128{v & m40, 0};
+  }
+  // tot >> 40 (K - 1), arithmetic; the shift is 120, 160 or 200 (b != 0)
+  constexpr int o = 40 * (K - 1), a = o >> 6, b = o & 63;
+  const uint64_t lo = (tot.w[a] >> b) | (tot.w[a + 1] << (64 - b));
+  uint64_t hi;
+  if constexpr (a + 2 <= 4) hi = (tot.w[a + 1] >> b) | (tot.w[a + 2] << (64 - b));
+  else hi = (uint64_t)((int64_t)tot.w[a + 1] >> b);
+  F[0] = W128{lo, (int64_t)hi};
+}
 
 template <int K, int CNT>
-__global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT))
+__global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
     sum_f64_fixed_kernel(const double* __restrict__ x, int64_t n, uint32_t one, FixedCtl* ctl,
                          unsigned char* __restrict__ parts, double* __restrict__ result) {
   extern __shared__ __align__(16) unsigned char fx_smem[];
   const uint32_t NT = CNT ? (uint32_t)CNT : blockDim.x;
   uint64_t* A = (uint64_t*)fx_smem + threadIdx.x;
-  uint32_t* B = (uint32_t*)(fx_smem + (size_t)CELLS * 8 * NT) + threadIdx.x;
+  typedef FxGeo<K> Geo;
+  typedef typename FxTot<K>::type Tot;
+  uint32_t* B = (uint32_t*)(fx_smem + (size_t)Geo::CELLS * 8 * NT) + threadIdx.x;
   __shared__ unsigned s_emax;
 
   // the gated fallback kernel may start launching now; it waits for this
@@ -62,13 +106,13 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT))
   // the shortcuts need g_f/2 above every subnormal and every x with a forced
   // hidden bit below the grid: beta_f >= -1019; Inf/NaN in the sample fail too
   const bool usable = (bf >= -1019) && (eb_max < 0x7FF);
-  const FxConst kc = make_const(bf, one);
+  const FxConst kc = make_const(bf, one, Geo::STR);
   // largest valid shift: the top of bin Ig
   const int u_thr = bin_top_exponent<double>(Ig) + (int)kc.Cp;
 
   // 2. Deposits: full chunks from a dynamic queue, then the ragged rest.
 #pragma unroll
-  for (int w = 0; w < CELLS; ++w) {
+  for (int w = 0; w < Geo::CELLS; ++w) {
     A[w * NT] = 0;
     B[w * NT] = 0;
   }
@@ -98,18 +142,20 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT))
       for (int q = 0; q < FX_U; ++q) v[q] = __ldcs(base + (int64_t)(j * FX_U + q) * NT);
 #pragma unroll
       for (int q = 0; q < FX_U; ++q) {
-        fx_deposit((uint32_t)__double2hiint(v[q].x), (uint32_t)__double2loint(v[q].x), kc, A, B, NT, umax);
-        fx_deposit((uint32_t)__double2hiint(v[q].y), (uint32_t)__double2loint(v[q].y), kc, A, B, NT, umax);
+        fx_deposit<Geo::STR>((uint32_t)__double2hiint(v[q].x), (uint32_t)__double2loint(v[q].x), kc, A, B, NT,
+                             umax);
+        fx_deposit<Geo::STR>((uint32_t)__double2hiint(v[q].y), (uint32_t)__double2loint(v[q].y), kc, A, B, NT,
+                             umax);
       }
     }
     if (++since == FX_FOLD_CHUNKS) {
-      fx_fold(A, B, NT);
+      fx_fold<Geo::STR>(A, B, NT);
       since = 0;
     }
     if (threadIdx.x == 0) s_q[slot ^ 1] = nxt;
     __syncthreads();
   }
-  fx_fold(A, B, NT);
+  fx_fold<Geo::STR>(A, B, NT);
   if (usable) {
     // head element(s) and everything after the last full chunk
     const int64_t tail0 = head + 2 * nchunks * CV;
@@ -118,21 +164,21 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT))
     int cnt = 0;
     for (int64_t r = gt; r < R; r += G_) {
       double v = __ldg(x + (r < head ? r : tail0 + (r - head)));
-      fx_deposit((uint32_t)__double2hiint(v), (uint32_t)__double2loint(v), kc, A, B, NT, umax);
+      fx_deposit<Geo::STR>((uint32_t)__double2hiint(v), (uint32_t)__double2loint(v), kc, A, B, NT, umax);
       if (++cnt == 992) {
-        fx_fold(A, B, NT);
+        fx_fold<Geo::STR>(A, B, NT);
         cnt = 0;
       }
     }
-    fx_fold(A, B, NT);
+    fx_fold<Geo::STR>(A, B, NT);
   }
   const int fail = __syncthreads_or(!usable || umax > u_thr);
 
   // 3. Block total, partial, and the last block's merge and conversion.
-  I192 t = fx_block_total(A, NT, (W128(*)[10])fx_smem);
+  Tot t = fx_block_total_t<Geo::STR, Tot>(A, NT, (W128(*)[2 * Geo::NPOS])fx_smem);
   __shared__ bool last;
   if (threadIdx.x == 0) {
-    I192* pp = (I192*)parts + blockIdx.x;
+    Tot* pp = (Tot*)parts + blockIdx.x;
     *pp = t;
     if (fail) atomicOr(&ctl->fail, 1u);
     __threadfence();
@@ -143,41 +189,31 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT))
   if (!last) return;
   __threadfence();
   if (__ldcg(&ctl->fail)) return;   // the general pass writes the result
-  I192 s{0, 0, 0};
-  for (int p = threadIdx.x; p < (int)gridDim.x; p += NT) {
-    const I192* q = (const I192*)parts + p;
-    s = i192_add(s, I192{__ldcg(&q->w0), __ldcg(&q->w1), __ldcg(&q->w2)});
-  }
+  Tot s{};
+  for (int p = threadIdx.x; p < (int)gridDim.x; p += NT) s = tot_add(s, tot_ldcg((const Tot*)parts + p));
 #pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) s = i192_add(s, i192_shfl_xor(s, m));
-  I192* sw = (I192*)fx_smem;   // the cells are no longer needed
+  for (int m = 16; m >= 1; m >>= 1) s = tot_add(s, tot_shfl_xor(s, m));
+  Tot* sw = (Tot*)fx_smem;   // the cells are no longer needed
   if ((threadIdx.x & 31) == 0) sw[threadIdx.x >> 5] = s;
   __syncthreads();
   if (threadIdx.x == 0) {
-    I192 tot{0, 0, 0};
-    for (int w = 0; w < (int)(NT >> 5); ++w) tot = i192_add(tot, sw[w]);
-    // folds of the total (any split with the right weighted sum converts alike)
+    Tot tot{};
+    for (int w = 0; w < (int)(NT >> 5); ++w) tot = tot_add(tot, sw[w]);
     W128 F[K];
-    const uint64_t m40 = (1ull << 40) - 1;
-    F[K - 1] = W128{tot.w0 & m40, 0};
-    if (K == 3) {
-      F[1] = W128{((tot.w0 >> 40) | (tot.w1 << 24)) & m40, 0};
-      // tot >> 80 (arithmetic)
-      F[0] = W128{(tot.w1 >> 16) | (tot.w2 << 48), (int64_t)tot.w2 >> 16};
-    } else {
-      // tot >> 40 (arithmetic)
-      F[0] = W128{(tot.w0 >> 40) | (tot.w1 << 24), (int64_t)((tot.w1 >> 40) | (tot.w2 << 24))};
-    }
+    fx_folds<K>(tot, F);
     *result = convert_fast<double, K>(Ig, 0, F);
   }
 }
 
 // ------------------------------------------------------------------ host
 namespace {
-// cells, and at least the epilogue's reduction scratch (32 x 10 W128)
+// cells, and at least the epilogue's reduction scratch (32 warps x
+// 2 (STR - 2) W128)
+template <int K>
 size_t fx_smem_bytes(int block) {
-  size_t cells = (size_t)block * CELLS * 12;
-  return cells > 5120 ? cells : 5120;
+  const size_t cells = (size_t)block * FxGeo<K>::CELLS * 12;
+  const size_t red = (size_t)32 * 2 * FxGeo<K>::NPOS * sizeof(W128);
+  return cells > red ? cells : red;
 }
 
 template <int K, int CNT>
@@ -190,7 +226,7 @@ int fixed_blocks_per_sm(int block) {
   }
   int* slot = &cached[dev][block >> 5];
   if (*slot) return *slot;
-  size_t smem = fx_smem_bytes(block);
+  size_t smem = fx_smem_bytes<K>(block);
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(sum_f64_fixed_kernel<K, CNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess) {
@@ -218,7 +254,7 @@ int blocks_per_sm_k(int block) {
 template <int K>
 void launch_k(const double* x, int64_t n, unsigned* ctl, unsigned char* parts, double* result, int grid, int block,
               cudaStream_t s) {
-  size_t smem = fx_smem_bytes(block);
+  size_t smem = fx_smem_bytes<K>(block);
   if (block == 128)
     sum_f64_fixed_kernel<K, 128><<<grid, block, smem, s>>>(x, n, 1u, (FixedCtl*)ctl, parts, result);
   else if (block == 256)
@@ -229,20 +265,33 @@ void launch_k(const double* x, int64_t n, unsigned* ctl, unsigned char* parts, d
 }  // namespace
 
 int sum_f64_fixed_grid(int K, int block, int sms) {
-  if (K != 2 && K != 3) return 0;
   if (block < 32 || block > 1024 || (block & 31)) return 0;
-  int nb = (K == 2) ? blocks_per_sm_k<2>(block) : blocks_per_sm_k<3>(block);
+  int nb = 0;
+  switch (K) {
+    case 2: nb = blocks_per_sm_k<2>(block); break;
+    case 3: nb = blocks_per_sm_k<3>(block); break;
+    case 4: nb = blocks_per_sm_k<4>(block); break;
+    case 5: nb = blocks_per_sm_k<5>(block); break;
+    case 6: nb = blocks_per_sm_k<6>(block); break;
+    default: return 0;
+  }
   return nb > 0 ? nb * sms : 0;
 }
 
-size_t sum_f64_fixed_workspace_bytes(int grid) { return (size_t)grid * sizeof(I192); }
+// one partial per block, at the widest total's size
+size_t sum_f64_fixed_workspace_bytes(int grid) { return (size_t)grid * sizeof(I320); }
 
 cudaError_t launch_sum_f64_fixed(const double* x, int64_t n, int K, unsigned* ctl, unsigned char* parts,
                                  double* result, int grid, int block, cudaStream_t s) {
   // make sure the shared-memory attribute is set for this device and block size
   if (sum_f64_fixed_grid(K, block, 1) <= 0) return cudaErrorInvalidConfiguration;
-  if (K == 2) launch_k<2>(x, n, ctl, parts, result, grid, block, s);
-  else launch_k<3>(x, n, ctl, parts, result, grid, block, s);
+  switch (K) {
+    case 2: launch_k<2>(x, n, ctl, parts, result, grid, block, s); break;
+    case 3: launch_k<3>(x, n, ctl, parts, result, grid, block, s); break;
+    case 4: launch_k<4>(x, n, ctl, parts, result, grid, block, s); break;
+    case 5: launch_k<5>(x, n, ctl, parts, result, grid, block, s); break;
+    default: launch_k<6>(x, n, ctl, parts, result, grid, block, s); break;
+  }
   return cudaGetLastError();
 }
 
