@@ -246,8 +246,9 @@ def test_forms_agree(orc, name, x, Ks):
 def test_closed_form_brute_force(orc, dt):
     """The C closed form equals exact rational arithmetic on small inputs."""
     for seed in range(6):
-        for x in (tie_heavy(dt, 40, seed), inputs.wide_f64(40, seed=seed).astype(dt)):
-            for K in (2, 3, 4):
+        for K in (2, 3, 4, 5, 6):
+            # ties on the half grid of every fold of this K
+            for x in (tie_heavy(dt, 40, seed, K=K), inputs.wide_f64(40, seed=seed).astype(dt)):
                 want, I, F = brute_adn(x, K, dt)
                 got = orc.adn_sum(x, K)
                 I2, F2, fl = orc.adn_state(x, K)
@@ -306,7 +307,7 @@ def test_error_bound(orc, dt, nm):
         x = x[np.isfinite(x)]
         ex = orc.exact_sum_fraction(x)
         mx = Fraction(float(np.max(np.abs(x))))
-        for K in (2, 3, 4):
+        for K in (2, 3, 4, 6):
             r = orc.adn_sum(x, K)
             err = abs(Fraction(float(r)) - ex)
             ulp = Fraction(float(np.spacing(np.abs(r)))) if r != 0 else Fraction(0)
