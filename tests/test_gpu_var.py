@@ -76,6 +76,20 @@ def test_more_rows_than_resident_blocks(rows, cols):
     assert same_bits(m, wm)
 
 
+@pytest.mark.slow
+@pytest.mark.parametrize("cols", [4, 256])
+def test_rows_beyond_the_grid_cap(cols):
+    """More rows than the grid's 65535 * 16 blocks: blocks walk several rows
+    (a ragged thread at 4 columns, rows that fill the block at 256)."""
+    dev()
+    rows = 65535 * 16 + 1237
+    x = inputs.offset_rows(rows, cols, seed=cols)
+    v, m = gpu_var(x, 1, 1)
+    wv, wm = oracle.var_kernel(x, 1, 1)
+    assert same_bits(v, wv), first_diff(v, wv)
+    assert same_bits(m, wm)
+
+
 def test_nonfinite_inputs():
     dev()
     x = inputs.offset_rows(6, 513, seed=1)

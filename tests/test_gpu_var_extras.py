@@ -106,6 +106,20 @@ def test_complex_rows_one_pass_many_rows(rows, cols):
     assert same_bits(m, wm)
 
 
+@pytest.mark.slow
+def test_complex_rows_beyond_the_grid_cap():
+    """The one-pass complex kernel with more rows than its grid: blocks walk
+    several rows."""
+    dev()
+    rows = 65535 * 16 + 901
+    rng = np.random.default_rng(7)
+    z = (rng.standard_normal((rows, 3)) + 1e4 + 1j * rng.standard_normal((rows, 3))).astype(np.complex64)
+    v, m = gpu(z, 1, 1)
+    wv, wm = oracle.var_kernel_c64_2d(z, 1, 1)
+    assert same_bits(v, wv), first_diff(v, wv)
+    assert same_bits(m, wm)
+
+
 def test_complex_page_values():
     dev()
     g = load_kv("variance_complex.txt")
