@@ -536,8 +536,15 @@ __device__ __forceinline__ void c3_warp_total_tile(const T* __restrict__ in, int
     T v[NV * VW];
 #pragma unroll
     for (int u = 0; u < NV; ++u) {
-      if constexpr (sizeof(T) == 4) { v[4 * u] = r[u].x; v[4 * u + 1] = r[u].y; v[4 * u + 2] = r[u].z; v[4 * u + 3] = r[u].w; }
-      else { v[2 * u] = r[u].x; v[2 * u + 1] = r[u].y; }
+      if constexpr (sizeof(T) == 4) {
+        v[4 * u] = r[u].x;
+        v[4 * u + 1] = r[u].y;
+        v[4 * u + 2] = r[u].z;
+        v[4 * u + 3] = r[u].w;
+      } else {
+        v[2 * u] = r[u].x;
+        v[2 * u + 1] = r[u].y;
+      }
     }
     acc.template chunk<NV * VW>(v);
   } else {

@@ -117,7 +117,8 @@ extern "C" repro_status repro_sum_f32_noalloc(const float* x, size_t n, int K, c
   if (256 + (size_t)grid * stride + 64 > NOALLOC_SCRATCH_BYTES) return REPRO_ERR_CAPACITY;
   // the grid ticket must start at zero
   e = cudaMemsetAsync(d->scratch, 0, 256, stream);
-  if (e == cudaSuccess) e = repro::launch_sum<float>(x, (int64_t)n, K, d->scratch, result_dev, (int)grid, block, stream);
+  if (e == cudaSuccess)
+    e = repro::launch_sum<float>(x, (int64_t)n, K, d->scratch, result_dev, (int)grid, block, stream);
   if (e != cudaSuccess) {
     g_last_cuda_noalloc = (int)e;
     return REPRO_ERR_CUDA;
