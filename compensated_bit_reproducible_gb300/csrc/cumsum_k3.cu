@@ -1036,7 +1036,9 @@ __global__ void __launch_bounds__(1024) cf_scan(const fx::I192* __restrict__ cto
 
 // One lane's replay of its 16 elements (the first cnt - b of them when not
 // FULL): running total t from the lane's prefix, a conversion after every
-// element, results written back over the staged inputs.
+// element, results written back over the staged inputs.  The common paths
+// unroll 8 and the rare wide-total paths not at all: fully unrolled, the
+// kernel's code stalled on instruction fetch.
 template <typename T, bool FULL>
 __device__ __forceinline__ void cf_replay_lanes(T* buf, int sb, int b, int cnt, fx::I192 t, const fx::FxConst& kc,
                                                 const fx::F32Const& fk, int bf) {
@@ -1047,7 +1049,7 @@ __device__ __forceinline__ void cf_replay_lanes(T* buf, int sb, int b, int cnt, 
     const uint64_t sx = (uint64_t)((int64_t)t.w1 >> 63);
     if (t.w2 == sx && ((int64_t)t.w1 >> 62) == ((int64_t)t.w1 >> 63)) {
       uint64_t t0 = t.w0, t1 = t.w1;
-#pragma unroll
+#pragma unroll 8
       for (int i = 0; i < 16; ++i) {
         if (FULL || b + i < cnt) {
           const double v = buf[sb + i];
@@ -1077,7 +1079,7 @@ __device__ __forceinline__ void cf_replay_lanes(T* buf, int sb, int b, int cnt, 
         }
       }
     } else {
-#pragma unroll
+#pragma unroll 1
       for (int i = 0; i < 16; ++i) {
         if (FULL || b + i < cnt) {
           const double v = buf[sb + i];
@@ -1097,7 +1099,7 @@ __device__ __forceinline__ void cf_replay_lanes(T* buf, int sb, int b, int cnt, 
     const uint64_t sx = (uint64_t)(a0 >> 63);
     if (t.w1 == sx && t.w2 == sx && (a0 >> 62) == (a0 >> 63)) {
       uint32_t lo = (uint32_t)t.w0, hi = (uint32_t)(t.w0 >> 32);
-#pragma unroll
+#pragma unroll 8
       for (int i = 0; i < 16; ++i) {
         if (FULL || b + i < cnt) {
           const uint32_t bits = __float_as_uint(buf[sb + i]);
@@ -1120,7 +1122,7 @@ __device__ __forceinline__ void cf_replay_lanes(T* buf, int sb, int b, int cnt, 
       }
     } else {
       fx::I96 a{(uint32_t)t.w0, (uint32_t)(t.w0 >> 32), (uint32_t)t.w1};
-#pragma unroll
+#pragma unroll 1
       for (int i = 0; i < 16; ++i) {
         if (FULL || b + i < cnt) {
           const uint32_t bits = __float_as_uint(buf[sb + i]);
