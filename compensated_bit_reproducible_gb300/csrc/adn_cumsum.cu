@@ -340,9 +340,35 @@ __global__ void __launch_bounds__(1024) cumsum_fast_scan(const unsigned char* __
   }
 }
 
+// First level of the tile scan: block b scans tiles [256 b, 256 b + 256),
+// one per thread, into prefixes within its segment and writes the
+// segment's total (states past the last tile are zero, the merge identity).
+// cumsum_fast_scan then scans the segment totals, and the replay merges
+// both prefixes: binned merges are exact, so the order does not matter.
+constexpr int CS_SEG = 256;
+template <typename T, int KT>
+__global__ void __launch_bounds__(CS_SEG) cumsum_seg_scan(const unsigned char* __restrict__ tstate, int64_t ntiles,
+                                                          unsigned char* __restrict__ tpref,
+                                                          unsigned char* __restrict__ segtot) {
+  __shared__ RS<KT> sm[32];
+  const int I0 = Geom<T>::NB - KT;
+  const size_t st = 16 + 16 * (size_t)KT;
+  const int64_t t = (int64_t)blockIdx.x * CS_SEG + threadIdx.x;
+  RS<KT> x;
+  rs_zero(x, I0);
+  if (t < ntiles) rs_load(x, tstate + (size_t)t * st);
+  RS<KT> exc = rs_block_exclusive<KT>(x, I0, sm);
+  if (t < ntiles) rs_store(exc, tpref + (size_t)t * st);
+  if (threadIdx.x == CS_SEG - 1) {
+    rs_merge(exc, x);
+    rs_store(exc, segtot + (size_t)blockIdx.x * st);
+  }
+}
+
 template <typename T, int KT>
 __global__ void __launch_bounds__(CS_BLOCK) cumsum_fast_replay(const T* in, T* out, int64_t n,
-                                                               const unsigned char* __restrict__ tpref) {
+                                                               const unsigned char* __restrict__ tpref,
+                                                               const unsigned char* __restrict__ segpref) {
   __shared__ T sm[CS_TILE + CS_TILE / CS_ITEMS];
   __shared__ RS<KT> wsm[CS_BLOCK / 32];
   const int I0 = Geom<T>::NB - KT;
@@ -360,8 +386,10 @@ __global__ void __launch_bounds__(CS_BLOCK) cumsum_fast_replay(const T* in, T* o
       if (b + i < cnt) rs_deposit<T, KT>(mine, dg, sm[sb + i]);
   }
   RS<KT> run = rs_block_exclusive<KT>(mine, I0, wsm);
-  RS<KT> s;
+  RS<KT> s, sp;
   rs_load(s, tpref + (size_t)blockIdx.x * (16 + 16 * (size_t)KT));
+  rs_load(sp, segpref + (size_t)(blockIdx.x / CS_SEG) * (16 + 16 * (size_t)KT));
+  rs_merge(s, sp);
   rs_merge(s, run);
   Digits<T, KT> dg;
   dg.set(s.I);
@@ -543,17 +571,23 @@ template <typename T>
 size_t cumsum_workspace_bytes(int64_t n, int K) {
   if (K == 3) return cumsum_k3_workspace_bytes<T>(n);
   int64_t nt = (n + CS_TILE - 1) / CS_TILE;
-  return 2 * (size_t)nt * (16 + 16 * (size_t)K) + 64;
+  int64_t nseg = (nt + CS_SEG - 1) / CS_SEG;
+  return 2 * (size_t)(nt + nseg) * (16 + 16 * (size_t)K) + 64;   // tile and segment states and prefixes
 }
 
 template <typename T, int KT>
 static cudaError_t launch_cumsum_k(const T* in, T* out, int64_t n, int K, unsigned char* ws, cudaStream_t s) {
   int64_t nt = (n + CS_TILE - 1) / CS_TILE;
+  int64_t nseg = (nt + CS_SEG - 1) / CS_SEG;
+  const size_t st = 16 + 16 * (size_t)K;
   unsigned char* tstate = ws;
-  unsigned char* tpref = ws + (size_t)nt * (16 + 16 * (size_t)K);
+  unsigned char* tpref = tstate + (size_t)nt * st;
+  unsigned char* segtot = tpref + (size_t)nt * st;
+  unsigned char* segpref = segtot + (size_t)nseg * st;
   cumsum_fast_reduce<T, KT><<<(unsigned)nt, CS_BLOCK, 0, s>>>(in, n, K, tstate);
-  cumsum_fast_scan<T, KT><<<1, 1024, 0, s>>>(tstate, nt, tpref);
-  cumsum_fast_replay<T, KT><<<(unsigned)nt, CS_BLOCK, 0, s>>>(in, out, n, tpref);
+  cumsum_seg_scan<T, KT><<<(unsigned)nseg, CS_SEG, 0, s>>>(tstate, nt, tpref, segtot);
+  cumsum_fast_scan<T, KT><<<1, 1024, 0, s>>>(segtot, nseg, segpref);
+  cumsum_fast_replay<T, KT><<<(unsigned)nt, CS_BLOCK, 0, s>>>(in, out, n, tpref, segpref);
   return cudaGetLastError();
 }
 

@@ -41,6 +41,17 @@ def test_parity_other_k(dt, K):
     assert same_bits(got, want), first_diff(got, want)
 
 
+@pytest.mark.parametrize("dt,K", [(F64, 2), (F64, 4), (F64, 6), (F32, 4), (F32, 8)])
+def test_parity_other_k_many_tiles(dt, K):
+    """More tiles than one scan segment (256 tiles of 4096): the tile scan
+    runs in two levels; a ragged last segment and tile."""
+    dev()
+    x = inputs.wide_f64(1_300_003, seed=K + 100).astype(dt)
+    got = gpu_cumsum(x, K)
+    want = oracle.adn_cumsum(x, K)
+    assert same_bits(got, want), first_diff(got, want)
+
+
 def test_quickstart_last_prefix_equals_sum():
     dev()
     x = inputs.quickstart_f64()
