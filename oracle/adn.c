@@ -14,8 +14,10 @@
  * 10000 ones sum to exactly 10000 and the last prefix equals the sum), the
  * capacity constants, canonical NaN bits, the 10^6 x 0.001f example, equality
  * of the two forms below, brute-force permutation invariance, the closed-form
- * identity ADN = RN(exact) on grid-aligned inputs, and the absolute error
- * bound of "Template Parameters".
+ * identity ADN = RN(exact) on grid-aligned inputs, the absolute error
+ * bound of "Template Parameters", and the renormalisation period: runs of
+ * several periods of the largest odd last-fold piece, checked against exact
+ * rationals, fail with any longer period.
  */
 #include "oracle.h"
 #include "fixacc.h"

@@ -133,6 +133,13 @@ void orc_var_variant_f32(const float* x, int64_t rows, int64_t cols, int axis, i
    give 0, closeness to the exact rational variance. */
 void orc_var_kernel_f64(const double* x, int64_t rows, int64_t cols, int axis, int ddof,
                         double* var_out, double* mean_out);
+/* TwoSum of the compensated tree (section 2, step 3): *s = RN(a + b) and
+   *e the exact rounding error, so that *s + *e = a + b.  Pins: the exact
+   identity on random pairs of every exponent spread, and the tree's s2
+   equal to the correctly rounded sum of the squared residuals on slices
+   where the carries are exact and the plain tree rounds. */
+void orc_two_sum_f32(float a, float b, float* s, float* e);
+void orc_two_sum_f64(double a, double b, double* s, double* e);
 
 #ifdef __cplusplus
 }

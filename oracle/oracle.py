@@ -94,6 +94,8 @@ def _L():
             "orc_var_kernel_c64_2d": (None, [P, i64, i64, ci, ci, P, P]),
             "orc_var_variant_f32": (None, [P, i64, i64, ci, ci, ci, P, P]),
             "orc_var_kernel_f64": (None, [P, i64, i64, ci, ci, P, P]),
+            "orc_two_sum_f32": (None, [ctypes.c_float, ctypes.c_float, P, P]),
+            "orc_two_sum_f64": (None, [ctypes.c_double, ctypes.c_double, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -311,3 +313,14 @@ def var_kernel_c64_2d(z2d, axis: int = 1, ddof: int = 0):
     _L().orc_var_kernel_c64_2d(p, rows, cols, axis, ddof, v.ctypes.data_as(ctypes.c_void_p),
                                m.ctypes.data_as(ctypes.c_void_p))
     return v, m
+
+
+def two_sum(a, b):
+    """(s, e) of the variance tree's TwoSum, in the type of a (float32/float64)."""
+    if isinstance(a, np.float32):
+        s, e = ctypes.c_float(0), ctypes.c_float(0)
+        _L().orc_two_sum_f32(float(a), float(b), ctypes.byref(s), ctypes.byref(e))
+        return np.float32(s.value), np.float32(e.value)
+    s, e = ctypes.c_double(0), ctypes.c_double(0)
+    _L().orc_two_sum_f64(float(a), float(b), ctypes.byref(s), ctypes.byref(e))
+    return np.float64(s.value), np.float64(e.value)

@@ -31,7 +31,9 @@
  *
  * Pins: identical values give exactly 0.0 (kernel), the section 3 table
  * (reference and naive), the complex check 6.421875, Sterbenz exactness of
- * the shift, and closeness to the float64 two-pass value.
+ * the shift, closeness to the float64 two-pass value, TwoSum's exact error
+ * (s + e = a + b), and s2 equal to the correctly rounded sum of the leaves on
+ * integer slices where the carries are exact and a plain tree rounds.
  */
 #include "oracle.h"
 #include <math.h>
@@ -160,6 +162,11 @@ static void variant_slice_##SFX(const T* x, int64_t n, int ddof, int variant,  \
 
 DEFINE_VAR_PIECES(float, f)
 DEFINE_VAR_PIECES(double, d)
+
+/* The error-free transformation itself, exported so that it can be checked
+   on its own: s = RN(a + b) and s + e = a + b exactly. */
+void orc_two_sum_f32(float a, float b, float* s, float* e) { two_sum_f(a, b, s, e); }
+void orc_two_sum_f64(double a, double b, double* s, double* e) { two_sum_d(a, b, s, e); }
 
 static float tree_plain(float* a, int64_t n) { return tree_plain_f(a, n); }
 

@@ -567,3 +567,128 @@ def test_complex_2d_matches_parts_and_the_page(orc):
         vi, mi = orc.var_kernel(np.ascontiguousarray(zz.imag), axis, 1)
         assert arr_same(v, (vr + vi).astype(np.float32))
         assert arr_same(m.real.copy(), mr) and arr_same(m.imag.copy(), mi)
+
+
+# ------------------------------------------- compensation and renormalisation
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_two_sum_is_error_free(orc, dt):
+    """Variance note, section 2, step 3: TwoSum returns the rounded sum and
+    its exact rounding error, so s = RN(a + b) and s + e = a + b exactly,
+    whatever the exponent spread of the two operands."""
+    rng = np.random.default_rng(31)
+    span = 30 if dt == F32 else 60
+    nonzero_errors = 0
+    for _ in range(3000):
+        a = dt(rng.standard_normal() * 2.0 ** int(rng.integers(-span, span)))
+        b = dt(rng.standard_normal() * 2.0 ** int(rng.integers(-span, span)))
+        s, e = orc.two_sum(a, b)
+        assert same_bits(s, dt(a + b))
+        assert Fraction(float(s)) + Fraction(float(e)) == Fraction(float(a)) + Fraction(float(b))
+        nonzero_errors += e != 0
+    assert nonzero_errors > 1000      # the pairs do round
+
+
+def _plain_tree(v, dt):
+    """Adjacent-pair tree of plain rounded adds (only used to pick slices on
+    which the plain tree and the compensated tree must differ)."""
+    a = [dt(t) for t in v]
+    while len(a) > 1:
+        nxt = [dt(a[2 * i] + a[2 * i + 1]) for i in range(len(a) // 2)]
+        if len(a) % 2:
+            nxt.append(a[-1])
+        a = nxt
+    return a[0]
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_twosum_tree_gives_the_rounded_exact_sum(orc, dt):
+    """Variance note, section 2, step 3 (errors carried up a second array,
+    final sum plus final carry).  On integer slices of a power-of-two length
+    whose values sum to zero, the shift and centring are exact, so d = x,
+    s1 = 0 and var = s2 / n exactly.  The TwoSum errors are small integers,
+    so the carries add without rounding and s2 must be the correctly rounded
+    exact sum of the leaves RN(d_i * d_i).  Deviations up to 1.2 * 2^(p/2)
+    make some leaves round and most partial sums need more than p bits, so
+    the plain tree (a dropped error term) gives another value on many of
+    these slices."""
+    g = GEO[dt]
+    rng = np.random.default_rng(41)
+    lim = int(1.2 * 2 ** (g["prec"] // 2))
+    differ = 0
+    for _ in range(300):
+        n = int(rng.choice([4, 8, 16, 32]))
+        half = rng.integers(1, lim, n // 2)
+        d = np.concatenate([half, -half])
+        rng.shuffle(d)
+        x = d.astype(dt)[None, :]
+        leaves = [dt(dt(v) * dt(v)) for v in d]
+        want = round_frac(sum(Fraction(float(t)) for t in leaves), g["prec"], g["qmin"], g["emax"])
+        if dt == F32:
+            var, mean = orc.var_kernel(x, 1)
+        else:
+            var, mean = orc.var_kernel_f64(x, 1)
+        assert float(var[0]) * n == want, (d.tolist(), float(var[0]) * n, want)
+        assert mean[0] == 0
+        differ += float(_plain_tree(leaves, dt)) != want
+    assert differ >= 30, differ
+    if dt == F32:
+        # the plain-tree variant (section 4, row 3) is the dropped-error tree
+        x = np.array([[4095, -4095, 1, -1, 4095, -4095, 3, -3]], F32)
+        plain = float(orc.var_variant(x, 3, 1)[0][0]) * 8
+        comp = float(orc.var_kernel(x, 1)[0][0]) * 8
+        leaves = [F32(F32(v) * F32(v)) for v in x[0]]
+        assert comp == round_frac(sum(Fraction(float(t)) for t in leaves), 24, -149, 128)
+        assert plain == float(_plain_tree(leaves, F32))
+
+
+def _odd_last_piece_values(dt, K):
+    """(values, I) for the renormalisation pin: a leading value that fixes the
+    index at I, then a value whose last-fold piece is 2^(W-1) - 1 grid units
+    (odd, the largest a fold takes) and whose piece on the fold above it is
+    4095 grid units."""
+    g = GEO[dt]
+    W = g["W"]
+    I = 8 if dt == F32 else 24
+    grid = [Fraction(2) ** (g["b0"] - W * (I + k)) for k in range(K)]
+    lead = grid[0]                                   # pieces (1, 0, ...)
+    v = 4095 * grid[K - 2] + (2 ** (W - 1) - 1) * grid[K - 1]
+    if dt == F32:
+        v = 2047 * grid[K - 2] + (2 ** (W - 1) - 1) * grid[K - 1]   # 24 bits
+    out = [dt(float(lead)), dt(float(v))]
+    assert [Fraction(float(t)) for t in out] == [lead, v]
+    return out, I
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+@pytest.mark.parametrize("K", [2, 3])
+def test_renormalisation_period(orc, dt, K):
+    """SyclReproSum, How It Works, step 2: every 2^(p-W-2) deposits the
+    primaries give their drift to the carries.  A primary starts in
+    [1.5, 1.75) of its binade and each deposit moves it by at most
+    2^(W-1) grid units, so one period keeps it in its binade; a longer one
+    lets it leave, its ulp doubles and odd pieces round.  In a fold above the
+    last that only moves the rounding difference down to the next fold, and
+    the total stays; the last fold drops it.  So the pin drifts the last fold
+    with its largest odd piece, in runs of both signs, for several periods,
+    and compares the sequential primary form with exact rationals."""
+    g = GEO[dt]
+    period = 2 ** (g["prec"] - g["W"] - 2)
+    (lead, v), I = _odd_last_piece_values(dt, K)
+    want1, I1, F1 = brute_adn([lead, v], K, dt)
+    assert I1 == I and F1[K - 1] == 2 ** (g["W"] - 1) - 1 and F1[K - 2] != 0
+    _, _, Fv = brute_adn([lead, v], K, dt)
+    Fv = [Fv[k] - (1 if k == 0 else 0) for k in range(K)]      # v's own pieces
+    # lead and -lead fix the index and cancel, so the result is small enough
+    # for its last bits to show the last fold's grid unit
+    for runs in ((4 * period, -4 * period + 1), (-4 * period, 4 * period - 1),
+                 (3 * period, -5 * period, 2 * period + 5), (8 * period + 77, -8 * period)):
+        xs = np.concatenate([[lead, -lead]] + [np.full(abs(r), v if r > 0 else -v, dt) for r in runs])
+        xs = xs.astype(dt)
+        m = sum(runs)
+        tot = sum(m * Fv[k] * Fraction(2) ** (g["b0"] - g["W"] * (I + k)) for k in range(K))
+        want = dt(round_frac(tot, g["prec"], g["qmin"], g["emax"]))
+        assert same_bits(orc.adn_sum(xs, K, "fp"), want), (runs,)
+        assert same_bits(orc.adn_sum(xs, K, "closed"), want), (runs,)
+    # the fold sums themselves, by brute force on one run
+    xs = np.concatenate([[lead], np.full(4 * period, v, dt)]).astype(dt)
+    assert brute_adn(xs, K, dt)[2] == [(1 if k == 0 else 0) + 4 * period * Fv[k] for k in range(K)]
