@@ -119,8 +119,7 @@ std::mutex g_env_mu;
 int g_env_state[64] = {0};   // 0 unknown, 1 ok, 2 failed
 
 repro_status validate_env(cudaStream_t stream) {
-  const char* force = std::getenv("REPRO_FORCE_ENV_FAIL");
-  if (force && force[0] == '1') return REPRO_ERR_ENV;
+  if (env_fail_forced()) return REPRO_ERR_ENV;
   int dev = 0;
   CK(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return REPRO_ERR_ENV;
@@ -605,3 +604,11 @@ repro_status repro_state_finalize_f64(const void* state, int K, double* result_d
 }
 
 }  // extern "C"
+
+namespace repro {
+void set_last_cuda(cudaError_t e) { g_last_cuda = (int)e; }
+bool env_fail_forced() {
+  const char* force = std::getenv("REPRO_FORCE_ENV_FAIL");
+  return force && force[0] == '1';
+}
+}  // namespace repro

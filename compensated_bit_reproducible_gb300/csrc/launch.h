@@ -70,5 +70,11 @@ constexpr int COMPENSATED_CHUNK = 4096;
 
 // environment probe: writes check bits to *out (device), 0 = all passed
 cudaError_t launch_env_probe(unsigned* out, cudaStream_t s);
+// true when REPRO_FORCE_ENV_FAIL=1 asks every environment check to fail
+bool env_fail_forced();
+
+// The calling host thread's last CUDA error, the one repro_last_cuda_error()
+// returns; every entry point that returns REPRO_ERR_CUDA records its code here.
+void set_last_cuda(cudaError_t e);
 
 }  // namespace repro

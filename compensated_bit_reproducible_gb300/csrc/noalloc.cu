@@ -20,7 +20,12 @@
 //    must order them (one stream, or events between streams);
 //  - the first call on a device does the set-up (the array's device address
 //    and the floating-point environment probe) and waits for it; make that
-//    first call before any stream capture.
+//    first call before any stream capture;
+//  - the device address is kept for the life of the process: after a
+//    cudaDeviceReset the array belongs to a context that no longer exists,
+//    and the entry point must not be called again in that process;
+//  - CUDA errors are reported like every other entry point's: status
+//    REPRO_ERR_CUDA, code in repro_last_cuda_error().
 #include <cuda_runtime.h>
 #include <cstdint>
 #include <mutex>
@@ -45,7 +50,6 @@ struct DevInfo {
 
 std::mutex g_mu;
 DevInfo g_dev[NOALLOC_MAX_DEVICES];
-thread_local int g_last_cuda_noalloc = 0;
 
 // Once per device, with that device current: the array's device address, the
 // SM count and the environment probe (its one result word is written into the
@@ -57,13 +61,13 @@ repro_status setup(int dev, cudaStream_t stream, DevInfo** out) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) {
-      g_last_cuda_noalloc = (int)e;
+      repro::set_last_cuda(e);
       return REPRO_ERR_CUDA;
     }
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) {
-      g_last_cuda_noalloc = (int)e;
+      repro::set_last_cuda(e);
       return REPRO_ERR_CUDA;
     }
     unsigned probe = 0xFFFFFFFFu;
@@ -71,7 +75,7 @@ repro_status setup(int dev, cudaStream_t stream, DevInfo** out) {
     if (e == cudaSuccess) e = cudaMemcpyAsync(&probe, p, sizeof(unsigned), cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) {
-      g_last_cuda_noalloc = (int)e;
+      repro::set_last_cuda(e);
       return REPRO_ERR_CUDA;
     }
     d.scratch = (unsigned char*)p;
@@ -94,10 +98,11 @@ extern "C" repro_status repro_sum_f32_noalloc(const float* x, size_t n, int K, c
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) {
-    g_last_cuda_noalloc = (int)e;
+    repro::set_last_cuda(e);
     return REPRO_ERR_CUDA;
   }
   if (dev < 0 || dev >= NOALLOC_MAX_DEVICES) return REPRO_ERR_INVALID_ARG;
+  if (repro::env_fail_forced()) return REPRO_ERR_ENV;
   DevInfo* d = nullptr;
   repro_status st = setup(dev, stream, &d);
   if (st != REPRO_OK) return st;
@@ -120,7 +125,7 @@ extern "C" repro_status repro_sum_f32_noalloc(const float* x, size_t n, int K, c
   if (e == cudaSuccess)
     e = repro::launch_sum<float>(x, (int64_t)n, K, d->scratch, result_dev, (int)grid, block, stream);
   if (e != cudaSuccess) {
-    g_last_cuda_noalloc = (int)e;
+    repro::set_last_cuda(e);
     return REPRO_ERR_CUDA;
   }
   return REPRO_OK;

@@ -115,7 +115,11 @@ repro_status repro_sum_f64_async(const double* x, size_t n, int K, cudaStream_t 
    share the array (each clears what must start at zero): calls whose work
    overlaps on the GPU race, so order them on one stream or with events.  The
    first call on a device sets up (device address of the array, environment
-   probe) and waits for it; make it before any stream capture. */
+   probe) and waits for it; make it before any stream capture.  The address
+   is kept until the process exits: after cudaDeviceReset do not call this
+   entry point again in that process.  A failed CUDA call gives
+   REPRO_ERR_CUDA with its code in repro_last_cuda_error(); the environment
+   check honours REPRO_FORCE_ENV_FAIL like every other (REPRO_ERR_ENV). */
 repro_status repro_sum_f32_noalloc(const float* x, size_t n, int K, cudaStream_t stream, float* result_dev);
 
 /* ---- binned states ("How It Works": deposit and merge; "API Reference":

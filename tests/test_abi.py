@@ -108,3 +108,26 @@ def test_state_calls_check_arguments_first(L):
 def test_strerror(L):
     for s in range(7):
         assert L.repro_strerror(s)
+
+
+def test_noalloc_cuda_error_reaches_last_cuda_error(L):
+    """Without a usable GPU the allocation-free sum fails in its first CUDA
+    call; the code must come back through repro_last_cuda_error() in the
+    calling thread, like every other entry point's.  A fresh thread starts
+    with an empty error slot, so a code kept anywhere else reads as 0."""
+    import threading
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("needs a machine without a usable GPU (the pointers here are not real)")
+    P = ctypes.c_void_p
+    got = {}
+
+    def call():
+        got["rc"] = L.repro_sum_f32_noalloc(P(0x1000), 16, 3, None, P(0x2000))
+        got["cuda"] = L.repro_last_cuda_error()
+
+    t = threading.Thread(target=call)
+    t.start()
+    t.join()
+    assert got["rc"] == 5, got
+    assert got["cuda"] != 0, got

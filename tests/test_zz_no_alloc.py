@@ -13,6 +13,7 @@ import pytest
 import torch
 
 from compensated_bit_reproducible_gb300 import api, inputs
+from oracle import oracle as orc
 
 pytestmark = pytest.mark.gpu
 
@@ -58,6 +59,23 @@ def test_matches_the_allocating_sum_on_consecutive_calls():
         second = _noalloc(t, K)
         assert first.tobytes() == want.tobytes()
         assert second.tobytes() == want.tobytes()
+        # and the oracle's binned sum of the same input
+        assert first.tobytes() == np.array([orc.adn_sum(x, K)], np.float32).tobytes()
+
+
+def test_forced_environment_failure(monkeypatch):
+    """REPRO_FORCE_ENV_FAIL=1 makes the environment check fail here as in
+    every other entry point, before anything is launched."""
+    d = _dev()
+    x = torch.ones(1000, dtype=torch.float32, device=d)
+    out = torch.full((1,), 7.0, dtype=torch.float32, device=d)
+    L = api.lib()
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    monkeypatch.setenv("REPRO_FORCE_ENV_FAIL", "1")
+    assert L.repro_sum_f32_noalloc(ctypes.c_void_p(x.data_ptr()), 1000, 3, s, ctypes.c_void_p(out.data_ptr())) == 4
+    monkeypatch.delenv("REPRO_FORCE_ENV_FAIL")
+    assert L.repro_sum_f32_noalloc(ctypes.c_void_p(x.data_ptr()), 1000, 3, s, ctypes.c_void_p(out.data_ptr())) == 0
+    assert out.item() == 1000.0
 
 
 def test_empty_input_and_rejected_arguments():
