@@ -133,6 +133,61 @@ __device__ __forceinline__ bool t128_to_double_normal(uint64_t t0, uint64_t t1, 
   return true;
 }
 
+// Conversions through the hardware's integer-to-floating-point rounding.
+// A value S rounds alike directly and through its round-to-odd window: with
+// S = W 2^k + r (0 <= r < 2^k, W = floor(S / 2^k)), W' = W | [r != 0] is
+// the odd neighbour of S / 2^k unless that is an integer, and RN(W') equals
+// RN(S / 2^k) to p bits whenever W' carries at least p + 2 bits.  k is the
+// smallest shift that fits W in the signed window (62 or 30 value bits), so
+// the window holds more than enough; the cvt then rounds to nearest even and
+// 2^k 2^lsb enters as an exponent-field addition.  False (nothing written)
+// for S = 0 and for results outside the normal range.
+
+// funnel right shift (hi:lo) >> n, n in [0, 32] (32 gives hi)
+__device__ __forceinline__ uint32_t shr_pair_clamp(uint32_t lo, uint32_t hi, int n) {
+  uint32_t r;
+  asm("shf.r.clamp.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(lo), "r"(hi), "r"(n));
+  return r;
+}
+
+// Signed 128-bit S = (t1:t0) times 2^lsb to double: a 64-bit window and
+// one cvt.rn.f64.s64.
+__device__ __forceinline__ bool t128_to_double_win(uint64_t t0, uint64_t t1, int lsb, double* out) {
+  const uint32_t x0 = (uint32_t)t0, x1 = (uint32_t)(t0 >> 32), x2 = (uint32_t)t1, x3 = (uint32_t)(t1 >> 32);
+  const uint32_t s = (uint32_t)((int32_t)x3 >> 31);
+  const bool fits = (x3 == s) & (x2 == s) & ((uint32_t)((int32_t)x1 >> 31) == s);
+  const uint32_t ah = x3 ^ s, al = x2 ^ s;
+  const int lz = ah ? __clz((int)ah) : 32 + __clz((int)al);   // 1 .. 64 when S does not fit
+  const int k = fits ? 0 : 65 - lz;                           // 0 .. 64
+  const bool up = k >= 32;
+  const uint32_t a0 = up ? x1 : x0, a1 = up ? x2 : x1, a2 = up ? x3 : x2;
+  const int kk = up ? k - 32 : k;                             // 0 .. 32
+  const uint32_t wh = shr_pair_clamp(a1, a2, kk);
+  const uint32_t st = (fx::shl_clamp32(a0, 32 - kk) | (up ? x0 : 0u)) != 0u ? 1u : 0u;
+  const uint32_t wl = shr_pair_clamp(a0, a1, kk) | st;
+  double d;
+  asm("cvt.rn.f64.s64 %0, %1;" : "=d"(d) : "l"((long long)(((uint64_t)wh << 32) | wl)));
+  const uint32_t bh = (uint32_t)__double2hiint(d);
+  const int E = (int)((bh >> 20) & 0x7FFu), E2 = E + k + lsb;
+  if (E == 0 || (unsigned)(E2 - 1) > 2045u) return false;
+  *out = __hiloint2double((int)(bh + ((uint32_t)(k + lsb) << 20)), __double2loint(d));
+  return true;
+}
+
+// Signed 64-bit S = (hi:lo) times 2^lsb to float: a 32-bit window and one
+// cvt.rn.f32.s32 (a full-rate conversion, unlike the 64-bit ones).
+__device__ __forceinline__ bool i64_to_float_win(uint32_t lo, uint32_t hi, int lsb, uint32_t* out) {
+  const uint32_t s = (uint32_t)((int32_t)hi >> 31);
+  const bool fits = (hi == s) & ((uint32_t)((int32_t)lo >> 31) == s);
+  const int k = fits ? 0 : 33 - __clz((int)(hi ^ s));         // 0 .. 32
+  const uint32_t w = shr_pair_clamp(lo, hi, k) | (fx::shl_clamp32(lo, 32 - k) != 0u ? 1u : 0u);
+  const uint32_t b = __float_as_uint(__int2float_rn((int)w));
+  const int E = (int)((b >> 23) & 0xFFu), E2 = E + k + lsb;
+  if (E == 0 || (unsigned)(E2 - 1) > 253u) return false;
+  *out = b + ((uint32_t)(k + lsb) << 23);
+  return true;
+}
+
 // double: T is a signed 192-bit integer (t2:t1:t0) times 2^lsb.
 __device__ __forceinline__ double round_t192_d(int64_t t2, uint64_t t1, uint64_t t0, int lsb) {
   double r;
@@ -825,11 +880,11 @@ __device__ __forceinline__ void cf_stage(T* buf, const T* g, int cnt, int lane) 
 // Double totals: each thread deposits its elements' rounded values into
 // 64-bit word cells in shared memory (cell k + 8 s: word position k of
 // M' 2^u for the sign s, the rounding of the binned sum's fixed-index
-// deposit), the cells accumulating over all of the thread's chunks.  The
-// value of the cells is sum_s (-1)^s sum_{k = 2..6} cell 2^(32 (k - 2)) in
-// units of g_f (positions 0, 1 lie below the grid; 7 only beyond the guessed
-// bin, which fails the guess), so a lane's sum over its 16 elements is the
-// difference of the values after and before them.
+// deposit).  The value of the cells is
+// sum_s (-1)^s sum_{k = 2..6} cell 2^(32 (k - 2)) in units of g_f
+// (positions 0, 1 lie below the grid and are never read; 7 only beyond the
+// guessed bin, which fails the guess); a lane takes that value after its 16
+// elements and clears the cells it read.
 constexpr int CT_CELLS = 16;
 template <typename T>
 __host__ __device__ constexpr int ct_cell_bytes() {
@@ -856,15 +911,26 @@ __device__ __forceinline__ void ct_deposit(uint32_t hi, uint32_t lo, const fx::F
   p[2 * C3_BLOCK] = fx::madw(w2, k.one, p[2 * C3_BLOCK]);
 }
 
-__device__ __forceinline__ fx::I192 ct_value(const uint64_t* A) {
-  fx::I192 t{0, 0, 0};
+// The value of the thread's cells, which are then cleared: the sum of the
+// rounded values deposited since the last call.  Per word position the two
+// signs' cells subtract to a 64-bit d_w (each cell sums at most 16 words
+// between calls), and the five d_w combine at their 32-bit offsets.
+__device__ __forceinline__ fx::I192 ct_take(uint64_t* A) {
+  int64_t d[5];
 #pragma unroll
-  for (int s = 0; s < 2; ++s)
-#pragma unroll
-    for (int w = 2; w < 7; ++w) {
-      const fx::I192 v = fx::i192_from_shifted(W128{A[(w + 8 * s) * C3_BLOCK], 0}, w - 2);
-      t = fx::i192_add(t, s ? fx::i192_neg(v) : v);
-    }
+  for (int w = 2; w < 7; ++w) {
+    const uint64_t pos = A[w * C3_BLOCK], neg = A[(w + 8) * C3_BLOCK];
+    A[w * C3_BLOCK] = 0;
+    A[(w + 8) * C3_BLOCK] = 0;
+    d[w - 2] = (int64_t)(pos - neg);
+  }
+  const uint64_t x0 = (uint64_t)(d[0] >> 63), x1 = (uint64_t)(d[1] >> 63), x2 = (uint64_t)(d[2] >> 63),
+                 x3 = (uint64_t)(d[3] >> 63);
+  fx::I192 t{(uint64_t)d[0], x0, x0};
+  t = fx::i192_add(t, fx::I192{(uint64_t)d[1] << 32, (uint64_t)(d[1] >> 32), x1});
+  t = fx::i192_add(t, fx::I192{0, (uint64_t)d[2], x2});
+  t = fx::i192_add(t, fx::I192{0, (uint64_t)d[3] << 32, (uint64_t)(d[3] >> 32)});
+  t.w2 += (uint64_t)d[4];
   return t;
 }
 
@@ -907,7 +973,6 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
     if (L < facc.I) facc.raise(L);
   }
   uint64_t* A = (uint64_t*)ct_smem + threadIdx.x;   // double: this thread's cells
-  fx::I192 prev{0, 0, 0};                             // double: value of the cells so far
   const uint32_t c8 = 8u * one;
   if constexpr (sizeof(T) == 8) {
 #pragma unroll
@@ -924,15 +989,27 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
     __syncwarp();
     const int b = lane * 16, sb = b + lane;
     T v[16];
+    uint32_t em = 0;   // largest magnitude bits (hi word shifted past the sign)
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       v[i] = b + i < cnt ? buf[sb + i] : (T)0;
       uint32_t hi;
       if constexpr (sizeof(T) == 8) hi = (uint32_t)__double2hiint(v[i]);
       else hi = __float_as_uint(v[i]);
-      const int eb = (int)((hi << 1) >> (sizeof(T) == 8 ? 21 : 24));
-      ebmax = max(ebmax, eb);
-      if (look && eb >= eb_bot) first = min(first, c0 + b + i);
+      em = max(em, hi << 1);
+    }
+    ebmax = max(ebmax, (int)(em >> (sizeof(T) == 8 ? 21 : 24)));
+    if (look) {
+#pragma unroll 1
+      for (int i = 0; i < 16 && b + i < cnt; ++i) {
+        uint32_t hi;
+        if constexpr (sizeof(T) == 8) hi = (uint32_t)__double2hiint(buf[sb + i]);
+        else hi = __float_as_uint(buf[sb + i]);
+        if ((int)((hi << 1) >> (sizeof(T) == 8 ? 21 : 24)) >= eb_bot) {
+          first = min(first, c0 + b + i);
+          break;
+        }
+      }
     }
     const size_t li = (size_t)ch * 32 + lane;
     if constexpr (sizeof(T) == 8) {
@@ -940,9 +1017,7 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
 #pragma unroll
       for (int i = 0; i < 16; ++i)
         ct_deposit((uint32_t)__double2hiint(v[i]), (uint32_t)__double2loint(v[i]), kc, c8, A);
-      const fx::I192 val = ct_value(A);
-      const fx::I192 own = fx::i192_add(val, fx::i192_neg(prev));
-      prev = val;
+      const fx::I192 own = ct_take(A);
       const fx::I192 exc = i192_warp_exclusive(own, &tot);
       const size_t plane = (size_t)nch * 32;
       uint64_t* lp = (uint64_t*)lanep;
@@ -1034,6 +1109,163 @@ __global__ void __launch_bounds__(1024) cf_scan(const fx::I192* __restrict__ cto
   }
 }
 
+// Lanes with a fixed window.  If every element of a lane rounds to
+// |R| <= 2^A and the lane starts from t with |t| <= 2^(p0 + 1), every
+// prefix of the lane stays below 2^pu, pu = max(p0 + 1, A + 4) + 1.  The
+// double lanes keep their total pre-shifted, S' = S 2^c with c = 126 - pu,
+// so that S' never overflows and the round-to-odd window of a prefix is the
+// top word of S' with the bits below as one sticky bit, whenever that word
+// holds enough bits (|W| >= 2^54): no leading-bit search and no shift per
+// element.  A prefix below that (cancellation within the lane) takes the
+// general conversion of S'.  Each increment enters as R 2^c, with the
+// product bits below 2^(64 + c) (the grid's fraction) masked off.  The
+// window results' exponent range is checked once for the lane; lanes
+// outside it, or with c < 0, take the general loop.
+
+// The lane's largest exponent field, over its valid elements.
+template <typename T>
+__device__ __forceinline__ uint32_t lane_exp_max(const T* buf, int sb, int b, int cnt) {
+  uint32_t em = 0;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    uint32_t hi;
+    if constexpr (sizeof(T) == 8) hi = (uint32_t)__double2hiint(buf[sb + i]);
+    else hi = __float_as_uint(buf[sb + i]);
+    const uint32_t e = (hi << 1) >> (sizeof(T) == 8 ? 21 : 24);
+    if (b + i < cnt) em = max(em, e);
+  }
+  return em;
+}
+
+// Double lanes, 128-bit totals (t1:t0).  Returns false, writing nothing,
+// when the lane cannot take the window.
+__device__ __forceinline__ bool cf_lane_window_f64(double* buf, int sb, int b, int cnt, uint64_t t0, uint64_t t1,
+                                                   const fx::FxConst& kc, int bf) {
+  const int e = max((int)lane_exp_max<double>(buf, sb, b, cnt), 1) - 1023;   // |x| < 2^(e + 1)
+  const int A = e + 1 - bf;                                                   // |R| <= 2^A
+  const uint64_t sg = (uint64_t)((int64_t)t1 >> 63);
+  const uint64_t a1 = t1 ^ sg, a0 = t0 ^ sg;
+  const int p0 = 127 - (a1 ? __clzll((long long)a1) : 64 + __clzll((long long)a0));   // |t| <= 2^(p0 + 1)
+  const int pu = max(p0 + 1, A + 4) + 1;
+  const int c = 126 - pu;
+  if (c < 0 || pu - 8 + bf < -1022 || pu + bf > 1023) return false;
+  // S' = t 2^c, masks of R' = R 2^c (low c bits clear), exponent offset of the window
+  uint64_t u0 = t0, u1 = t1, m0 = ~0ull, m1 = ~0ull;
+  if (c >= 64) {
+    u1 = t0 << (c - 64);
+    u0 = 0;
+    m0 = 0;
+    m1 = ~0ull << (c - 64);
+  } else if (c > 0) {
+    u1 = (t1 << c) | (t0 >> (64 - c));
+    u0 = t0 << c;
+    m0 = ~0ull << c;
+  }
+  const uint32_t eadd = (uint32_t)(64 - c + bf) << 20;
+  const uint32_t cc = (uint32_t)c;
+#pragma unroll 8
+  for (int i = 0; i < 16; ++i) {
+    if (b + i < cnt) {
+      const double v = buf[sb + i];
+      const uint32_t hi = (uint32_t)__double2hiint(v), lo = (uint32_t)__double2loint(v);
+      // the element's rounding at g_f (as in fx::round_f64), placed c bits higher
+      const uint32_t eb = fx::mad32(hi, kc.one + kc.one, 0u) >> 21;
+      const uint32_t u = (uint32_t)max((int)fx::mad32(eb, kc.one, kc.Cp), 0);
+      const uint32_t mh = (hi & 0xFFFFFu) | 0x100000u;
+      const uint32_t hl = fx::shl_clamp32(1u, (int)fx::mad32(u, kc.negone, kc.c63));
+      const uint32_t hh = fx::shl_clamp32(1u, (int)fx::mad32(u, kc.negone, kc.c31));
+      const uint32_t rb = min(mh & fx::mad32(hl, kc.c256, 0u), 1u);
+      const uint64_t Mp = ((((uint64_t)mh) << 32) | lo) + ((((uint64_t)hh) << 32) | hl) - (uint64_t)rb;
+      const uint32_t lo2 = (uint32_t)Mp, mh2 = (uint32_t)(Mp >> 32);
+      const uint32_t up = fx::mad32(u, kc.one, cc);
+      const uint32_t q0 = fx::shl_clamp32(1u, (int)up), q1 = fx::shl_clamp32(1u, (int)up - 32),
+                     q2 = fx::shl_clamp32(1u, (int)up - 64), q3 = fx::shl_clamp32(1u, (int)up - 96),
+                     q4 = fx::shl_clamp32(1u, (int)up - 128);
+      const uint64_t a0 = fx::madw(lo2, q0, 0), a1 = fx::madw(lo2, q1, 0), a2 = fx::madw(lo2, q2, 0),
+                     a3 = fx::madw(lo2, q3, 0), a4 = fx::madw(lo2, q4, 0);
+      const uint64_t s0 = fx::madw(mh2, q0, a0 >> 32), s1 = fx::madw(mh2, q1, a1 >> 32),
+                     s2 = fx::madw(mh2, q2, a2 >> 32), s3 = fx::madw(mh2, q3, a3 >> 32),
+                     s4 = fx::madw(mh2, q4, a4 >> 32);
+      const uint32_t V0 = (uint32_t)a2 | (uint32_t)s1 | (uint32_t)(s0 >> 32);
+      const uint32_t V1 = (uint32_t)a3 | (uint32_t)s2 | (uint32_t)(s1 >> 32);
+      const uint32_t V2 = (uint32_t)a4 | (uint32_t)s3 | (uint32_t)(s2 >> 32);
+      const uint32_t V3 = (uint32_t)s4 | (uint32_t)(s3 >> 32);
+      const uint64_t rl = ((((uint64_t)V1) << 32) | V0) & m0, rh = ((((uint64_t)V3) << 32) | V2) & m1;
+      const uint32_t sm = (uint32_t)((int32_t)hi >> 31);
+      const uint64_t S = (uint64_t)(int64_t)(int32_t)sm;
+      const uint64_t xl = rl ^ S, xh = rh ^ S;
+      uint32_t r0, r1, r2, r3;
+      asm("{\n\t.reg .u32 c;\n\t"
+          "add.cc.u32 c, %4, 0xFFFFFFFF;\n\t"
+          "addc.cc.u32 %0, %5, %9;\n\t"
+          "addc.cc.u32 %1, %6, %10;\n\t"
+          "addc.cc.u32 %2, %7, %11;\n\t"
+          "addc.u32 %3, %8, %12;\n\t}"
+          : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+          : "r"(sm & 1u), "r"((uint32_t)u0), "r"((uint32_t)(u0 >> 32)), "r"((uint32_t)u1),
+            "r"((uint32_t)(u1 >> 32)), "r"((uint32_t)xl), "r"((uint32_t)(xl >> 32)), "r"((uint32_t)xh),
+            "r"((uint32_t)(xh >> 32)));
+      u0 = ((uint64_t)r1 << 32) | r0;
+      u1 = ((uint64_t)r3 << 32) | r2;
+      double res;
+      if (((r3 ^ (uint32_t)((int32_t)r3 >> 31)) >> 22) != 0u) {
+        // window: the top word, the bits below as a sticky bit
+        const uint32_t st = min(r0 | r1, 1u);
+        double d;
+        asm("cvt.rn.f64.s64 %0, %1;" : "=d"(d) : "l"((long long)(u1 | st)));
+        res = __hiloint2double((int)((uint32_t)__double2hiint(d) + eadd), __double2loint(d));
+      } else if (!t128_to_double_win(u0, u1, bf - c, &res)) {
+        res = round_t192_d((int64_t)u1 >> 63, u1, u0, bf - c);
+      }
+      buf[sb + i] = res;
+    }
+  }
+  return true;
+}
+
+// Float lanes, 64-bit totals: a 32-bit window, taken only when the lane's
+// start dominates its elements (p0 >= A + 6: the 16 increments move the
+// total by at most 2^(p0 - 2), so every prefix keeps its leading bit
+// within p0 - 1 .. p0 + 1 and the window, with c = 60 - p0, always holds
+// 27 to 30 bits).  No check per element: for float data that condition
+// holds for nearly every lane, and a per-element check measured slower
+// than the rare lanes that take the general loop.
+__device__ __forceinline__ bool cf_lane_window_f32(float* buf, int sb, int b, int cnt, int64_t t,
+                                                   const fx::F32Const& fk, int bf) {
+  const int e = max((int)lane_exp_max<float>(buf, sb, b, cnt), 1) - 127;
+  const int A = e + 1 - bf;
+  const uint64_t a = (uint64_t)(t ^ (t >> 63));
+  const int p0 = 63 - __clzll((long long)a);   // 2^p0 <= |t| <= 2^(p0 + 1)
+  const int c = 60 - p0, ex = p0 + bf;
+  if (!(p0 >= 0 && p0 >= A + 6 && c >= 0 && ex - 1 >= -126 && ex + 1 <= 127)) return false;
+  const uint64_t ts = (uint64_t)t << c;
+  uint32_t lo = (uint32_t)ts, hi = (uint32_t)(ts >> 32);
+  const bool cw = c >= 32;
+  const uint32_t cs = (uint32_t)(c & 31);
+  const uint32_t eadd = (uint32_t)(32 - c + bf) << 23;
+#pragma unroll 8
+  for (int i = 0; i < 16; ++i) {
+    if (b + i < cnt) {
+      const uint32_t bits = __float_as_uint(buf[sb + i]);
+      uint32_t rl, rh;
+      fx::round_f32w(bits, fk, rl, rh);
+      // R 2^c (R is an integer: exact)
+      const uint32_t ls = rl << cs, hs = fx::funnel_l(rl, rh, cs);
+      const uint32_t xl = cw ? 0u : ls, xh = cw ? ls : hs;
+      const uint32_t sm = (uint32_t)((int32_t)bits >> 31);
+      asm("{\n\t.reg .u32 c;\n\t"
+          "add.cc.u32 c, %2, 0xFFFFFFFF;\n\t"
+          "addc.cc.u32 %0, %0, %3;\n\t"
+          "addc.u32 %1, %1, %4;\n\t}"
+          : "+r"(lo), "+r"(hi)
+          : "r"(sm & 1u), "r"(xl ^ sm), "r"(xh ^ sm));
+      const uint32_t w = hi | min(lo, 1u);
+      buf[sb + i] = __uint_as_float(__float_as_uint(__int2float_rn((int)w)) + eadd);
+    }
+  }
+  return true;
+}
+
 // One lane's replay of its 16 elements (the first cnt - b of them when not
 // FULL): running total t from the lane's prefix, a conversion after every
 // element, results written back over the staged inputs.  The common paths
@@ -1048,6 +1280,7 @@ __device__ __forceinline__ void cf_replay_lanes(T* buf, int sb, int b, int cnt, 
     // usual case); otherwise 192.
     const uint64_t sx = (uint64_t)((int64_t)t.w1 >> 63);
     if (t.w2 == sx && ((int64_t)t.w1 >> 62) == ((int64_t)t.w1 >> 63)) {
+      if (cf_lane_window_f64(buf, sb, b, FULL ? 512 : cnt, t.w0, t.w1, kc, bf)) return;
       uint64_t t0 = t.w0, t1 = t.w1;
 #pragma unroll 8
       for (int i = 0; i < 16; ++i) {
@@ -1074,7 +1307,7 @@ __device__ __forceinline__ void cf_replay_lanes(T* buf, int sb, int b, int cnt, 
           t0 = ((uint64_t)r1 << 32) | r0;
           t1 = ((uint64_t)r3 << 32) | r2;
           double r;
-          if (!t128_to_double_normal(t0, t1, bf, &r)) r = round_t192_d((int64_t)t1 >> 63, t1, t0, bf);
+          if (!t128_to_double_win(t0, t1, bf, &r)) r = round_t192_d((int64_t)t1 >> 63, t1, t0, bf);
           buf[sb + i] = r;
         }
       }
@@ -1098,6 +1331,7 @@ __device__ __forceinline__ void cf_replay_lanes(T* buf, int sb, int b, int cnt, 
     const int64_t a0 = (int64_t)t.w0;
     const uint64_t sx = (uint64_t)(a0 >> 63);
     if (t.w1 == sx && t.w2 == sx && (a0 >> 62) == (a0 >> 63)) {
+      if (cf_lane_window_f32(buf, sb, b, FULL ? 512 : cnt, a0, fk, bf)) return;
       uint32_t lo = (uint32_t)t.w0, hi = (uint32_t)(t.w0 >> 32);
 #pragma unroll 8
       for (int i = 0; i < 16; ++i) {
@@ -1113,9 +1347,8 @@ __device__ __forceinline__ void cf_replay_lanes(T* buf, int sb, int b, int cnt, 
               "addc.u32 %1, %1, %4;\n\t}"
               : "+r"(lo), "+r"(hi)
               : "r"(sm & 1u), "r"(rl ^ sm), "r"(rh ^ sm));
-          const int64_t a = (int64_t)(((uint64_t)hi << 32) | lo);
           uint32_t fb;
-          if (!fx::i64_to_float_normal(a, bf, &fb))
+          if (!i64_to_float_win(lo, hi, bf, &fb))
             fb = __float_as_uint(fx::i96_to_float(fx::I96{lo, hi, (uint32_t)((int32_t)hi >> 31)}, bf));
           buf[sb + i] = __uint_as_float(fb);
         }
