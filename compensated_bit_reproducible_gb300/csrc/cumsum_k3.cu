@@ -878,24 +878,29 @@ __device__ __forceinline__ void cf_stage(T* buf, const T* g, int cnt, int lane) 
 }
 
 // Double totals: each thread deposits its elements' rounded values into
-// 64-bit word cells in shared memory (cell k + 8 s: word position k of
-// M' 2^u for the sign s, the rounding of the binned sum's fixed-index
-// deposit).  The value of the cells is
-// sum_s (-1)^s sum_{k = 2..6} cell 2^(32 (k - 2)) in units of g_f
-// (positions 0, 1 lie below the grid and are never read; 7 only beyond the
-// guessed bin, which fails the guess); a lane takes that value after its 16
-// elements and clears the cells it read.
-constexpr int CT_CELLS = 16;
+// 64-bit cells in shared memory.  An element's value M' 2^u (the rounding
+// of the binned sum's fixed-index deposit) is three 32-bit words w0, w1, w2
+// at word positions c, c + 1, c + 2 (c = u >> 5; positions 0 and 1 lie
+// below the grid and are dropped).  w0 goes to an A cell (positions 2..4)
+// and the pair (w2:w1), below 2^54, to one P cell as a 64-bit value at
+// position c + 1 (positions 2..5): two cell updates per element instead of
+// three, the shared-memory traffic that binds this pass.  For c < 2 the
+// dropped words are zeroed first (c = 0: only w2 remains, as the low word
+// of P at position 2).  Those selects are multiply-adds by 0/1 flags, which
+// run on the multiply-add pipe.  Per sign there are 7 cells (A 2..4, P 2..5);
+// a lane takes their value after its 16 elements and clears them.
+constexpr int CT_CELLS = 14;
 template <typename T>
 __host__ __device__ constexpr int ct_cell_bytes() {
   return sizeof(T) == 8 ? CT_CELLS * C3_BLOCK * 8 : 0;
 }
 
-__device__ __forceinline__ void ct_deposit(uint32_t hi, uint32_t lo, const fx::FxConst& k, uint32_t c8, uint64_t* A) {
+__device__ __forceinline__ void ct_deposit(uint32_t hi, uint32_t lo, const fx::FxConst& k, uint32_t c7, uint64_t* A) {
   const uint32_t eb = fx::mad32(hi, k.one + k.one, 0u) >> 21;   // biased exponent
   const int us = (int)fx::mad32(eb, k.one, k.Cp);               // shift of M
   const uint32_t u = (uint32_t)max(us, 0);
-  const uint32_t c = min(u >> 5, 5u);
+  // beyond the guessed bin (which fails the guess) c is kept in bounds
+  const uint32_t c = min(u >> 5, 4u);
   const uint32_t mh = (hi & 0xFFFFFu) | 0x100000u;
   const uint32_t hl = fx::shl_clamp32(1u, (int)fx::mad32(u, k.negone, k.c63));
   const uint32_t hh = fx::shl_clamp32(1u, (int)fx::mad32(u, k.negone, k.c31));
@@ -905,32 +910,47 @@ __device__ __forceinline__ void ct_deposit(uint32_t hi, uint32_t lo, const fx::F
   const uint32_t w0 = fx::funnel_l(0u, lo2, u);
   const uint32_t w1 = fx::funnel_l(lo2, mh2, u);
   const uint32_t w2 = fx::funnel_l(mh2, 0u, u);
-  uint64_t* p = A + fx::mad32(fx::mad32(hi >> 31, c8, c), (uint32_t)C3_BLOCK, 0u);
-  p[0] = fx::madw(w0, k.one, p[0]);
-  p[C3_BLOCK] = fx::madw(w1, k.one, p[C3_BLOCK]);
-  p[2 * C3_BLOCK] = fx::madw(w2, k.one, p[2 * C3_BLOCK]);
+  const uint32_t c2 = fx::mad32(c, k.one, 2u);
+  const uint32_t f2 = fx::mad32(c, k.one, 126u) >> 7;   // c >= 2
+  const uint32_t f1 = fx::mad32(c, k.one, 127u) >> 7;   // c >= 1
+  const uint32_t w0m = fx::mad32(w0, f2, 0u);
+  const uint32_t apos = fx::mad32(f2, 0xFFFFFFFEu, c2);  // c (w0 zero when c < 2: any position)
+  const uint32_t plo = fx::mad32(f1, w1 - w2, w2);      // c >= 1: w1, else w2
+  const uint32_t phi = fx::mad32(w2, f1, 0u);           // c >= 1: w2, else 0
+  const uint32_t ppos = fx::mad32(f1, 0xFFFFFFFFu, c2);  // c + 1, or 2 when c = 0
+  const uint32_t sb = fx::mad32(hi >> 31, c7, 0u);
+  uint64_t* pa = A + fx::mad32(sb + apos - 2u, (uint32_t)C3_BLOCK, 0u);
+  uint64_t* pp = A + fx::mad32(sb + ppos + 1u, (uint32_t)C3_BLOCK, 0u);
+  *pa = fx::madw(w0m, k.one, *pa);
+  const uint64_t t = fx::madw(plo, k.one, *pp);
+  *pp = ((uint64_t)fx::mad32(phi, k.one, (uint32_t)(t >> 32)) << 32) | (uint32_t)t;
 }
 
 // The value of the thread's cells, which are then cleared: the sum of the
 // rounded values deposited since the last call.  Per word position the two
-// signs' cells subtract to a 64-bit d_w (each cell sums at most 16 words
-// between calls), and the five d_w combine at their 32-bit offsets.
+// signs' cells subtract to a 64-bit d_w (a P cell sums at most 16 values
+// below 2^54 between calls), and the four d_w combine at their 32-bit
+// offsets.
 __device__ __forceinline__ fx::I192 ct_take(uint64_t* A) {
-  int64_t d[5];
+  int64_t d[4];
 #pragma unroll
-  for (int w = 2; w < 7; ++w) {
-    const uint64_t pos = A[w * C3_BLOCK], neg = A[(w + 8) * C3_BLOCK];
-    A[w * C3_BLOCK] = 0;
+  for (int w = 2; w < 6; ++w) {
+    uint64_t pos = A[(w + 1) * C3_BLOCK], neg = A[(w + 8) * C3_BLOCK];   // P cells
+    A[(w + 1) * C3_BLOCK] = 0;
     A[(w + 8) * C3_BLOCK] = 0;
+    if (w <= 4) {   // A cells
+      pos += A[(w - 2) * C3_BLOCK];
+      neg += A[(w + 5) * C3_BLOCK];
+      A[(w - 2) * C3_BLOCK] = 0;
+      A[(w + 5) * C3_BLOCK] = 0;
+    }
     d[w - 2] = (int64_t)(pos - neg);
   }
-  const uint64_t x0 = (uint64_t)(d[0] >> 63), x1 = (uint64_t)(d[1] >> 63), x2 = (uint64_t)(d[2] >> 63),
-                 x3 = (uint64_t)(d[3] >> 63);
+  const uint64_t x0 = (uint64_t)(d[0] >> 63), x1 = (uint64_t)(d[1] >> 63), x2 = (uint64_t)(d[2] >> 63);
   fx::I192 t{(uint64_t)d[0], x0, x0};
   t = fx::i192_add(t, fx::I192{(uint64_t)d[1] << 32, (uint64_t)(d[1] >> 32), x1});
   t = fx::i192_add(t, fx::I192{0, (uint64_t)d[2], x2});
   t = fx::i192_add(t, fx::I192{0, (uint64_t)d[3] << 32, (uint64_t)(d[3] >> 32)});
-  t.w2 += (uint64_t)d[4];
   return t;
 }
 
@@ -973,7 +993,7 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
     if (L < facc.I) facc.raise(L);
   }
   uint64_t* A = (uint64_t*)ct_smem + threadIdx.x;   // double: this thread's cells
-  const uint32_t c8 = 8u * one;
+  const uint32_t c7 = 7u * one;
   if constexpr (sizeof(T) == 8) {
 #pragma unroll
     for (int k = 0; k < CT_CELLS; ++k) A[k * C3_BLOCK] = 0;
@@ -1016,7 +1036,7 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
       // padding elements are zero and deposit nothing
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        ct_deposit((uint32_t)__double2hiint(v[i]), (uint32_t)__double2loint(v[i]), kc, c8, A);
+        ct_deposit((uint32_t)__double2hiint(v[i]), (uint32_t)__double2loint(v[i]), kc, c7, A);
       const fx::I192 own = ct_take(A);
       const fx::I192 exc = i192_warp_exclusive(own, &tot);
       const size_t plane = (size_t)nch * 32;
