@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librepro_gb300.so")
-SOURCES = ["api.cu", "adn_sum.cu", "sum_f64_fixed.cu", "adn_cumsum.cu", "cumsum_k3.cu", "var.cu", "compare.cu",
+SOURCES = ["api.cu", "adn_sum.cu", "sum_f64_fixed.cu", "adn_cumsum.cu", "cumsum_k3.cu", "cumsum_fx.cu", "var.cu", "compare.cu",
            "noalloc.cu"]
 HEADERS = ["adn.cuh", "accum.cuh", "fixed_index.cuh", "f32x2.cuh", "launch.h"]
 

@@ -299,29 +299,44 @@ __device__ __forceinline__ void rs_deposit(RS<K>& s, Digits<T, K>& dg, T x) {
   for (int k = 0; k < K; ++k) s.F[k] = w_add(s.F[k], w_from(a[k]));
 }
 
+// A gate (when not null) makes a kernel a fallback that runs only when the
+// fast path before it asked for it: the kernel may start early (programmatic
+// stream serialization) and waits for that grid before it reads the gate.
+__device__ __forceinline__ bool cs_gated_off(const unsigned* gate) {
+  if (!gate) return false;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  return *gate == 0u;
+}
+
 template <typename T, int KT>
 __global__ void __launch_bounds__(CS_BLOCK) cumsum_fast_reduce(const T* __restrict__ in, int64_t n, int K,
-                                                               unsigned char* __restrict__ tstate) {
+                                                               unsigned char* __restrict__ tstate,
+                                                               const unsigned* gate) {
   typedef typename AccOf<T, KT>::type Acc;
-  int64_t base = (int64_t)blockIdx.x * CS_TILE;
-  int64_t cnt = min((int64_t)CS_TILE, n - base);
-  Acc acc;
-  acc.init(K);
-  const T* p = in + base;
-  for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
-    T v[1] = {p[i]};
-    acc.template chunk<1>(v);
+  if (cs_gated_off(gate)) return;
+  const int64_t nt = (n + CS_TILE - 1) / CS_TILE;
+  for (int64_t tile = blockIdx.x; tile < nt; tile += gridDim.x) {
+    int64_t base = tile * CS_TILE;
+    int64_t cnt = min((int64_t)CS_TILE, n - base);
+    Acc acc;
+    acc.init(K);
+    const T* p = in + base;
+    for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+      T v[1] = {p[i]};
+      acc.template chunk<1>(v);
+    }
+    acc.finish();
+    State<KT> st;
+    block_merge<KT>(acc.I, acc.flags, acc.L, K, &st);
+    if (threadIdx.x == 0) store_partial<KT>(tstate, (int)tile, K, st);
   }
-  acc.finish();
-  State<KT> st;
-  block_merge<KT>(acc.I, acc.flags, acc.L, K, &st);
-  if (threadIdx.x == 0) store_partial<KT>(tstate, blockIdx.x, K, st);
 }
 
 template <typename T, int KT>
 __global__ void __launch_bounds__(1024) cumsum_fast_scan(const unsigned char* __restrict__ tstate, int64_t ntiles,
-                                                         unsigned char* __restrict__ tpref) {
+                                                         unsigned char* __restrict__ tpref, const unsigned* gate) {
   __shared__ RS<KT> sm[32];
+  if (cs_gated_off(gate)) return;
   const int I0 = Geom<T>::NB - KT;
   const size_t st = 16 + 16 * (size_t)KT;
   int64_t per = (ntiles + blockDim.x - 1) / blockDim.x;
@@ -349,8 +364,9 @@ constexpr int CS_SEG = 256;
 template <typename T, int KT>
 __global__ void __launch_bounds__(CS_SEG) cumsum_seg_scan(const unsigned char* __restrict__ tstate, int64_t ntiles,
                                                           unsigned char* __restrict__ tpref,
-                                                          unsigned char* __restrict__ segtot) {
+                                                          unsigned char* __restrict__ segtot, const unsigned* gate) {
   __shared__ RS<KT> sm[32];
+  if (cs_gated_off(gate)) return;
   const int I0 = Geom<T>::NB - KT;
   const size_t st = 16 + 16 * (size_t)KT;
   const int64_t t = (int64_t)blockIdx.x * CS_SEG + threadIdx.x;
@@ -366,13 +382,11 @@ __global__ void __launch_bounds__(CS_SEG) cumsum_seg_scan(const unsigned char* _
 }
 
 template <typename T, int KT>
-__global__ void __launch_bounds__(CS_BLOCK) cumsum_fast_replay(const T* in, T* out, int64_t n,
-                                                               const unsigned char* __restrict__ tpref,
-                                                               const unsigned char* __restrict__ segpref) {
-  __shared__ T sm[CS_TILE + CS_TILE / CS_ITEMS];
-  __shared__ RS<KT> wsm[CS_BLOCK / 32];
+__device__ __forceinline__ void cumsum_replay_tile(const T* in, T* out, int64_t n, int64_t tile,
+                                                   const unsigned char* __restrict__ tpref,
+                                                   const unsigned char* __restrict__ segpref, T* sm, RS<KT>* wsm) {
   const int I0 = Geom<T>::NB - KT;
-  int cnt = load_tile<T>(in, n, blockIdx.x, sm);
+  int cnt = load_tile<T>(in, n, tile, sm);
   const int b = threadIdx.x * CS_ITEMS;
   const int sb = b + threadIdx.x;    // padded position of this thread's first element
   // this thread's own total, then its incoming state
@@ -387,8 +401,8 @@ __global__ void __launch_bounds__(CS_BLOCK) cumsum_fast_replay(const T* in, T* o
   }
   RS<KT> run = rs_block_exclusive<KT>(mine, I0, wsm);
   RS<KT> s, sp;
-  rs_load(s, tpref + (size_t)blockIdx.x * (16 + 16 * (size_t)KT));
-  rs_load(sp, segpref + (size_t)(blockIdx.x / CS_SEG) * (16 + 16 * (size_t)KT));
+  rs_load(s, tpref + (size_t)tile * (16 + 16 * (size_t)KT));
+  rs_load(sp, segpref + (size_t)(tile / CS_SEG) * (16 + 16 * (size_t)KT));
   rs_merge(s, sp);
   rs_merge(s, run);
   Digits<T, KT> dg;
@@ -401,9 +415,24 @@ __global__ void __launch_bounds__(CS_BLOCK) cumsum_fast_replay(const T* in, T* o
     }
   }
   __syncthreads();
-  int64_t base = (int64_t)blockIdx.x * CS_TILE;
+  int64_t base = tile * CS_TILE;
   for (int i = threadIdx.x; i < cnt; i += blockDim.x) out[base + i] = sm[i + i / CS_ITEMS];
+  __syncthreads();
 }
+
+template <typename T, int KT>
+__global__ void __launch_bounds__(CS_BLOCK) cumsum_fast_replay(const T* in, T* out, int64_t n,
+                                                               const unsigned char* __restrict__ tpref,
+                                                               const unsigned char* __restrict__ segpref,
+                                                               const unsigned* gate) {
+  __shared__ T sm[CS_TILE + CS_TILE / CS_ITEMS];
+  __shared__ RS<KT> wsm[CS_BLOCK / 32];
+  if (cs_gated_off(gate)) return;
+  const int64_t nt = (n + CS_TILE - 1) / CS_TILE;
+  for (int64_t tile = blockIdx.x; tile < nt; tile += gridDim.x)
+    cumsum_replay_tile<T, KT>(in, out, n, tile, tpref, segpref, sm, wsm);
+}
+
 
 // ------------------------------------------------------------------
 // Run-time K (K > 8): a plain design.  Tile totals come from per-thread int64
@@ -570,13 +599,50 @@ __global__ void cumsum_generic_replay(const T* in, T* out, int64_t n, int K, con
 template <typename T>
 size_t cumsum_workspace_bytes(int64_t n, int K) {
   if (K == 3) return cumsum_k3_workspace_bytes<T>(n);
+  if (sizeof(T) == 8 && K >= 4 && K <= 6) return cumsum_fx_workspace_bytes(n, K);
   int64_t nt = (n + CS_TILE - 1) / CS_TILE;
   int64_t nseg = (nt + CS_SEG - 1) / CS_SEG;
   return 2 * (size_t)(nt + nseg) * (16 + 16 * (size_t)K) + 64;   // tile and segment states and prefixes
 }
 
+template <typename Kn, typename... A>
+static cudaError_t cs_launch(Kn kernel, int64_t grid, int block, cudaStream_t s, bool pdl, A... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+static int cs_sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 1;
+  }
+  if (!cached[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) {
+      cudaGetLastError();
+      v = 1;
+    }
+    cached[dev] = v;
+  }
+  return cached[dev];
+}
+
+// gate: null, or a device word that a fast path before these kernels sets
+// to nonzero when they must run (otherwise they return at once; their grids
+// are then kept to a few blocks per SM, each walking several tiles).
 template <typename T, int KT>
-static cudaError_t launch_cumsum_k(const T* in, T* out, int64_t n, int K, unsigned char* ws, cudaStream_t s) {
+static cudaError_t launch_cumsum_k(const T* in, T* out, int64_t n, int K, unsigned char* ws, cudaStream_t s,
+                                   const unsigned* gate = nullptr) {
   int64_t nt = (n + CS_TILE - 1) / CS_TILE;
   int64_t nseg = (nt + CS_SEG - 1) / CS_SEG;
   const size_t st = 16 + 16 * (size_t)K;
@@ -584,11 +650,38 @@ static cudaError_t launch_cumsum_k(const T* in, T* out, int64_t n, int K, unsign
   unsigned char* tpref = tstate + (size_t)nt * st;
   unsigned char* segtot = tpref + (size_t)nt * st;
   unsigned char* segpref = segtot + (size_t)nseg * st;
-  cumsum_fast_reduce<T, KT><<<(unsigned)nt, CS_BLOCK, 0, s>>>(in, n, K, tstate);
-  cumsum_seg_scan<T, KT><<<(unsigned)nseg, CS_SEG, 0, s>>>(tstate, nt, tpref, segtot);
-  cumsum_fast_scan<T, KT><<<1, 1024, 0, s>>>(segtot, nseg, segpref);
-  cumsum_fast_replay<T, KT><<<(unsigned)nt, CS_BLOCK, 0, s>>>(in, out, n, tpref, segpref);
-  return cudaGetLastError();
+  const bool pdl = gate != nullptr;
+  const int64_t grid = pdl ? min(nt, (int64_t)4 * cs_sm_count()) : nt;
+  cudaError_t e;
+  if ((e = cs_launch(cumsum_fast_reduce<T, KT>, grid, CS_BLOCK, s, pdl, in, n, K, tstate, gate)) != cudaSuccess)
+    return e;
+  if ((e = cs_launch(cumsum_seg_scan<T, KT>, nseg, CS_SEG, s, pdl, (const unsigned char*)tstate, nt, tpref, segtot,
+                     gate)) != cudaSuccess)
+    return e;
+  if ((e = cs_launch(cumsum_fast_scan<T, KT>, 1, 1024, s, pdl, (const unsigned char*)segtot, nseg, segpref,
+                     gate)) != cudaSuccess)
+    return e;
+  return cs_launch(cumsum_fast_replay<T, KT>, grid, CS_BLOCK, s, pdl, in, out, n, (const unsigned char*)tpref,
+                   (const unsigned char*)segpref, gate);
+}
+
+template <typename T>
+cudaError_t launch_cumsum_general(const T* in, T* out, int64_t n, int K, unsigned char* ws, cudaStream_t s,
+                                  const unsigned* gate) {
+  switch (K) {
+    case 4: return launch_cumsum_k<T, 4>(in, out, n, K, ws, s, gate);
+    case 5: return launch_cumsum_k<T, 5>(in, out, n, K, ws, s, gate);
+    case 6: return launch_cumsum_k<T, 6>(in, out, n, K, ws, s, gate);
+    default: return cudaErrorInvalidValue;
+  }
+}
+template cudaError_t launch_cumsum_general<double>(const double*, double*, int64_t, int, unsigned char*,
+                                                   cudaStream_t, const unsigned*);
+
+size_t cumsum_general_bytes(int64_t n, int K) {
+  int64_t nt = (n + CS_TILE - 1) / CS_TILE;
+  int64_t nseg = (nt + CS_SEG - 1) / CS_SEG;
+  return 2 * (size_t)(nt + nseg) * (16 + 16 * (size_t)K) + 64;   // tile and segment states and prefixes
 }
 
 template <typename T>
@@ -608,9 +701,13 @@ cudaError_t launch_cumsum(const T* in, T* out, int64_t n, int K, unsigned char* 
   switch (K) {
     case 2: return launch_cumsum_k<T, 2>(in, out, n, K, ws, s);
     case 3: return launch_cumsum_k3<T>(in, out, n, ws, s);
-    case 4: return launch_cumsum_k<T, 4>(in, out, n, K, ws, s);
-    case 5: return launch_cumsum_k<T, 5>(in, out, n, K, ws, s);
-    case 6: return launch_cumsum_k<T, 6>(in, out, n, K, ws, s);
+    case 4:
+    case 5:
+    case 6:
+      if constexpr (sizeof(T) == 8) return launch_cumsum_fx(in, out, n, K, ws, s);
+      else if (K == 4) return launch_cumsum_k<T, 4>(in, out, n, K, ws, s);
+      else if (K == 5) return launch_cumsum_k<T, 5>(in, out, n, K, ws, s);
+      else return launch_cumsum_k<T, 6>(in, out, n, K, ws, s);
     case 7: return launch_cumsum_k<T, 7>(in, out, n, K, ws, s);
     case 8: return launch_cumsum_k<T, 8>(in, out, n, K, ws, s);
     default: return launch_cumsum_generic<T>(in, out, n, K, ws, s);

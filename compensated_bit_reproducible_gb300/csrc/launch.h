@@ -44,6 +44,16 @@ template <typename T>
 size_t cumsum_workspace_bytes(int64_t n, int K);
 template <typename T>
 cudaError_t launch_cumsum(const T* in, T* out, int64_t n, int K, unsigned char* ws, int block, cudaStream_t s);
+// The general per-fold kernels for K = 4..6 on doubles, optionally gated (see
+// adn_cumsum.cu), and their workspace.
+template <typename T>
+cudaError_t launch_cumsum_general(const T* in, T* out, int64_t n, int K, unsigned char* ws, cudaStream_t s,
+                                  const unsigned* gate);
+size_t cumsum_general_bytes(int64_t n, int K);
+// Doubles with K = 4..6 (cumsum_fx.cu): the fixed-index path for long inputs,
+// the general kernels otherwise.
+size_t cumsum_fx_workspace_bytes(int64_t n, int K);
+cudaError_t launch_cumsum_fx(const double* in, double* out, int64_t n, int K, unsigned char* ws, cudaStream_t s);
 template <typename T>
 size_t cumsum_k3_workspace_bytes(int64_t n);
 template <typename T>

@@ -1,6 +1,7 @@
-"""K = 3 cumulative sum for n >= 2^17: the fixed-index fast path (first tile
-replayed per fold when the prefix index is still settling there), and the
-general kernels as its fallback.  Every prefix must equal the oracle's."""
+"""Cumulative sums for n >= 2^17 on the fixed-index fast paths (K = 3 for
+both types; K = 4..6 for double), with the first tile recomputed per fold
+when the prefix index is still settling there, and the general kernels as
+their fallback.  Every prefix must equal the oracle's."""
 import numpy as np
 import pytest
 
@@ -13,18 +14,23 @@ F32, F64 = np.float32, np.float64
 N = 200_003   # above the fast-path threshold; odd, so the last tile is partial
 
 
-def cumsum(x, inplace=False, offset=0):
+# (type, K): both K = 3 paths and the K = 4..6 double path
+CASES = [(F32, 3), (F64, 3), (F64, 4), (F64, 6)]
+CASE_IDS = ["f32-K3", "f64-K3", "f64-K4", "f64-K6"]
+
+
+def cumsum(x, inplace=False, offset=0, K=3):
     t = to_dev(x)
     if offset:
         t = t[offset:]
-    r = api.repro_cumsum(t, out=t if inplace else None, K=3)
+    r = api.repro_cumsum(t, out=t if inplace else None, K=K)
     return r.cpu().numpy()
 
 
-def check(x, **kw):
+def check(x, K=3, **kw):
     off = kw.get("offset", 0)
-    got = cumsum(x, **kw)
-    want = oracle.adn_cumsum(x[off:], 3)
+    got = cumsum(x, K=K, **kw)
+    want = oracle.adn_cumsum(x[off:], K)
     assert same_bits(got, want), first_diff(got, want)
 
 
@@ -32,17 +38,17 @@ def base(dt, seed):
     return inputs.wide_f64(N, seed=seed) if dt == F64 else inputs.normal_f32(N, seed=seed, spikes=True)
 
 
-@pytest.mark.parametrize("dt", [F32, F64])
-def test_typical_and_ties(dt):
+@pytest.mark.parametrize("dt,K", CASES, ids=CASE_IDS)
+def test_typical_and_ties(dt, K):
     dev()
-    check(base(dt, 21))
+    check(base(dt, 21), K)
     from tests.test_oracle import tie_heavy
-    check(tie_heavy(dt, N, 22))
+    check(tie_heavy(dt, N, 22, K=K), K)
 
 
-@pytest.mark.parametrize("dt", [F32, F64])
+@pytest.mark.parametrize("dt,K", CASES, ids=CASE_IDS)
 @pytest.mark.parametrize("first", [0, 1, 4000, 4095, 4096, 9000, N // 2])
-def test_where_the_index_settles(dt, first):
+def test_where_the_index_settles(dt, K, first):
     """Everything before `first` is scaled far down, so the prefix index
     settles there: in the first tile (per-fold replay of that tile), at
     position 0 (all fast), or later (the general path)."""
@@ -51,67 +57,70 @@ def test_where_the_index_settles(dt, first):
     x[:first] *= dt(1e-9) if dt == F32 else 1e-30
     big = np.argmax(np.abs(x))
     x[first], x[big] = x[big], x[first]   # the maximum sits at `first`
-    check(x)
+    check(x, K)
 
 
-@pytest.mark.parametrize("dt", [F32, F64])
+@pytest.mark.parametrize("dt,K", CASES, ids=CASE_IDS)
 @pytest.mark.parametrize("pos", [3, 5000, N - 1])
-def test_outlier_outside_the_guessed_bin(dt, pos):
+def test_outlier_outside_the_guessed_bin(dt, K, pos):
     dev()
     x = base(dt, 24).copy()
     x[pos] = dt(3e30) if dt == F32 else 3e200
-    check(x)
+    check(x, K)
 
 
-@pytest.mark.parametrize("dt", [F32, F64])
-def test_specials_zeros_subnormals(dt):
+@pytest.mark.parametrize("dt,K", CASES, ids=CASE_IDS)
+def test_specials_zeros_subnormals(dt, K):
     dev()
     b = base(dt, 25)
     for kind in ("nan", "pinf", "pninf"):
-        check(inputs.inject_specials(b, kind, seed=2))
-    check(np.zeros(N, dt))
+        check(inputs.inject_specials(b, kind, seed=2), K)
+    check(np.zeros(N, dt), K)
     m = b.copy()
     m[::3] = 0
     m[1::7] = dt(1e-45) if dt == F32 else 5e-324
-    check(m)
+    check(m, K)
 
 
-@pytest.mark.parametrize("dt", [F32, F64])
-def test_in_place_and_misaligned(dt):
+@pytest.mark.parametrize("dt,K", CASES, ids=CASE_IDS)
+def test_in_place_and_misaligned(dt, K):
     dev()
     x = base(dt, 26)
-    check(x, inplace=True)
+    check(x, K, inplace=True)
     for off in (1, 3):
-        check(x, offset=off)
+        check(x, K, offset=off)
 
 
 @pytest.mark.parametrize("n", [(1 << 17) - 1, 1 << 17, (1 << 17) + 1, 4096 * 40])
-@pytest.mark.parametrize("dt", [F32, F64])
-def test_threshold_sizes(n, dt):
+@pytest.mark.parametrize("dt,K", CASES, ids=CASE_IDS)
+def test_threshold_sizes(n, dt, K):
     dev()
     x = inputs.wide_f64(n, seed=n).astype(dt)
-    check(x)
+    check(x, K)
 
 
-def test_cancellation_f64():
+@pytest.mark.parametrize("K", [3, 4, 6])
+def test_cancellation_f64(K):
+    """Every prefix of the second half cancels toward zero: lanes whose
+    window cannot hold their prefixes take the exact conversion."""
     dev()
     a = inputs.wide_f64(N // 2, seed=27)
-    check(np.concatenate([a, -a[::-1], [1.0]]))
+    check(np.concatenate([a, -a[::-1], [1.0]]), K)
 
 
-@pytest.mark.parametrize("dt", [F32, F64])
-def test_many_chunks_in_and_out_of_place_repeatable(dt):
+@pytest.mark.parametrize("dt,K", CASES, ids=CASE_IDS)
+def test_many_chunks_in_and_out_of_place_repeatable(dt, K):
     """About 2000 chunks (two levels of the chunk scan): out of place equal
     to the oracle, in place equal to it, and repeats bit for bit."""
     dev()
     n = 1_000_003
     x = inputs.wide_f64(n, seed=31).astype(dt) if dt == F64 else inputs.normal_f32(n, seed=31, spikes=True)
-    want = oracle.adn_cumsum(x, 3)
-    got = cumsum(x)
+    want = oracle.adn_cumsum(x, K)
+    got = cumsum(x, K=K)
     assert same_bits(got, want), first_diff(got, want)
-    assert same_bits(cumsum(x, inplace=True), want)
+    assert same_bits(cumsum(x, inplace=True, K=K), want)
     for _ in range(3):
-        assert same_bits(cumsum(x), got)
+        assert same_bits(cumsum(x, K=K), got)
 
 
 def test_float_totals_beyond_64_bits():
@@ -142,3 +151,18 @@ def test_double_totals_beyond_128_bits():
     x = np.where((i // 1000) % 2 == 0, v, -v)
     x[::13] *= 0.75
     check(x)
+
+
+@pytest.mark.parametrize("K", [4, 5, 6])
+def test_wide_folds_magnitudes(K):
+    """K = 4..6: values spread over the whole width of the folds (rounded
+    values up to 2^(10 + 40 (K - 1)) grid units, down to ties on the finest
+    grid), with runs that push the running total up and back."""
+    dev()
+    from tests.test_oracle import tie_heavy
+    x = tie_heavy(F64, N, 40 + K, K=K)
+    rng = np.random.default_rng(K)
+    x[rng.integers(0, N, 500)] *= 2.0 ** 40
+    check(x, K)
+    runs = np.repeat(np.where(np.arange(N // 997 + 1) % 2 == 0, 1.0, -1.0), 997)[:N]
+    check(base(F64, 41) * runs * 1e10, K)
