@@ -73,6 +73,7 @@ def lib():
             sig["repro_state_deposit_" + t] = (I, [P, P, S, I, P])
             sig["repro_state_merge_" + t] = (I, [P, P, I, P])
             sig["repro_state_finalize_" + t] = (I, [P, I, P, P])
+            sig["repro_cumsum_from_state_" + t] = (I, [P, P, S, I, P, P])
         for mode in ("naive", "pairwise", "kahan", "neumaier"):
             for t in ("f32", "f64"):
                 sig["repro_sum_%s_%s" % (mode, t)] = (I, [P, S, P, P])
@@ -286,4 +287,19 @@ def state_finalize(state: torch.Tensor, dtype, K: int = 3, out: torch.Tensor | N
         out = torch.empty(1, dtype=dtype, device=state.device)
     _check(getattr(lib(), "repro_state_finalize_" + sfx)(_ptr(state), K, _ptr(out), _stream(stream)),
            "repro_state_finalize_" + sfx)
+    return out
+
+
+def repro_cumsum_from_state(x: torch.Tensor, state: torch.Tensor, K: int = 3, out: torch.Tensor | None = None,
+                            stream=None) -> torch.Tensor:
+    """Binned cumulative sum of x that starts from a binned state: out[i]
+    is the binned sum of the state's contents and x[0..i].  Device tensors
+    only; out may be x itself."""
+    sfx = _sfx(x)
+    assert x.is_contiguous() and state.dtype == torch.uint8
+    if out is None:
+        out = torch.empty_like(x)
+    assert out.dtype == x.dtype and out.is_contiguous() and out.numel() == x.numel()
+    _check(getattr(lib(), "repro_cumsum_from_state_" + sfx)(_ptr(x), _ptr(out), x.numel(), K, _ptr(state),
+                                                            _stream(stream)), "repro_cumsum_from_state_" + sfx)
     return out

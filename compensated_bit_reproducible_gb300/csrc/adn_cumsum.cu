@@ -332,9 +332,30 @@ __global__ void __launch_bounds__(CS_BLOCK) cumsum_fast_reduce(const T* __restri
   }
 }
 
+// carry: null, or a binned state in the repro_state layout (32-byte header
+// {index, flags, K, type}, then K 128-bit folds) that every prefix includes;
+// a header that is not a state of this K and type gives the canonical NaN.
+template <typename T>
+__device__ __forceinline__ int carry_flags(const unsigned char* p, int K) {
+  const int* h = (const int*)p;
+  return h[1] | ((h[2] != K || h[3] != (sizeof(T) == 8 ? 2 : 1)) ? FL_NAN : 0);
+}
+
+template <typename T, int KT>
+__device__ __forceinline__ void rs_from_carry(RS<KT>& s, const unsigned char* p) {
+  rs_zero(s, Geom<T>::NB - KT);
+  s.flags = carry_flags<T>(p, KT);
+  if (s.flags & FL_NAN) return;   // no fold is read from a state of another K or type
+  s.I = ((const int*)p)[0];
+  const int64_t* F = (const int64_t*)(p + 32);
+#pragma unroll
+  for (int k = 0; k < KT; ++k) s.F[k] = W128{(uint64_t)F[2 * k], F[2 * k + 1]};
+}
+
 template <typename T, int KT>
 __global__ void __launch_bounds__(1024) cumsum_fast_scan(const unsigned char* __restrict__ tstate, int64_t ntiles,
-                                                         unsigned char* __restrict__ tpref, const unsigned* gate) {
+                                                         unsigned char* __restrict__ tpref, const unsigned* gate,
+                                                         const unsigned char* __restrict__ carry) {
   __shared__ RS<KT> sm[32];
   if (cs_gated_off(gate)) return;
   const int I0 = Geom<T>::NB - KT;
@@ -348,6 +369,11 @@ __global__ void __launch_bounds__(1024) cumsum_fast_scan(const unsigned char* __
     rs_merge(agg, x);
   }
   RS<KT> run = rs_block_exclusive<KT>(agg, I0, sm);
+  if (carry) {
+    RS<KT> c;
+    rs_from_carry<T, KT>(c, carry);
+    rs_merge(run, c);
+  }
   for (int64_t t = b; t < e; ++t) {
     rs_store(run, tpref + (size_t)t * st);
     rs_load(x, tstate + (size_t)t * st);
@@ -570,11 +596,25 @@ __global__ void __launch_bounds__(CS_BLOCK) cumsum_generic_reduce(const T* __res
 
 template <typename T>
 __global__ void cumsum_generic_scan(const unsigned char* __restrict__ tstate, int64_t ntiles, int K,
-                                    unsigned char* __restrict__ tpref) {
+                                    unsigned char* __restrict__ tpref, const unsigned char* __restrict__ carry) {
   __shared__ GState<T> s;
   if (threadIdx.x != 0) return;
   const size_t st = 16 + 16 * (size_t)K;
   gs_zero(&s, K);
+  if (carry) {
+    // the carried state, restated in the tile-state layout (header, folds)
+    const int fl = carry_flags<T>(carry, K);
+    if (fl & FL_NAN) {
+      s.flags |= fl;
+    } else {
+      const int Ic = ((const int*)carry)[0];
+      if (Ic < s.I) gs_raise(&s, Ic, K);
+      s.flags |= fl;
+      const int64_t* F = (const int64_t*)(carry + 32);
+      const int d = Ic - s.I;
+      for (int k = d; k < K; ++k) gs_add(&s, k, W128{(uint64_t)F[2 * (k - d)], F[2 * (k - d) + 1]});
+    }
+  }
   for (int64_t t = 0; t < ntiles; ++t) {
     gs_store(&s, tpref + (size_t)t * st, K);
     gs_merge_stored(&s, tstate + (size_t)t * st, K);
@@ -642,7 +682,7 @@ static int cs_sm_count() {
 // are then kept to a few blocks per SM, each walking several tiles).
 template <typename T, int KT>
 static cudaError_t launch_cumsum_k(const T* in, T* out, int64_t n, int K, unsigned char* ws, cudaStream_t s,
-                                   const unsigned* gate = nullptr) {
+                                   const unsigned* gate = nullptr, const unsigned char* carry = nullptr) {
   int64_t nt = (n + CS_TILE - 1) / CS_TILE;
   int64_t nseg = (nt + CS_SEG - 1) / CS_SEG;
   const size_t st = 16 + 16 * (size_t)K;
@@ -659,7 +699,7 @@ static cudaError_t launch_cumsum_k(const T* in, T* out, int64_t n, int K, unsign
                      gate)) != cudaSuccess)
     return e;
   if ((e = cs_launch(cumsum_fast_scan<T, KT>, 1, 1024, s, pdl, (const unsigned char*)segtot, nseg, segpref,
-                     gate)) != cudaSuccess)
+                     gate, carry)) != cudaSuccess)
     return e;
   return cs_launch(cumsum_fast_replay<T, KT>, grid, CS_BLOCK, s, pdl, in, out, n, (const unsigned char*)tpref,
                    (const unsigned char*)segpref, gate);
@@ -685,39 +725,54 @@ size_t cumsum_general_bytes(int64_t n, int K) {
 }
 
 template <typename T>
-static cudaError_t launch_cumsum_generic(const T* in, T* out, int64_t n, int K, unsigned char* ws, cudaStream_t s) {
+static cudaError_t launch_cumsum_generic(const T* in, T* out, int64_t n, int K, unsigned char* ws, cudaStream_t s,
+                                         const unsigned char* carry) {
   int64_t nt = (n + CS_TILE - 1) / CS_TILE;
   unsigned char* tstate = ws;
   unsigned char* tpref = ws + (size_t)nt * (16 + 16 * (size_t)K);
   cumsum_generic_reduce<T><<<(unsigned)nt, CS_BLOCK, 0, s>>>(in, n, K, tstate);
-  cumsum_generic_scan<T><<<1, 32, 0, s>>>(tstate, nt, K, tpref);
+  cumsum_generic_scan<T><<<1, 32, 0, s>>>(tstate, nt, K, tpref, carry);
   cumsum_generic_replay<T><<<(unsigned)nt, 32, 0, s>>>(in, out, n, K, tpref);
   return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_cumsum(const T* in, T* out, int64_t n, int K, unsigned char* ws, int block, cudaStream_t s) {
+cudaError_t launch_cumsum(const T* in, T* out, int64_t n, int K, unsigned char* ws, int block, cudaStream_t s,
+                          const unsigned char* carry) {
   (void)block;
   switch (K) {
-    case 2: return launch_cumsum_k<T, 2>(in, out, n, K, ws, s);
-    case 3: return launch_cumsum_k3<T>(in, out, n, ws, s);
+    case 2: return launch_cumsum_k<T, 2>(in, out, n, K, ws, s, nullptr, carry);
+    case 3: return launch_cumsum_k3<T>(in, out, n, ws, s, carry);
     case 4:
     case 5:
     case 6:
-      if constexpr (sizeof(T) == 8) return launch_cumsum_fx(in, out, n, K, ws, s);
-      else if (K == 4) return launch_cumsum_k<T, 4>(in, out, n, K, ws, s);
-      else if (K == 5) return launch_cumsum_k<T, 5>(in, out, n, K, ws, s);
-      else return launch_cumsum_k<T, 6>(in, out, n, K, ws, s);
-    case 7: return launch_cumsum_k<T, 7>(in, out, n, K, ws, s);
-    case 8: return launch_cumsum_k<T, 8>(in, out, n, K, ws, s);
-    default: return launch_cumsum_generic<T>(in, out, n, K, ws, s);
+      if constexpr (sizeof(T) == 8) {
+        if (!carry) return launch_cumsum_fx(in, out, n, K, ws, s);
+      }
+      if (K == 4) return launch_cumsum_k<T, 4>(in, out, n, K, ws, s, nullptr, carry);
+      if (K == 5) return launch_cumsum_k<T, 5>(in, out, n, K, ws, s, nullptr, carry);
+      return launch_cumsum_k<T, 6>(in, out, n, K, ws, s, nullptr, carry);
+    case 7: return launch_cumsum_k<T, 7>(in, out, n, K, ws, s, nullptr, carry);
+    case 8: return launch_cumsum_k<T, 8>(in, out, n, K, ws, s, nullptr, carry);
+    default: return launch_cumsum_generic<T>(in, out, n, K, ws, s, carry);
   }
 }
 
+// Workspace of a cumulative sum with a carried state (the general kernels).
+template <typename T>
+size_t cumsum_carry_workspace_bytes(int64_t n, int K) {
+  if (K == 3) return cumsum_k3_general_bytes<T>(n);
+  if (sizeof(T) == 8 && K >= 4 && K <= 6) return cumsum_general_bytes(n, K);
+  return cumsum_workspace_bytes<T>(n, K);
+}
+template size_t cumsum_carry_workspace_bytes<float>(int64_t, int);
+template size_t cumsum_carry_workspace_bytes<double>(int64_t, int);
+
 template size_t cumsum_workspace_bytes<float>(int64_t, int);
 template size_t cumsum_workspace_bytes<double>(int64_t, int);
-template cudaError_t launch_cumsum<float>(const float*, float*, int64_t, int, unsigned char*, int, cudaStream_t);
+template cudaError_t launch_cumsum<float>(const float*, float*, int64_t, int, unsigned char*, int, cudaStream_t,
+                                          const unsigned char*);
 template cudaError_t launch_cumsum<double>(const double*, double*, int64_t, int, unsigned char*, int,
-                                           cudaStream_t);
+                                           cudaStream_t, const unsigned char*);
 
 }  // namespace repro

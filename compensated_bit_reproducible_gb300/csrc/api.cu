@@ -346,6 +346,29 @@ repro_status cumsum_impl(const T* in, T* out, size_t n, int K, cudaStream_t stre
   return REPRO_OK;
 }
 
+// Cumulative sum that starts from a binned state: every prefix includes the
+// state's value ("How It Works": states merge exactly, so a chunked or
+// sharded input scans as one).  Device-accessible pointers only.
+template <typename T>
+repro_status cumsum_from_state_impl(const T* in, T* out, size_t n, int K, const void* state, cudaStream_t stream) {
+  if (K < 2 || K > Lim<T>::MAXK) return REPRO_ERR_INVALID_ARG;
+  if ((uint64_t)n > Lim<T>::COUNT) return REPRO_ERR_CAPACITY;
+  if (!state || ((uintptr_t)state & 15u)) return REPRO_ERR_INVALID_ARG;   // states are 16-byte aligned
+  if (n == 0) return REPRO_OK;
+  if (!in || !out || !aligned(in) || !aligned(out)) return REPRO_ERR_INVALID_ARG;
+  uintptr_t a0 = (uintptr_t)in, a1 = a0 + n * sizeof(T), b0 = (uintptr_t)out, b1 = b0 + n * sizeof(T);
+  if (in != out && a0 < b1 && b0 < a1) return REPRO_ERR_OVERLAP;
+  repro_status st = validate_env(stream);
+  if (st != REPRO_OK) return st;
+  if (is_host_only(in) || is_host_only(out) || is_host_only(state)) return REPRO_ERR_INVALID_ARG;
+  Scratch ws;
+  ws.s = stream;
+  const size_t wsb = cumsum_carry_workspace_bytes<T>((int64_t)n, K);
+  if (wsb) CK(ws_alloc(&ws.p, wsb, stream));
+  CK(launch_cumsum<T>(in, out, (int64_t)n, K, (unsigned char*)ws.p, 0, stream, (const unsigned char*)state));
+  return REPRO_OK;
+}
+
 // Shape checks shared by the variance calls; n must be exact in the element
 // type (2^24 for float32, 2^53 for float64).
 repro_status var_shape_ok(int64_t rows, int64_t cols, int axis, int ddof, int64_t nmax) {
@@ -601,6 +624,14 @@ repro_status repro_state_finalize_f32(const void* state, int K, float* result_de
 }
 repro_status repro_state_finalize_f64(const void* state, int K, double* result_dev, cudaStream_t s) {
   return state_finalize_impl<double>(state, K, result_dev, s);
+}
+repro_status repro_cumsum_from_state_f32(const float* in, float* out, size_t n, int K, const void* state,
+                                         cudaStream_t s) {
+  return cumsum_from_state_impl<float>(in, out, n, K, state, s);
+}
+repro_status repro_cumsum_from_state_f64(const double* in, double* out, size_t n, int K, const void* state,
+                                         cudaStream_t s) {
+  return cumsum_from_state_impl<double>(in, out, n, K, state, s);
 }
 
 }  // extern "C"

@@ -664,8 +664,31 @@ __global__ void __launch_bounds__(1024) c3_scan_tiles(const unsigned char* __res
   }
 }
 
+// carry: null, or a binned state (the repro_state layout: 32-byte header
+// {index, flags, K, type}, then K 128-bit folds) that every prefix includes.
+// A header that is not a K = 3 state of this type gives the canonical NaN.
+template <typename T>
+__device__ __forceinline__ S3 s3_from_carry(const unsigned char* p) {
+  const int4 h = *(const int4*)p;
+  S3 s = s3_zero(Geom<T>::NB - 3);
+  if (h.z != 3 || h.w != (sizeof(T) == 8 ? 2 : 1)) {
+    s.flags = FL_NAN;   // no fold is read from a state of another K or type
+    return s;
+  }
+  s.I = h.x;
+  s.flags = h.y;
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const longlong2 f = *(const longlong2*)(p + 32 + 16 * k);
+    s.F[k] = W128{(uint64_t)f.x, (int64_t)f.y};
+  }
+  return s;
+}
+
+template <typename T>
 __global__ void __launch_bounds__(1024) c3_scan_blocks(unsigned char* __restrict__ btot, int64_t nb, int I0,
-                                                       unsigned char* __restrict__ bpre, const unsigned* gate) {
+                                                       unsigned char* __restrict__ bpre, const unsigned* gate,
+                                                       const unsigned char* __restrict__ carry) {
   __shared__ S3 sm[32];
   if (c3_gated_off(gate)) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -678,6 +701,7 @@ __global__ void __launch_bounds__(1024) c3_scan_blocks(unsigned char* __restrict
   if (lane == 31) sm[warp] = inc;
   __syncthreads();
   S3 run = s3_zero(I0);
+  if (carry) s3_merge(run, s3_from_carry<T>(carry));
   for (int w = 0; w < warp; ++w) s3_merge(run, sm[w]);
   S3 exc = s3_shfl_up(inc, 1);
   if (lane == 0) exc = s3_zero(I0);
@@ -1534,14 +1558,22 @@ static size_t cf_bytes(int64_t n) {
 }
 
 template <typename T>
+size_t cumsum_k3_general_bytes(int64_t n) {
+  return c3_general_bytes<T>(n);
+}
+template size_t cumsum_k3_general_bytes<float>(int64_t);
+template size_t cumsum_k3_general_bytes<double>(int64_t);
+
+template <typename T>
 size_t cumsum_k3_workspace_bytes(int64_t n) {
   if (n <= C3_TILE) return 0;   // one block, no workspace
   return c3_general_bytes<T>(n) + (n >= CF_MIN_N ? cf_bytes<T>(n) : 0);
 }
 
 template <typename T>
-cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, cudaStream_t s) {
-  if (n <= C3_TILE) {
+cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, cudaStream_t s,
+                             const unsigned char* carry) {
+  if (n <= C3_TILE && !carry) {
     c3_single_tile<T><<<1, C3_BLOCK, 0, s>>>(in, out, n);
     return cudaGetLastError();
   }
@@ -1555,7 +1587,7 @@ cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, 
   const unsigned* gate = nullptr;
   int64_t ggrid = nt;
   cudaError_t e;
-  if (n >= CF_MIN_N) {
+  if (n >= CF_MIN_N && !carry) {
     // fixed-index fast path; the general kernels below become its gated fallback
     unsigned char* f = ws + c3_general_bytes<T>(n);
     CsCtl* ctl = (CsCtl*)f;
@@ -1590,14 +1622,17 @@ cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, 
   if ((e = launch_gated(c3_scan_tiles, nb, 1024, 0, s, pdl, (const unsigned char*)wtot, nt, I0, tloc, btot, gate)) !=
       cudaSuccess)
     return e;
-  if ((e = launch_gated(c3_scan_blocks, 1, 1024, 0, s, pdl, btot, nb, I0, bpre, gate)) != cudaSuccess) return e;
+  if ((e = launch_gated(c3_scan_blocks<T>, 1, 1024, 0, s, pdl, btot, nb, I0, bpre, gate, carry)) != cudaSuccess)
+    return e;
   return launch_gated(c3_replay<T>, ggrid, C3_BLOCK, 0, s, pdl, in, out, n, nt, (const unsigned char*)tloc,
                       (const unsigned char*)bpre, gate);
 }
 
 template size_t cumsum_k3_workspace_bytes<float>(int64_t);
 template size_t cumsum_k3_workspace_bytes<double>(int64_t);
-template cudaError_t launch_cumsum_k3<float>(const float*, float*, int64_t, unsigned char*, cudaStream_t);
-template cudaError_t launch_cumsum_k3<double>(const double*, double*, int64_t, unsigned char*, cudaStream_t);
+template cudaError_t launch_cumsum_k3<float>(const float*, float*, int64_t, unsigned char*, cudaStream_t,
+                                             const unsigned char*);
+template cudaError_t launch_cumsum_k3<double>(const double*, double*, int64_t, unsigned char*, cudaStream_t,
+                                              const unsigned char*);
 
 }  // namespace repro

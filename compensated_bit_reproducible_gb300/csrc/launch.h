@@ -42,8 +42,11 @@ cudaError_t launch_segsum(const float* x, int64_t rows, int64_t cols, int axis, 
 // binned cumulative sum
 template <typename T>
 size_t cumsum_workspace_bytes(int64_t n, int K);
+// carry: null, or a device binned state (repro_state layout) that every
+// prefix includes; such calls take the general per-fold kernels.
 template <typename T>
-cudaError_t launch_cumsum(const T* in, T* out, int64_t n, int K, unsigned char* ws, int block, cudaStream_t s);
+cudaError_t launch_cumsum(const T* in, T* out, int64_t n, int K, unsigned char* ws, int block, cudaStream_t s,
+                          const unsigned char* carry = nullptr);
 // The general per-fold kernels for K = 4..6 on doubles, optionally gated (see
 // adn_cumsum.cu), and their workspace.
 template <typename T>
@@ -57,7 +60,12 @@ cudaError_t launch_cumsum_fx(const double* in, double* out, int64_t n, int K, un
 template <typename T>
 size_t cumsum_k3_workspace_bytes(int64_t n);
 template <typename T>
-cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, cudaStream_t s);
+size_t cumsum_k3_general_bytes(int64_t n);
+template <typename T>
+size_t cumsum_carry_workspace_bytes(int64_t n, int K);
+template <typename T>
+cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, cudaStream_t s,
+                             const unsigned char* carry = nullptr);
 
 // variance
 cudaError_t launch_var(const float* x, int64_t rows, int64_t cols, int axis, int ddof, float* out, float* mean,

@@ -155,6 +155,24 @@ repro_status repro_state_merge_f64(void* dst, const void* src, int K, cudaStream
 repro_status repro_state_finalize_f32(const void* state, int K, float* result_dev, cudaStream_t stream);
 repro_status repro_state_finalize_f64(const void* state, int K, double* result_dev, cudaStream_t stream);
 
+/* Cumulative sum that continues from a binned state ("How It Works": the
+   cumulative-sum scan carries binned prefixes; states merge exactly):
+   out[i] = binned sum of (everything deposited into *state) and in[0..i],
+   with the index of that combined prefix, so a shard's cumulative sum that
+   starts from the merged states of all earlier shards equals the
+   corresponding outputs of one cumulative sum over the whole input.  state is
+   a repro_state of the same K and type (another K or type gives the
+   canonical NaN in every output; no fold of it is read); it is only read.
+   in, out and state are device-accessible (device, managed or pinned) memory;
+   in == out is allowed, other overlaps give REPRO_ERR_OVERLAP.  Stream-ordered.
+   These calls run the general per-fold kernels (not the fixed-index paths).
+   Errors: as repro_cumsum, and REPRO_ERR_INVALID_ARG for a null or
+   misaligned state or for plain host memory. */
+repro_status repro_cumsum_from_state_f32(const float* in, float* out, size_t n, int K, const void* state,
+                                         cudaStream_t stream);
+repro_status repro_cumsum_from_state_f64(const double* in, double* out, size_t n, int K, const void* state,
+                                         cudaStream_t stream);
+
 /* ---- binned cumulative sums ("How It Works", cumsum paragraph; "API
    Reference": cumsum) ------------------------------------------------------ */
 /* out[i] = reproducible sum of in[0..i] (each prefix with its own bin

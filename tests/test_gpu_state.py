@@ -141,3 +141,60 @@ def test_state_bytes_through_host_memory(dt):
     b2 = torch.from_numpy(host).to(a.device)
     api.state_merge(a, b2, TD[dt], 3)
     assert same_bits(final(a, dt, 3), oracle.adn_sum(x, 3, "fp"))
+
+
+# ------------------------------------------- cumulative sums from a state
+@pytest.mark.parametrize("dt,K", [(F32, 3), (F64, 3), (F32, 2), (F64, 4), (F64, 6), (F32, 6), (F64, 9)])
+def test_cumsum_from_state_continues_the_whole_scan(dt, K):
+    """A state holding x[:p] and the cumulative sum of x[p:] started from it
+    give the whole input's cumulative sum at positions p.. (prefix indices,
+    raises on either side of the cut, one- and multi-tile shards)."""
+    dev()
+    rng = np.random.default_rng(50 + K)
+    n = 30_011
+    x = data(dt, n, 60 + K).copy()
+    x[:7000] *= dt(1e-12) if dt == F32 else 1e-40   # the index rises after the cut for some p
+    want = oracle.adn_cumsum(x, K)
+    for p in (0, 1, 4096, 6999, 7001, 12_345, n - 1):
+        t = to_dev(x)
+        st = api.state_new(t.dtype, K)
+        if p:
+            api.state_deposit(st, t[:p], K)
+        got = api.repro_cumsum_from_state(t[p:].contiguous(), st, K).cpu().numpy()
+        assert same_bits(got, want[p:]), (p, np.flatnonzero(got.view(np.uint8) != want[p:].view(np.uint8))[:3])
+    # chained over shards: each shard starts from the merged states before it
+    cuts = [0, 3000, 3001, 17_000, n]
+    t = to_dev(x)
+    carry = api.state_new(t.dtype, K)
+    parts = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        parts.append(api.repro_cumsum_from_state(t[a:b].contiguous(), carry, K).cpu().numpy())
+        api.state_deposit(carry, t[a:b], K)
+    assert same_bits(np.concatenate(parts), want)
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
+def test_cumsum_from_state_specials_and_mismatch(dt):
+    dev()
+    x = data(dt, 5000, 71)
+    t = to_dev(x)
+    nan_bits = np.array([np.nan], dt).view(np.uint32 if dt == F32 else np.uint64)[0]
+    # a state holding a NaN makes every output the canonical NaN
+    bad = x[:10].copy()
+    bad[3] = np.nan
+    st = api.state_new(t.dtype, 3)
+    api.state_deposit(st, to_dev(bad), 3)
+    got = api.repro_cumsum_from_state(t, st, 3).cpu().numpy()
+    want = oracle.adn_cumsum(np.concatenate([bad, x]), 3)[10:]
+    assert same_bits(got, want) and np.all(np.isnan(got))
+    # a state of another K gives the canonical NaN, and no fold of it is read
+    st6 = api.state_new(t.dtype, 6)
+    got = api.repro_cumsum_from_state(t, st6, 3).cpu().numpy()
+    canon = 0x7fc00000 if dt == F32 else 0x7ff8000000000000
+    assert np.all(got.view(np.uint32 if dt == F32 else np.uint64) == canon)
+    # in place
+    st = api.state_new(t.dtype, 3)
+    api.state_deposit(st, t[:100], 3)
+    y = t[100:].clone()
+    api.repro_cumsum_from_state(y, st, 3, out=y)
+    assert same_bits(y.cpu().numpy(), oracle.adn_cumsum(x, 3)[100:])
