@@ -334,15 +334,66 @@ def run_e2e(args, api, torch, h32, h64, hA, dev, stream):
 
     one()
     n = max(1, args.e2e_steps)
-    t = time.perf_counter()
+    times = []
     for _ in range(n):
+        t = time.perf_counter()
         one()
-    dt = (time.perf_counter() - t) / n
+        times.append(time.perf_counter() - t)
+    dt = sum(times) / n
     elems = sum(nn for _, nn, _ in ROWS_SPEC)
     h2d = 4 * N_SUM + 8 * N_SUM + 4 * ROWS * COLS
     d2h = 4 * N_SUM + 8 * N_SUM + 4 + 8 + 3 * 4 * ROWS
+    # the host link in this run: pinned copies of 1 GiB each way, best of 3
+    link = measure_link(torch, dev)
     return {"value": round(elems / dt / 1e9, 3), "unit": "GElements/s", "ms_per_step": round(dt * 1e3, 3),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+            "ms_per_step_min": round(min(times) * 1e3, 3), "ms_per_step_max": round(max(times) * 1e3, 3),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "link_gbs": link,
+            "link_bound_ms": round(max(h2d / link["h2d"], d2h / link["d2h"]) / 1e6, 3),
+            "host_api": run_host_api(api, torch, h32, h64)}
+
+
+def measure_link(torch, dev):
+    """Pinned host<->device copy rates (GB/s) of 1 GiB, best of three."""
+    nb = 1 << 30
+    h = torch.empty(nb, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nb, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, dst, src in (("h2d", d, h), ("d2h", h, d)):
+        best = 1e9
+        for _ in range(3):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            dst.copy_(src, non_blocking=True)
+            b.record()
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b) * 1e-3)
+        out[name] = round(nb / best / 1e9, 1)
+    del h, d
+    return out
+
+
+def run_host_api(api, torch, h32, h64, reps=3):
+    """The library's own host-memory path: the synchronous calls given plain
+    (pageable) host arrays, which copy the input in (and, for the cumulative
+    sums, the output back) inside the call.  Mean wall time per call, after
+    one untimed call."""
+    res = {}
+    x32, x64 = torch.from_numpy(h32), torch.from_numpy(h64)
+    o32, o64 = torch.empty_like(x32), torch.empty_like(x64)
+    calls = {"sum_f32_1e8": lambda: api.repro_sum(x32, 3), "sum_f64_1e8": lambda: api.repro_sum(x64, 3),
+             "cumsum_f32_1e8": lambda: api.repro_cumsum(x32, out=o32, K=3),
+             "cumsum_f64_1e8": lambda: api.repro_cumsum(x64, out=o64, K=3)}
+    for name, fn in calls.items():
+        fn()
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        dt = (time.perf_counter() - t) / reps
+        res[name] = {"ms": round(dt * 1e3, 3), "gelem_s": round(N_SUM / dt / 1e9, 3)}
+    return res
 
 
 def run_comparisons(api, torch, x32, x64, A, stream):
@@ -366,6 +417,12 @@ def run_comparisons(api, torch, x32, x64, A, stream):
 
     A64 = A.double()
     c64k6 = torch.empty_like(x64)
+    # inputs that leave the fast paths: magnitudes ascending (the cumulative
+    # sum's index settles late), and one value far above the sampled bins (the
+    # double sum's index guess misses)
+    asc = x64.abs().sort().values * torch.sign(x64)
+    outl = x64.clone()
+    outl[-1] = 3e200
     AC = A.view(torch.complex64)   # [4096, 2048] complex pairs of the same floats
     st32 = api.state_new(torch.float32, 3)
     st64 = api.state_new(torch.float64, 3)
@@ -383,6 +440,10 @@ def run_comparisons(api, torch, x32, x64, A, stream):
     for name, fn, n in (
         ("sum_f64_k6_1e8", lambda: api.repro_sum_async(x64, r64, 6), N_SUM),
         ("cumsum_f64_k6_1e8", lambda: api.repro_cumsum(x64, out=c64k6, K=6), N_SUM),
+        ("cumsum_f64_k4_1e8", lambda: api.repro_cumsum(x64, out=c64k6, K=4), N_SUM),
+        ("adn_cumsum_f64_1e8", lambda: api.repro_cumsum(x64, out=c64k6, K=3), N_SUM),
+        ("cumsum_f64_ascending_1e8", lambda: api.repro_cumsum(asc, out=c64k6, K=3), N_SUM),
+        ("sum_f64_one_outlier_1e8", lambda: api.repro_sum_async(outl, r64, 3), N_SUM),
         ("state_8_chunks_f32_1e8", lambda: chunked(x32, st32, r32), N_SUM),
         ("state_8_chunks_f64_1e8", lambda: chunked(x64, st64, r64), N_SUM),
         # the hot-path calls again, timed the same way as the others here
@@ -413,6 +474,7 @@ def run_comparisons(api, torch, x32, x64, A, stream):
     ):
         ms = timed(fn)
         out[name] = {"ms": round(ms, 4), "gelem_s": round(n / (ms * 1e-3) / 1e9, 2)}
+    del asc, outl
     return out
 
 
@@ -598,7 +660,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", default="", help="comma list of rows to run (profiling); default: all")
