@@ -149,11 +149,11 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     calls = {
         "var_f32_4096x4096": lambda: api.stable_var(A, axis=1, ddof=1, out=vout, mean_out=vmean),
-        "sum_f32_1e8": lambda: api.repro_sum_async(x32, s32, 3),
+        "sum_f32_1e8": lambda: api.repro_sum_async(x32, s32, args.k),
         "segsum_f32_4096x4096": lambda: api.repro_segsum(A, axis=1, K=3, out=segout),
-        "cumsum_f32_1e8": lambda: api.repro_cumsum(x32, out=c32, K=3),
-        "sum_f64_1e8": lambda: api.repro_sum_async(x64, s64, 3),
-        "cumsum_f64_1e8": lambda: api.repro_cumsum(x64, out=c64, K=3),
+        "cumsum_f32_1e8": lambda: api.repro_cumsum(x32, out=c32, K=args.k),
+        "sum_f64_1e8": lambda: api.repro_sum_async(x64, s64, args.k),
+        "cumsum_f64_1e8": lambda: api.repro_cumsum(x64, out=c64, K=args.k),
     }
     # kernels per call: the double sum is the fixed-index kernel plus its
     # gated fallback; a cumulative sum is totals, scan and replay plus four
@@ -229,7 +229,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "f32+f64 inputs, exact int64/int128 binned lanes",
         "data": "synthetic (seeded numpy generators, shapes and distributions of the pages' workloads)",
-        "config": {"workload": WORKLOAD if N_SUM == 100_000_000 else WORKLOAD.replace("1e8", "%d" % N_SUM), "K": 3,
+        "config": {"workload": WORKLOAD if N_SUM == 100_000_000 else WORKLOAD.replace("1e8", "%d" % N_SUM),
+                   "K": args.k,
                    "elements_per_step_per_gpu": elems_step,
                    "l2": "every input is larger than L2 or follows >= 400 MB of other traffic in the step",
                    "parallelism": "independent replicas" if ws > 1 else "single GPU"},
@@ -661,6 +662,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--k", type=int, default=3,
+                    help="fold count of the sum and cumulative-sum rows (for profiling other K; the metric is "
+                         "quoted at K = 3)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", default="", help="comma list of rows to run (profiling); default: all")
