@@ -84,3 +84,28 @@ def test_f64_specials_sum_and_cumsum(K, kind):
     want = oracle.adn_cumsum_at(y, pos, K)
     assert same_bits(g, want), first_diff(g, want)
     assert np.all(np.isfinite(g[pos < first])) and not np.any(np.isfinite(g[pos >= first]))
+
+
+def test_general_cumsum_segment_scan_walks_several_segments():
+    """The per-fold cumulative sum scans 4096-element tiles in segments of 256
+    and then the segment totals in one block of 1024 threads; above 2^30
+    elements (1024 segments) each thread of that block walks more than one
+    segment.  1.1e9 floats, K = 4 (the per-fold path for float), prefixes
+    sampled around segment boundaries on both sides of the 1024th."""
+    dev()
+    n = 1_100_000_000
+    rng = np.random.default_rng(77)
+    x = rng.standard_normal(n, dtype=np.float32)
+    x[rng.integers(0, n, 1000)] *= np.float32(1e6)
+    t = to_dev(x)
+    got = api.repro_cumsum(t, K=4)
+    del t
+    seg = 256 * 4096
+    pos = [0, n - 1]
+    for k in (1, 2, 1022, 1023, 1024, 1025, 1026, 1048):
+        for d in (-2, -1, 0, 1, 4097):
+            pos.append(k * seg + d)
+    pos = np.unique(np.array([p for p in pos if 0 <= p < n] + rng.integers(0, n, 200).tolist()))
+    g = got[torch.from_numpy(pos).to(got.device)].cpu().numpy()
+    want = oracle.adn_cumsum_at(x, pos, 4)
+    assert same_bits(g, want), first_diff(g, want)
