@@ -1181,6 +1181,17 @@ __device__ __forceinline__ uint32_t lane_exp_max(const T* buf, int sb, int b, in
   return em;
 }
 
+__device__ __forceinline__ uint32_t lop3_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xFE;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+__device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t b, uint32_t c) {   // (a & b) ^ c
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
 // Double lanes, 128-bit totals (t1:t0).  Returns false, writing nothing,
 // when the lane cannot take the window.
 __device__ __forceinline__ bool cf_lane_window_f64(double* buf, int sb, int b, int cnt, uint64_t t0, uint64_t t1,
@@ -1230,14 +1241,14 @@ __device__ __forceinline__ bool cf_lane_window_f64(double* buf, int sb, int b, i
       const uint64_t s0 = fx::madw(mh2, q0, a0 >> 32), s1 = fx::madw(mh2, q1, a1 >> 32),
                      s2 = fx::madw(mh2, q2, a2 >> 32), s3 = fx::madw(mh2, q3, a3 >> 32),
                      s4 = fx::madw(mh2, q4, a4 >> 32);
-      const uint32_t V0 = (uint32_t)a2 | (uint32_t)s1 | (uint32_t)(s0 >> 32);
-      const uint32_t V1 = (uint32_t)a3 | (uint32_t)s2 | (uint32_t)(s1 >> 32);
-      const uint32_t V2 = (uint32_t)a4 | (uint32_t)s3 | (uint32_t)(s2 >> 32);
-      const uint32_t V3 = (uint32_t)s4 | (uint32_t)(s3 >> 32);
-      const uint64_t rl = ((((uint64_t)V1) << 32) | V0) & m0, rh = ((((uint64_t)V3) << 32) | V2) & m1;
       const uint32_t sm = (uint32_t)((int32_t)hi >> 31);
-      const uint64_t S = (uint64_t)(int64_t)(int32_t)sm;
-      const uint64_t xl = rl ^ S, xh = rh ^ S;
+      // each word: (a | b | c), masked and XORed with the sign: two three-input logic ops
+      const uint32_t x0 = lop3_and_xor(lop3_or((uint32_t)a2, (uint32_t)s1, (uint32_t)(s0 >> 32)), (uint32_t)m0, sm);
+      const uint32_t x1 = lop3_and_xor(lop3_or((uint32_t)a3, (uint32_t)s2, (uint32_t)(s1 >> 32)),
+                                       (uint32_t)(m0 >> 32), sm);
+      const uint32_t x2 = lop3_and_xor(lop3_or((uint32_t)a4, (uint32_t)s3, (uint32_t)(s2 >> 32)), (uint32_t)m1, sm);
+      const uint32_t x3 = lop3_and_xor((uint32_t)s4 | (uint32_t)(s3 >> 32), (uint32_t)(m1 >> 32), sm);
+      const uint64_t xl = ((uint64_t)x1 << 32) | x0, xh = ((uint64_t)x3 << 32) | x2;
       uint32_t r0, r1, r2, r3;
       asm("{\n\t.reg .u32 c;\n\t"
           "add.cc.u32 c, %4, 0xFFFFFFFF;\n\t"
