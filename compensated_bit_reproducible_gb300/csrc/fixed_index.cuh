@@ -30,19 +30,19 @@ namespace repro {
 namespace fx {
 
 constexpr int SAMPLE = 256;   // elements sampled for the index guess
-// Sum cells per sign, one per 32-bit word position of P'', for K folds.  A
-// valid element (inside the guessed bin) has shift u <= 50 + W (K - 1) over
-// g_f, so its three words end at position (u >> 5) + 2.  K <= 3 keeps 7
-// positions (0..6); K = 6 needs 10.
+// Word positions of P'' for K folds.  A valid element (inside the guessed
+// bin) has shift u <= 50 + W (K - 1) over g_f, so its three words end at
+// position (u >> 5) + 2.  K <= 3 keeps 7 positions (0..6); K = 6 needs 10.
+// The double sum keeps, per sign and per thread, STR - 1 cell pairs (see
+// fx_deposit).
 template <int K>
 struct FxGeo {
   static constexpr int UMAX = 50 + 40 * (K - 1);
   static constexpr int STR = K <= 3 ? 7 : (UMAX >> 5) + 3;
-  static constexpr int NPOS = STR - 2;   // kept positions 2..STR-1
-  static constexpr int CELLS = 2 * STR;  // both signs
+  static constexpr int NPOS = STR - 2;        // kept positions 2..STR-1
+  static constexpr int CELLS = 2 * (STR - 1); // sum cell pairs, both signs
 };
 constexpr int STRIDE = FxGeo<3>::STR;
-constexpr int CELLS = FxGeo<3>::CELLS;
 
 __device__ __forceinline__ uint32_t shl_clamp32(uint32_t v, int s) {   // s outside [0, 31] gives 0
   uint32_t r;
@@ -72,8 +72,16 @@ struct FxConst {
   uint32_t one, negone, c63, c31, c256, c7, Cp;
 };
 
-// One deposit.  A: 64-bit cells (stride NT), B: 32-bit cells; sign s word k
-// at cell k + 7 s (B: k - 2 + 7 s, only k >= 2 is used).
+// One deposit into the sum cells.  Sign s, position c = 0..STR-2 has a
+// 64-bit cell A[c + (STR - 1) s] (words c and c + 1 of P'') and a 32-bit
+// cell B[c + (STR - 1) s] (word c + 2), both at stride NT.  An element's
+// words (w2, w1, w0) at position c enter as one 96-bit add into the pair,
+// the carry out of A going into B: two cell updates per element.  Words at
+// positions 0 and 1 are fraction bits of the element's own P'' and are
+// multiplied by 0 before the add (a carry out of them would reach position
+// 2).  B takes at most 2^22 per deposit and is emptied by fx_fold every 992
+// deposits.  An element beyond the bin (flagged through umax) lands at
+// position STR - 2, in bounds.  k.c7 must be (STR - 1) k.one.
 template <int STR = STRIDE>
 __device__ __forceinline__ void fx_deposit(uint32_t hi, uint32_t lo, const FxConst& k, uint64_t* A, uint32_t* B,
                                            uint32_t NT, int& umax) {
@@ -81,7 +89,7 @@ __device__ __forceinline__ void fx_deposit(uint32_t hi, uint32_t lo, const FxCon
   int us = (int)mad32(eb, k.one, k.Cp);                       // shift of M
   umax = max(umax, us);
   uint32_t u = (uint32_t)max(us, 0);   // tiny values: their words stay below position 2
-  uint32_t c = min(u >> 5, (uint32_t)(STR - 2));   // beyond the bin (flagged through umax): kept in bounds
+  uint32_t c = min(u >> 5, (uint32_t)(STR - 2));
   uint32_t mh = (hi & 0xFFFFFu) | 0x100000u;
   uint32_t hl = shl_clamp32(1u, (int)mad32(u, k.negone, k.c63));
   uint32_t hh = shl_clamp32(1u, (int)mad32(u, k.negone, k.c31));
@@ -91,23 +99,44 @@ __device__ __forceinline__ void fx_deposit(uint32_t hi, uint32_t lo, const FxCon
   uint32_t w0 = funnel_l(0u, lo2, u);
   uint32_t w1 = funnel_l(lo2, mh2, u);
   uint32_t w2 = funnel_l(mh2, 0u, u);
+  uint32_t f1 = min(c, 1u), f0 = min(c >> 1, 1u);              // word c kept iff c >= 2, c + 1 iff c >= 1
   uint32_t off = mad32(mad32(hi >> 31, k.c7, c), NT, 0u);
   uint64_t* p = A + off;
   uint32_t* pb = B + off;
-  p[0] = madw(w0, k.one, p[0]);
-  p[NT] = madw(w1, k.one, p[NT]);
-  pb[0] = mad32(w2, k.one, pb[0]);
+  uint32_t a0, a1, bb = *pb;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(a0), "=r"(a1) : "l"(*p));
+  asm("mad.lo.cc.u32 %0, %3, %4, %0;\n\tmadc.lo.cc.u32 %1, %5, %6, %1;\n\tmadc.lo.u32 %2, %7, %8, %2;"
+      : "+r"(a0), "+r"(a1), "+r"(bb)
+      : "r"(w0), "r"(f0), "r"(w1), "r"(f1), "r"(w2), "r"(k.one));
+  uint64_t an;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(an) : "r"(a0), "r"(a1));
+  *p = an;
+  *pb = bb;
 }
 
+// Empties the B cells: B at position c + 2 is word 1 of the pair at c + 1,
+// and the carry of that add goes to the next B (lowest first, so each
+// carry is moved on in the same pass).  The carry of the top pair stays in
+// the top B cell (position STR), which no deposit of a valid element uses.
 template <int STR = STRIDE>
 __device__ __forceinline__ void fx_fold(uint64_t* A, uint32_t* B, uint32_t NT) {
 #pragma unroll
-  for (int s = 0; s < 2; ++s)
+  for (int s = 0; s < 2; ++s) {
+    uint32_t carry = 0;
 #pragma unroll
-    for (int w = 2; w < STR; ++w) {
-      A[(w + STR * s) * NT] += B[(w - 2 + STR * s) * NT];
-      B[(w - 2 + STR * s) * NT] = 0;
+    for (int c = 0; c <= STR - 3; ++c) {
+      uint64_t* pa = A + (c + 1 + (STR - 1) * s) * NT;
+      uint32_t* pb = B + (c + (STR - 1) * s) * NT;
+      uint32_t a0, a1;
+      asm("mov.b64 {%0, %1}, %2;" : "=r"(a0), "=r"(a1) : "l"(*pa));
+      asm("add.cc.u32 %0, %0, %2;\n\taddc.u32 %1, 0, 0;" : "+r"(a1), "=r"(carry) : "r"(*pb + carry));
+      uint64_t an;
+      asm("mov.b64 %0, {%1, %2};" : "=l"(an) : "r"(a0), "r"(a1));
+      *pa = an;
+      *pb = 0;
     }
+    B[(STR - 2 + (STR - 1) * s) * NT] += carry;
+  }
 }
 
 // Signed 192-bit integer.
@@ -199,19 +228,25 @@ __device__ __forceinline__ I320 tot_ldcg(const I320* q) {
   return r;
 }
 
-// Block sum of the thread cells (STR positions per sign) into a signed total
-// TOT (units of g_f), valid in thread 0.  `red` (32 warps x 2 (STR - 2)
-// W128) may alias the cells: they are read into registers before it is
-// written.
+// Block sum of the thread cells (after fx_fold) into a signed total TOT
+// (units of g_f), valid in thread 0.  Per sign the kept columns, relative
+// to position 2, are: 0 (A[1] >> 32 and A[2]), j = 1..STR-4 (A[j + 2]) and
+// STR - 2 (the top B cell).  `red` (32 warps x 2 (STR - 2) W128) may alias
+// the cells: they are read into registers before it is written.
 template <int STR, typename TOT>
-__device__ __forceinline__ TOT fx_block_total_t(const uint64_t* A, uint32_t NT, W128 (*red)[2 * (STR - 2)]) {
+__device__ __forceinline__ TOT fx_block_total_t(const uint64_t* A, const uint32_t* B, uint32_t NT,
+                                                W128 (*red)[2 * (STR - 2)]) {
   constexpr int NP = STR - 2, NC = 2 * NP;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (int)(NT >> 5);
   W128 col[NC];
 #pragma unroll
-  for (int s = 0; s < 2; ++s)
+  for (int s = 0; s < 2; ++s) {
+    const uint64_t* As = A + (STR - 1) * s * NT;
+    col[s * NP] = w_add(W128{As[NT] >> 32, 0}, W128{As[2 * NT], 0});
 #pragma unroll
-    for (int w = 2; w < STR; ++w) col[s * NP + (w - 2)] = W128{A[(w + STR * s) * NT], 0};
+    for (int j = 1; j <= STR - 4; ++j) col[s * NP + j] = W128{As[(j + 2) * NT], 0};
+    col[s * NP + NP - 1] = W128{B[(STR - 2 + (STR - 1) * s) * NT], 0};
+  }
   __syncthreads();
 #pragma unroll
   for (int i = 0; i < NC; ++i) {
@@ -228,15 +263,13 @@ __device__ __forceinline__ TOT fx_block_total_t(const uint64_t* A, uint32_t NT, 
     for (int i = 0; i < NC; ++i) {
       W128 s = W128{0, 0};
       for (int w = 0; w < nw; ++w) s = w_add(s, red[w][i]);
+      const int j = i % NP;
       TOT v;
-      tot_from_shifted(s, i % NP, &v);
+      tot_from_shifted(s, j == NP - 1 ? STR - 2 : j, &v);
       t = tot_add(t, i < NP ? v : tot_neg(v));
     }
   }
   return t;
-}
-__device__ __forceinline__ I192 fx_block_total(const uint64_t* A, uint32_t NT, W128 (*red)[10]) {
-  return fx_block_total_t<STRIDE, I192>(A, NT, red);
 }
 
 // Index guess from the largest exponent field over SAMPLE evenly spaced

@@ -7,13 +7,14 @@
 //
 // Accumulation.  M + h - b shifted by u & 31 is three 32-bit words w0, w1,
 // w2 that land at word positions c, c + 1, c + 2 of P'' (c = u >> 5); words
-// below position 2 are dropped.  Each thread keeps one 64-bit cell per word
-// position (and sign) in shared memory, so a deposit is an add into three
-// cells and no variable-width shift of a wide accumulator.  The top word w2
-// is below 2^22 and goes to a 32-bit cell (1024 additions fit), folded into
-// the 64-bit cells every 992 deposits.  K sets only how many positions
-// there are (7 for K <= 3, 10 for K = 6) and the width of the block total
-// (192 or 320 bits): an element's three words are the same for any K.
+// below position 2 are dropped.  Each thread keeps, per position and sign,
+// a 64-bit cell for words c and c + 1 and a 32-bit cell for word c + 2 in
+// shared memory; a deposit is one 96-bit add into that pair (the carry out
+// of the 64-bit cell goes into the 32-bit one), with no variable-width shift
+// of a wide accumulator.  The 32-bit cells are moved into the 64-bit ones
+// every 992 deposits.  K sets only how many positions there are (7 for
+// K <= 3, 10 for K = 6) and the width of the block total (192 or 320 bits):
+// an element's three words are the same for any K.
 #include "accum.cuh"
 #include "fixed_index.cuh"
 #include "launch.h"
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
   // the shortcuts need g_f/2 above every subnormal and every x with a forced
   // hidden bit below the grid: beta_f >= -1019; Inf/NaN in the sample fail too
   const bool usable = (bf >= -1019) && (eb_max < 0x7FF);
-  const FxConst kc = make_const(bf, one, Geo::STR);
+  const FxConst kc = make_const(bf, one, Geo::STR - 1);   // cell pairs per sign
   // largest valid shift: the top of bin Ig
   const int u_thr = bin_top_exponent<double>(Ig) + (int)kc.Cp;
 
@@ -175,7 +176,7 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
   const int fail = __syncthreads_or(!usable || umax > u_thr);
 
   // 3. Block total, partial, and the last block's merge and conversion.
-  Tot t = fx_block_total_t<Geo::STR, Tot>(A, NT, (W128(*)[2 * Geo::NPOS])fx_smem);
+  Tot t = fx_block_total_t<Geo::STR, Tot>(A, B, NT, (W128(*)[2 * Geo::NPOS])fx_smem);
   __shared__ bool last;
   if (threadIdx.x == 0) {
     Tot* pp = (Tot*)parts + blockIdx.x;
