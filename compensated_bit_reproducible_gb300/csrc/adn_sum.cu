@@ -220,15 +220,16 @@ __global__ void state_finalize_kernel(const unsigned char* st, int K, uint64_t c
   *result = convert_state<T, KMax<T>::V>(s, K);
 }
 
-// Workspace: [0, 256) ticket counter (zero at launch); [256, ...) partials.
-// With a gate, the kernel runs only if *gate is nonzero (it is the fallback
-// of a faster path that decides on the device).
+// ticket: a counter that is zero at launch, and zero again when the kernel
+// ends; parts: one partial state per block.  With a gate, the kernel runs
+// only if *gate is nonzero (it is the fallback of a faster path that decides
+// on the device), and clears it.
 // With `state`, the merged result is added to that binned state (no
 // conversion; `result` unused).
 template <typename T, int KT, int U>
 __global__ void __launch_bounds__(1024) adn_sum_kernel(const T* __restrict__ x, int64_t n, int K,
-                                                       unsigned char* __restrict__ ws, T* __restrict__ result,
-                                                       const unsigned* __restrict__ gate,
+                                                       unsigned* ticket, unsigned char* __restrict__ parts,
+                                                       T* __restrict__ result, unsigned* gate,
                                                        unsigned char* __restrict__ state) {
   if (gate) {
     // launched as a programmatic dependent of the fast path: wait until that
@@ -245,8 +246,6 @@ __global__ void __launch_bounds__(1024) adn_sum_kernel(const T* __restrict__ x, 
   acc.finish();
   State<N> st;
   block_merge<N>(acc.I, acc.flags, acc.L, K, &st);
-  unsigned* ticket = (unsigned*)ws;
-  unsigned char* parts = ws + 256;
   __shared__ bool last;
   if (threadIdx.x == 0) {
     store_partial<N>(parts, blockIdx.x, K, st);
@@ -262,7 +261,9 @@ __global__ void __launch_bounds__(1024) adn_sum_kernel(const T* __restrict__ x, 
     if (state) state_add<T>(state, K, st.I, st.flags, st.F, (uint64_t)n);
     else if constexpr (KT != 0) *result = convert_fast<T, KT>(st.I, st.flags, st.F);
     else *result = convert_state<T, N>(st, K);
+    // leave the control words zero for the next call
     *ticket = 0u;
+    if (gate) *gate = 0u;
   }
 }
 
@@ -381,11 +382,11 @@ __global__ void __launch_bounds__(256) segsum_cols_kernel(const float* __restric
 
 // ------------------------------------------------------------------ launch
 template <typename T, int KT>
-static cudaError_t launch_sum_k(const T* x, int64_t n, int K, unsigned char* ws, T* result, int grid, int block,
-                                const unsigned* gate, cudaStream_t s, unsigned char* state = nullptr) {
+static cudaError_t launch_sum_k(const T* x, int64_t n, int K, unsigned* ticket, unsigned char* parts, T* result,
+                                int grid, int block, unsigned* gate, cudaStream_t s, unsigned char* state = nullptr) {
   constexpr int U = 4;
   if (!gate) {
-    adn_sum_kernel<T, KT, U><<<grid, block, 0, s>>>(x, n, K, ws, result, gate, state);
+    adn_sum_kernel<T, KT, U><<<grid, block, 0, s>>>(x, n, K, ticket, parts, result, gate, state);
     return cudaGetLastError();
   }
   // gated fallback: programmatic dependent launch overlaps its launch with
@@ -400,21 +401,21 @@ static cudaError_t launch_sum_k(const T* x, int64_t n, int K, unsigned char* ws,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, adn_sum_kernel<T, KT, U>, x, n, K, ws, result, gate, state);
+  return cudaLaunchKernelEx(&cfg, adn_sum_kernel<T, KT, U>, x, n, K, ticket, parts, result, gate, state);
 }
 
 template <typename T>
-cudaError_t launch_sum(const T* x, int64_t n, int K, unsigned char* ws, T* result, int grid, int block,
-                       cudaStream_t s, const unsigned* gate) {
+cudaError_t launch_sum(const T* x, int64_t n, int K, unsigned* ticket, unsigned char* parts, T* result, int grid,
+                       int block, cudaStream_t s, unsigned* gate) {
   switch (K) {
-    case 2: return launch_sum_k<T, 2>(x, n, K, ws, result, grid, block, gate, s);
-    case 3: return launch_sum_k<T, 3>(x, n, K, ws, result, grid, block, gate, s);
-    case 4: return launch_sum_k<T, 4>(x, n, K, ws, result, grid, block, gate, s);
-    case 5: return launch_sum_k<T, 5>(x, n, K, ws, result, grid, block, gate, s);
-    case 6: return launch_sum_k<T, 6>(x, n, K, ws, result, grid, block, gate, s);
-    case 7: return launch_sum_k<T, 7>(x, n, K, ws, result, grid, block, gate, s);
-    case 8: return launch_sum_k<T, 8>(x, n, K, ws, result, grid, block, gate, s);
-    default: return launch_sum_k<T, 0>(x, n, K, ws, result, grid, block, gate, s);
+    case 2: return launch_sum_k<T, 2>(x, n, K, ticket, parts, result, grid, block, gate, s);
+    case 3: return launch_sum_k<T, 3>(x, n, K, ticket, parts, result, grid, block, gate, s);
+    case 4: return launch_sum_k<T, 4>(x, n, K, ticket, parts, result, grid, block, gate, s);
+    case 5: return launch_sum_k<T, 5>(x, n, K, ticket, parts, result, grid, block, gate, s);
+    case 6: return launch_sum_k<T, 6>(x, n, K, ticket, parts, result, grid, block, gate, s);
+    case 7: return launch_sum_k<T, 7>(x, n, K, ticket, parts, result, grid, block, gate, s);
+    case 8: return launch_sum_k<T, 8>(x, n, K, ticket, parts, result, grid, block, gate, s);
+    default: return launch_sum_k<T, 0>(x, n, K, ticket, parts, result, grid, block, gate, s);
   }
 }
 
@@ -444,15 +445,17 @@ template cudaError_t launch_sum_single<double>(const double*, int64_t, int, doub
 template <typename T>
 cudaError_t launch_state_deposit(const T* x, int64_t n, int K, unsigned char* ws, unsigned char* state, int grid,
                                  int block, cudaStream_t s) {
+  unsigned* tk = (unsigned*)ws;
+  unsigned char* pp = ws + 256;
   switch (K) {
-    case 2: return launch_sum_k<T, 2>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
-    case 3: return launch_sum_k<T, 3>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
-    case 4: return launch_sum_k<T, 4>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
-    case 5: return launch_sum_k<T, 5>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
-    case 6: return launch_sum_k<T, 6>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
-    case 7: return launch_sum_k<T, 7>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
-    case 8: return launch_sum_k<T, 8>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
-    default: return launch_sum_k<T, 0>(x, n, K, ws, nullptr, grid, block, nullptr, s, state);
+    case 2: return launch_sum_k<T, 2>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
+    case 3: return launch_sum_k<T, 3>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
+    case 4: return launch_sum_k<T, 4>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
+    case 5: return launch_sum_k<T, 5>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
+    case 6: return launch_sum_k<T, 6>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
+    case 7: return launch_sum_k<T, 7>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
+    case 8: return launch_sum_k<T, 8>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
+    default: return launch_sum_k<T, 0>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
   }
 }
 
@@ -474,10 +477,10 @@ template cudaError_t launch_state_op<float>(int, unsigned char*, const unsigned 
 template cudaError_t launch_state_op<double>(int, unsigned char*, const unsigned char*, int, uint64_t, double*,
                                              cudaStream_t);
 
-template cudaError_t launch_sum<float>(const float*, int64_t, int, unsigned char*, float*, int, int, cudaStream_t,
-                                       const unsigned*);
-template cudaError_t launch_sum<double>(const double*, int64_t, int, unsigned char*, double*, int, int,
-                                        cudaStream_t, const unsigned*);
+template cudaError_t launch_sum<float>(const float*, int64_t, int, unsigned*, unsigned char*, float*, int, int,
+                                       cudaStream_t, unsigned*);
+template cudaError_t launch_sum<double>(const double*, int64_t, int, unsigned*, unsigned char*, double*, int, int,
+                                        cudaStream_t, unsigned*);
 
 // Resident blocks per SM of the sum kernel for this K and block size (one
 // wave of blocks covers the GPU; more would leave a partial second wave).

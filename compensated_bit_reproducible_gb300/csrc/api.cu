@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include "../../include/repro.h"
 #include "launch.h"
@@ -75,6 +76,41 @@ cudaError_t ws_alloc(void** p, size_t bytes, cudaStream_t stream) {
     pool = pools[dev];
   }
   return cudaMallocFromPoolAsync(p, bytes, pool, stream);
+}
+
+// Control words per device and stream: a page that every kernel using it
+// leaves zero when it ends (the sums' tickets, chunk queue, digit
+// accumulators and fallback flag).  Calls on one stream run in order, so
+// each finds the page zero and none needs a memset; calls on different
+// streams use different pages.  Pages live as long as the process (one per
+// stream ever used).  A stream that is destroyed while its calls are still
+// pending and whose handle is reused at once by a new stream would share
+// the page with them.
+constexpr size_t CTL_PAGE_BYTES = 4096;
+constexpr size_t CTL_SUM_TICKET = 0;      // general sum kernel's ticket
+constexpr size_t CTL_SUM_FIXED = 256;     // double fixed-index sum's control words
+
+cudaError_t ctl_page(cudaStream_t stream, unsigned char** out) {
+  static std::mutex mu;
+  static std::map<std::pair<int, cudaStream_t>, unsigned char*> pages;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> g(mu);
+  auto it = pages.find({dev, stream});
+  if (it != pages.end()) {
+    *out = it->second;
+    return cudaSuccess;
+  }
+  void* p = nullptr;
+  if ((e = cudaMalloc(&p, CTL_PAGE_BYTES)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(p, 0, CTL_PAGE_BYTES, stream)) != cudaSuccess) {
+    cudaFree(p);
+    return e;
+  }
+  pages[{dev, stream}] = (unsigned char*)p;
+  *out = (unsigned char*)p;
+  return cudaSuccess;
 }
 
 // At most this many elements, a sum runs in one block (no workspace, no
@@ -217,12 +253,9 @@ repro_status sum_async_impl(const T* x, size_t n, int K, cudaStream_t stream, T*
   }
   int grid = sum_grid((int64_t)n, block, 4 * (int)(16 / sizeof(T)), sum_blocks_per_sm<T>(K, block),
                       l);   // 4 vectors per thread per iteration, one wave of blocks
-  size_t wsb = sum_workspace_bytes(K, grid);
   // double with K = 2..6: the sampled fixed-index kernel runs first and the
-  // general kernel only if that one flags its guess (workspace header bytes
-  // [64, 76) are its control words)
+  // general kernel only if that one flags its guess
   int fgrid = 0, fblock = 0;
-  size_t foff = 0;
   if constexpr (sizeof(T) == 8) {
     if (K >= 2 && K <= 6 && n >= FIXED_MIN_N && (uint64_t)n <= FIXED_MAX_N) {
       fblock = (l && l->block) ? l->block : 128;
@@ -230,22 +263,22 @@ repro_status sum_async_impl(const T* x, size_t n, int K, cudaStream_t stream, T*
       // threads): the general kernel alone runs
       const int fcap = sum_f64_fixed_grid(K, fblock, sm_count());
       fgrid = fcap <= 0 ? 0 : ((l && l->grid > 0) ? l->grid : fcap);
-      if (fgrid > 0) {
-        foff = (wsb + 255) & ~(size_t)255;
-        wsb = foff + sum_f64_fixed_workspace_bytes(fgrid);
-      }
+      if (CTL_SUM_FIXED + sum_f64_fixed_ctl_bytes() > CTL_PAGE_BYTES) fgrid = 0;
     }
   }
+  // tickets and control words in the stream's page (zero between calls);
+  // the general kernel's partials in a workspace
+  unsigned char* page = nullptr;
+  CK(ctl_page(stream, &page));
+  unsigned* ticket = (unsigned*)(page + CTL_SUM_TICKET);
   Scratch ws;
   ws.s = stream;
-  CK(ws_alloc(&ws.p, wsb, stream));
-  CK(cudaMemsetAsync(ws.p, 0, 256, stream));
+  CK(ws_alloc(&ws.p, sum_workspace_bytes(K, grid), stream));
   unsigned char* w = (unsigned char*)ws.p;
   if constexpr (sizeof(T) == 8) {
     if (fgrid > 0) {
-      unsigned* ctl = (unsigned*)(w + 64);
-      CK(launch_sum_f64_fixed((const double*)x, (int64_t)n, K, ctl, w + foff, (double*)result_dev, fgrid, fblock,
-                              stream));
+      unsigned* ctl = (unsigned*)(page + CTL_SUM_FIXED);
+      CK(launch_sum_f64_fixed((const double*)x, (int64_t)n, K, ctl, (double*)result_dev, fgrid, fblock, stream));
       // the fallback runs when the guess misses: four blocks per SM keep its
       // idle launch short and still fill the GPU when it runs (measured on a
       // 1e8 sum with one value above the sampled bins: 1.06 ms with one block
@@ -256,11 +289,11 @@ repro_status sum_async_impl(const T* x, size_t n, int K, cudaStream_t stream, T*
       int64_t fb = grid < fcap ? grid : fcap;
       int fb_grid = (int)(fb > need ? fb : need);
       if (l && l->grid > 0) fb_grid = grid;
-      CK(launch_sum<T>(x, (int64_t)n, K, w, result_dev, fb_grid, block, stream, ctl + 2));
+      CK(launch_sum<T>(x, (int64_t)n, K, ticket, w, result_dev, fb_grid, block, stream, ctl + 2));
       return REPRO_OK;
     }
   }
-  CK(launch_sum<T>(x, (int64_t)n, K, w, result_dev, grid, block, stream));
+  CK(launch_sum<T>(x, (int64_t)n, K, ticket, w, result_dev, grid, block, stream));
   return REPRO_OK;
 }
 

@@ -228,48 +228,33 @@ __device__ __forceinline__ I320 tot_ldcg(const I320* q) {
   return r;
 }
 
-// Block sum of the thread cells (after fx_fold) into a signed total TOT
-// (units of g_f), valid in thread 0.  Per sign the kept columns, relative
-// to position 2, are: 0 (A[1] >> 32 and A[2]), j = 1..STR-4 (A[j + 2]) and
-// STR - 2 (the top B cell).  `red` (32 warps x 2 (STR - 2) W128) may alias
-// the cells: they are read into registers before it is written.
+// Number of 64-bit words of a total, and the words themselves.
+template <typename TOT> struct TotW;
+template <> struct TotW<I192> { static constexpr int N = 3; };
+template <> struct TotW<I320> { static constexpr int N = 5; };
+__device__ __forceinline__ uint64_t tot_word(const I192& t, int i) { return i == 0 ? t.w0 : i == 1 ? t.w1 : t.w2; }
+__device__ __forceinline__ uint64_t tot_word(const I320& t, int i) { return t.w[i]; }
+
+// The thread's cells (after fx_fold) as one signed total TOT in units of
+// g_f.  Per sign the kept columns, relative to position 2, are: 0 (A[1] >> 32
+// and A[2]), j = 1..STR-4 (A[j + 2]) and STR - 2 (the top B cell).
 template <int STR, typename TOT>
-__device__ __forceinline__ TOT fx_block_total_t(const uint64_t* A, const uint32_t* B, uint32_t NT,
-                                                W128 (*red)[2 * (STR - 2)]) {
-  constexpr int NP = STR - 2, NC = 2 * NP;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = (int)(NT >> 5);
-  W128 col[NC];
+__device__ __forceinline__ TOT fx_thread_total(const uint64_t* A, const uint32_t* B, uint32_t NT) {
+  TOT t[2];
 #pragma unroll
   for (int s = 0; s < 2; ++s) {
     const uint64_t* As = A + (STR - 1) * s * NT;
-    col[s * NP] = w_add(W128{As[NT] >> 32, 0}, W128{As[2 * NT], 0});
+    TOT v, w;
+    tot_from_shifted(W128{As[NT] >> 32, 0}, 0, &v);
 #pragma unroll
-    for (int j = 1; j <= STR - 4; ++j) col[s * NP + j] = W128{As[(j + 2) * NT], 0};
-    col[s * NP + NP - 1] = W128{B[(STR - 2 + (STR - 1) * s) * NT], 0};
-  }
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < NC; ++i) {
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) col[i] = w_add(col[i], shfl_xor_w(col[i], m));
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int i = 0; i < NC; ++i) red[warp][i] = col[i];
-  }
-  __syncthreads();
-  TOT t{};
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NC; ++i) {
-      W128 s = W128{0, 0};
-      for (int w = 0; w < nw; ++w) s = w_add(s, red[w][i]);
-      const int j = i % NP;
-      TOT v;
-      tot_from_shifted(s, j == NP - 1 ? STR - 2 : j, &v);
-      t = tot_add(t, i < NP ? v : tot_neg(v));
+    for (int j = 0; j <= STR - 4; ++j) {
+      tot_from_shifted(W128{As[(j + 2) * NT], 0}, j, &w);
+      v = tot_add(v, w);
     }
+    tot_from_shifted(W128{B[(STR - 2 + (STR - 1) * s) * NT], 0}, STR - 2, &w);
+    t[s] = tot_add(v, w);
   }
-  return t;
+  return tot_add(t[0], tot_neg(t[1]));
 }
 
 // Index guess from the largest exponent field over SAMPLE evenly spaced

@@ -123,7 +123,8 @@ extern "C" repro_status repro_sum_f32_noalloc(const float* x, size_t n, int K, c
   // the grid ticket must start at zero
   e = cudaMemsetAsync(d->scratch, 0, 256, stream);
   if (e == cudaSuccess)
-    e = repro::launch_sum<float>(x, (int64_t)n, K, d->scratch, result_dev, (int)grid, block, stream);
+    e = repro::launch_sum<float>(x, (int64_t)n, K, (unsigned*)d->scratch, d->scratch + 256, result_dev, (int)grid,
+                                 block, stream);
   if (e != cudaSuccess) {
     repro::set_last_cuda(e);
     return REPRO_ERR_CUDA;

@@ -29,11 +29,19 @@ constexpr int FX_U = 4;           // 16-byte vectors per thread per step
 constexpr int FX_J = 4;           // steps per chunk
 constexpr int FX_FOLD_CHUNKS = 31;   // 31 chunks x 32 deposits < 1024
 
-// Control words in the zeroed workspace header.
+// Control words, zero at launch; the kernel leaves them zero except the
+// fallback flag, which the general kernel clears.  The block totals are summed by
+// atomics as 32-bit digits in 64-bit accumulators (2^32 blocks before one
+// could carry out), one accumulator per 128-byte line so that the blocks'
+// additions to different digits do not queue on one line.
+constexpr int FX_DIGITS = 10;   // 320-bit totals
+constexpr int FX_DIG_STRIDE = 16;   // 64-bit words between two accumulators
 struct FixedCtl {
-  unsigned queue;    // next chunk of the dynamic queue
+  unsigned queue;    // next chunk of the dynamic queue (after the first gridDim.x)
   unsigned ticket;   // finished blocks
   unsigned fail;     // nonzero: the general pass computes the result
+  unsigned pad[29];
+  unsigned long long dig[FX_DIGITS * FX_DIG_STRIDE];
 };
 
 }  // namespace
@@ -88,7 +96,7 @@ __device__ __forceinline__ void fx_folds(const I320& tot, W128* F) {
 template <int K, int CNT>
 __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
     sum_f64_fixed_kernel(const double* __restrict__ x, int64_t n, uint32_t one, FixedCtl* ctl,
-                         unsigned char* __restrict__ parts, double* __restrict__ result) {
+                         double* __restrict__ result) {
   extern __shared__ __align__(16) unsigned char fx_smem[];
   const uint32_t NT = CNT ? (uint32_t)CNT : blockDim.x;
   uint64_t* A = (uint64_t*)fx_smem + threadIdx.x;
@@ -100,6 +108,21 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
   // the gated fallback kernel may start launching now; it waits for this
   // grid to complete before it reads the flag
   asm volatile("griddepcontrol.launch_dependents;");
+  // Chunks of CV 16-byte vectors from the first 16-byte boundary on.  Block
+  // b takes chunk b first and the rest from a dynamic queue; the first step
+  // of chunk b is loaded before the index guess, so its latency overlaps
+  // the sample's.
+  int64_t head = (int64_t)(((16 - ((uintptr_t)x & 15)) & 15) / 8);
+  if (head > n) head = n;
+  const double2* xv = (const double2*)(x + head);
+  const int64_t nv = (n - head) / 2;
+  const int64_t CV = (int64_t)NT * FX_U * FX_J;
+  const int64_t nch_all = nv / CV;
+  double2 v0[FX_U];
+  if ((int64_t)blockIdx.x < nch_all) {
+#pragma unroll
+    for (int q = 0; q < FX_U; ++q) v0[q] = __ldcs(xv + (int64_t)blockIdx.x * CV + threadIdx.x + (int64_t)q * NT);
+  }
   // 1. Index guess from a sample.
   int eb_max;
   const int Ig = guess_index<double>(x, n, K, &s_emax, &eb_max);
@@ -111,33 +134,33 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
   // largest valid shift: the top of bin Ig
   const int u_thr = bin_top_exponent<double>(Ig) + (int)kc.Cp;
 
-  // 2. Deposits: full chunks from a dynamic queue, then the ragged rest.
+  // 2. Deposits: full chunks, then the ragged rest.
 #pragma unroll
   for (int w = 0; w < Geo::CELLS; ++w) {
     A[w * NT] = 0;
     B[w * NT] = 0;
   }
   int umax = -1;
-  int64_t head = (int64_t)(((16 - ((uintptr_t)x & 15)) & 15) / 8);
-  if (head > n) head = n;
-  const double2* xv = (const double2*)(x + head);
-  const int64_t nv = (n - head) / 2;
-  const int64_t CV = (int64_t)NT * FX_U * FX_J;
-  const int64_t nchunks = usable ? nv / CV : 0;
+  const int64_t nchunks = usable ? nch_all : 0;
   int since = 0;
-  // chunk numbers come from the queue one chunk ahead, so the atomic's
-  // latency overlaps a chunk of deposits
+  // the next chunk number comes from the queue one chunk ahead, so the
+  // atomic's latency overlaps a chunk of deposits
   __shared__ unsigned s_q[2];
-  if (threadIdx.x == 0) s_q[0] = nchunks > 0 ? atomicAdd(&ctl->queue, 1u) : 0u;
-  __syncthreads();
-  for (int slot = 0;; slot ^= 1) {
-    const int64_t ch = s_q[slot];
-    if (ch >= nchunks) break;   // same value in every thread of the block
+  int64_t ch = blockIdx.x;   // same value in every thread of the block
+  int j0 = 1;                // the first step of the first chunk is in v0
+  if (ch < nchunks) {
+#pragma unroll
+    for (int q = 0; q < FX_U; ++q) {
+      fx_deposit<Geo::STR>((uint32_t)__double2hiint(v0[q].x), (uint32_t)__double2loint(v0[q].x), kc, A, B, NT, umax);
+      fx_deposit<Geo::STR>((uint32_t)__double2hiint(v0[q].y), (uint32_t)__double2loint(v0[q].y), kc, A, B, NT, umax);
+    }
+  }
+  for (int slot = 0; ch < nchunks; slot ^= 1) {
     unsigned nxt = 0;
-    if (threadIdx.x == 0) nxt = atomicAdd(&ctl->queue, 1u);
+    if (threadIdx.x == 0) nxt = gridDim.x + atomicAdd(&ctl->queue, 1u);
     const double2* base = xv + ch * CV + threadIdx.x;
 #pragma unroll 1
-    for (int j = 0; j < FX_J; ++j) {
+    for (int j = j0; j < FX_J; ++j) {
       double2 v[FX_U];
 #pragma unroll
       for (int q = 0; q < FX_U; ++q) v[q] = __ldcs(base + (int64_t)(j * FX_U + q) * NT);
@@ -149,12 +172,14 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
                              umax);
       }
     }
+    j0 = 0;
     if (++since == FX_FOLD_CHUNKS) {
       fx_fold<Geo::STR>(A, B, NT);
       since = 0;
     }
-    if (threadIdx.x == 0) s_q[slot ^ 1] = nxt;
+    if (threadIdx.x == 0) s_q[slot] = nxt;
     __syncthreads();
+    ch = s_q[slot];
   }
   fx_fold<Geo::STR>(A, B, NT);
   if (usable) {
@@ -175,46 +200,58 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
   }
   const int fail = __syncthreads_or(!usable || umax > u_thr);
 
-  // 3. Block total, partial, and the last block's merge and conversion.
-  Tot t = fx_block_total_t<Geo::STR, Tot>(A, B, NT, (W128(*)[2 * Geo::NPOS])fx_smem);
+  // 3. Block total into the digit accumulators; the last block converts.
+  Tot t = fx_thread_total<Geo::STR, Tot>(A, B, NT);
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) t = tot_add(t, tot_shfl_xor(t, m));
+  __shared__ Tot s_wt[32];
   __shared__ bool last;
+  if ((threadIdx.x & 31) == 0) s_wt[threadIdx.x >> 5] = t;
+  __syncthreads();
   if (threadIdx.x == 0) {
-    Tot* pp = (Tot*)parts + blockIdx.x;
-    *pp = t;
-    if (fail) atomicOr(&ctl->fail, 1u);
+    Tot bt = s_wt[0];
+    for (int w = 1; w < (int)(NT >> 5); ++w) bt = tot_add(bt, s_wt[w]);
+    if (fail) {
+      atomicOr(&ctl->fail, 1u);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2 * TotW<Tot>::N; ++i) {
+        const uint64_t wd = tot_word(bt, i >> 1);
+        atomicAdd(&ctl->dig[i * FX_DIG_STRIDE], (unsigned long long)((i & 1) ? wd >> 32 : wd & 0xFFFFFFFFull));
+      }
+    }
     __threadfence();
     unsigned tk = atomicAdd(&ctl->ticket, 1u);
     last = (tk == gridDim.x - 1);
   }
   __syncthreads();
-  if (!last) return;
+  if (!last || threadIdx.x != 0) return;
   __threadfence();
-  if (__ldcg(&ctl->fail)) return;   // the general pass writes the result
-  Tot s{};
-  for (int p = threadIdx.x; p < (int)gridDim.x; p += NT) s = tot_add(s, tot_ldcg((const Tot*)parts + p));
+  // sum of the digits D_i 2^(32 i), modulo 2^(64 N) (the total fits); the
+  // control words are left zero for the next call, except the flag, which
+  // the general pass clears
+  Tot tot{};
 #pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) s = tot_add(s, tot_shfl_xor(s, m));
-  Tot* sw = (Tot*)fx_smem;   // the cells are no longer needed
-  if ((threadIdx.x & 31) == 0) sw[threadIdx.x >> 5] = s;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    Tot tot{};
-    for (int w = 0; w < (int)(NT >> 5); ++w) tot = tot_add(tot, sw[w]);
-    W128 F[K];
-    fx_folds<K>(tot, F);
-    *result = convert_fast<double, K>(Ig, 0, F);
+  for (int i = 0; i < 2 * TotW<Tot>::N; ++i) {
+    Tot d;
+    tot_from_shifted(W128{__ldcg(&ctl->dig[i * FX_DIG_STRIDE]), 0}, i, &d);
+    ctl->dig[i * FX_DIG_STRIDE] = 0ull;
+    tot = tot_add(tot, d);
   }
+  ctl->queue = 0u;
+  ctl->ticket = 0u;
+  if (__ldcg(&ctl->fail)) return;   // the general pass writes the result
+  W128 F[K];
+  fx_folds<K>(tot, F);
+  *result = convert_fast<double, K>(Ig, 0, F);
 }
 
 // ------------------------------------------------------------------ host
 namespace {
-// cells, and at least the epilogue's reduction scratch (32 warps x
-// 2 (STR - 2) W128)
+// the cells: per thread a 64-bit and a 32-bit cell per position and sign
 template <int K>
 size_t fx_smem_bytes(int block) {
-  const size_t cells = (size_t)block * FxGeo<K>::CELLS * 12;
-  const size_t red = (size_t)32 * 2 * FxGeo<K>::NPOS * sizeof(W128);
-  return cells > red ? cells : red;
+  return (size_t)block * FxGeo<K>::CELLS * 12;
 }
 
 template <int K, int CNT>
@@ -253,15 +290,14 @@ int blocks_per_sm_k(int block) {
 }
 
 template <int K>
-void launch_k(const double* x, int64_t n, unsigned* ctl, unsigned char* parts, double* result, int grid, int block,
-              cudaStream_t s) {
+void launch_k(const double* x, int64_t n, unsigned* ctl, double* result, int grid, int block, cudaStream_t s) {
   size_t smem = fx_smem_bytes<K>(block);
   if (block == 128)
-    sum_f64_fixed_kernel<K, 128><<<grid, block, smem, s>>>(x, n, 1u, (FixedCtl*)ctl, parts, result);
+    sum_f64_fixed_kernel<K, 128><<<grid, block, smem, s>>>(x, n, 1u, (FixedCtl*)ctl, result);
   else if (block == 256)
-    sum_f64_fixed_kernel<K, 256><<<grid, block, smem, s>>>(x, n, 1u, (FixedCtl*)ctl, parts, result);
+    sum_f64_fixed_kernel<K, 256><<<grid, block, smem, s>>>(x, n, 1u, (FixedCtl*)ctl, result);
   else
-    sum_f64_fixed_kernel<K, 0><<<grid, block, smem, s>>>(x, n, 1u, (FixedCtl*)ctl, parts, result);
+    sum_f64_fixed_kernel<K, 0><<<grid, block, smem, s>>>(x, n, 1u, (FixedCtl*)ctl, result);
 }
 }  // namespace
 
@@ -279,19 +315,19 @@ int sum_f64_fixed_grid(int K, int block, int sms) {
   return nb > 0 ? nb * sms : 0;
 }
 
-// one partial per block, at the widest total's size
-size_t sum_f64_fixed_workspace_bytes(int grid) { return (size_t)grid * sizeof(I320); }
+// the control words and digit accumulators, zeroed by the caller
+size_t sum_f64_fixed_ctl_bytes() { return sizeof(FixedCtl); }
 
-cudaError_t launch_sum_f64_fixed(const double* x, int64_t n, int K, unsigned* ctl, unsigned char* parts,
-                                 double* result, int grid, int block, cudaStream_t s) {
+cudaError_t launch_sum_f64_fixed(const double* x, int64_t n, int K, unsigned* ctl, double* result, int grid, int block,
+                                 cudaStream_t s) {
   // make sure the shared-memory attribute is set for this device and block size
   if (sum_f64_fixed_grid(K, block, 1) <= 0) return cudaErrorInvalidConfiguration;
   switch (K) {
-    case 2: launch_k<2>(x, n, ctl, parts, result, grid, block, s); break;
-    case 3: launch_k<3>(x, n, ctl, parts, result, grid, block, s); break;
-    case 4: launch_k<4>(x, n, ctl, parts, result, grid, block, s); break;
-    case 5: launch_k<5>(x, n, ctl, parts, result, grid, block, s); break;
-    default: launch_k<6>(x, n, ctl, parts, result, grid, block, s); break;
+    case 2: launch_k<2>(x, n, ctl, result, grid, block, s); break;
+    case 3: launch_k<3>(x, n, ctl, result, grid, block, s); break;
+    case 4: launch_k<4>(x, n, ctl, result, grid, block, s); break;
+    case 5: launch_k<5>(x, n, ctl, result, grid, block, s); break;
+    default: launch_k<6>(x, n, ctl, result, grid, block, s); break;
   }
   return cudaGetLastError();
 }
