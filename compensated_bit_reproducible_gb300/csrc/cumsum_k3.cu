@@ -902,24 +902,24 @@ __device__ __forceinline__ void cf_stage(T* buf, const T* g, int cnt, int lane) 
 }
 
 // Double totals: each thread deposits its elements' rounded values into
-// 64-bit cells in shared memory.  An element's value M' 2^u (the rounding
-// of the binned sum's fixed-index deposit) is three 32-bit words w0, w1, w2
-// at word positions c, c + 1, c + 2 (c = u >> 5; positions 0 and 1 lie
-// below the grid and are dropped).  w0 goes to an A cell (positions 2..4)
-// and the pair (w2:w1), below 2^54, to one P cell as a 64-bit value at
-// position c + 1 (positions 2..5): two cell updates per element instead of
-// three, the shared-memory traffic that binds this pass.  For c < 2 the
-// dropped words are zeroed first (c = 0: only w2 remains, as the low word
-// of P at position 2).  Those selects are multiply-adds by 0/1 flags, which
-// run on the multiply-add pipe.  Per sign there are 7 cells (A 2..4, P 2..5);
-// a lane takes their value after its 16 elements and clears them.
-constexpr int CT_CELLS = 14;
+// cells in shared memory.  An element's value M' 2^u (the rounding of the
+// binned sum's fixed-index deposit) is three 32-bit words w0, w1, w2 at word
+// positions c, c + 1, c + 2 (c = u >> 5 <= 4; positions 0 and 1 lie below
+// the grid and are dropped).  Per sign and position c the thread has a
+// 64-bit cell A (words c, c + 1) and a 32-bit cell B (word c + 2); a deposit
+// is one 96-bit add into that pair, the carry out of A going into B.  The
+// words at positions 0 and 1 are multiplied by 0 first (a carry out of them
+// would reach position 2); the 0/1 factors come from multiply-adds.  A lane
+// takes the cells' value after its 16 elements (B stays below 2^26) and
+// clears them.
+constexpr int CT_PAIRS = 10;   // 5 positions x 2 signs
 template <typename T>
 __host__ __device__ constexpr int ct_cell_bytes() {
-  return sizeof(T) == 8 ? CT_CELLS * C3_BLOCK * 8 : 0;
+  return sizeof(T) == 8 ? CT_PAIRS * C3_BLOCK * 12 : 0;
 }
 
-__device__ __forceinline__ void ct_deposit(uint32_t hi, uint32_t lo, const fx::FxConst& k, uint32_t c7, uint64_t* A) {
+__device__ __forceinline__ void ct_deposit(uint32_t hi, uint32_t lo, const fx::FxConst& k, uint32_t c5, uint64_t* A,
+                                           uint32_t* B) {
   const uint32_t eb = fx::mad32(hi, k.one + k.one, 0u) >> 21;   // biased exponent
   const int us = (int)fx::mad32(eb, k.one, k.Cp);               // shift of M
   const uint32_t u = (uint32_t)max(us, 0);
@@ -934,47 +934,58 @@ __device__ __forceinline__ void ct_deposit(uint32_t hi, uint32_t lo, const fx::F
   const uint32_t w0 = fx::funnel_l(0u, lo2, u);
   const uint32_t w1 = fx::funnel_l(lo2, mh2, u);
   const uint32_t w2 = fx::funnel_l(mh2, 0u, u);
-  const uint32_t c2 = fx::mad32(c, k.one, 2u);
-  const uint32_t f2 = fx::mad32(c, k.one, 126u) >> 7;   // c >= 2
+  const uint32_t f0 = fx::mad32(c, k.one, 126u) >> 7;   // c >= 2
   const uint32_t f1 = fx::mad32(c, k.one, 127u) >> 7;   // c >= 1
-  const uint32_t w0m = fx::mad32(w0, f2, 0u);
-  const uint32_t apos = fx::mad32(f2, 0xFFFFFFFEu, c2);  // c (w0 zero when c < 2: any position)
-  const uint32_t plo = fx::mad32(f1, w1 - w2, w2);      // c >= 1: w1, else w2
-  const uint32_t phi = fx::mad32(w2, f1, 0u);           // c >= 1: w2, else 0
-  const uint32_t ppos = fx::mad32(f1, 0xFFFFFFFFu, c2);  // c + 1, or 2 when c = 0
-  const uint32_t sb = fx::mad32(hi >> 31, c7, 0u);
-  uint64_t* pa = A + fx::mad32(sb + apos - 2u, (uint32_t)C3_BLOCK, 0u);
-  uint64_t* pp = A + fx::mad32(sb + ppos + 1u, (uint32_t)C3_BLOCK, 0u);
-  *pa = fx::madw(w0m, k.one, *pa);
-  const uint64_t t = fx::madw(plo, k.one, *pp);
-  *pp = ((uint64_t)fx::mad32(phi, k.one, (uint32_t)(t >> 32)) << 32) | (uint32_t)t;
+  const uint32_t off = fx::mad32(fx::mad32(hi >> 31, c5, c), (uint32_t)C3_BLOCK, 0u);
+  uint64_t* p = A + off;
+  uint32_t* pb = B + off;
+  uint32_t a0, a1, bb = *pb;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(a0), "=r"(a1) : "l"(*p));
+  asm("mad.lo.cc.u32 %0, %3, %4, %0;\n\tmadc.lo.cc.u32 %1, %5, %6, %1;\n\tmadc.lo.u32 %2, %7, %8, %2;"
+      : "+r"(a0), "+r"(a1), "+r"(bb)
+      : "r"(w0), "r"(f0), "r"(w1), "r"(f1), "r"(w2), "r"(k.one));
+  uint64_t an;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(an) : "r"(a0), "r"(a1));
+  *p = an;
+  *pb = bb;
+}
+
+// D * 2^(32 j) as I192 for a signed 96-bit D = (d2:d1:d0), j = -2..2 (for
+// j < 0 the words shifted out are zero).
+__device__ __forceinline__ fx::I192 ct_s96(uint32_t d0, uint32_t d1, uint32_t d2, int j) {
+  const uint32_t sx = (uint32_t)((int32_t)d2 >> 31);
+  uint32_t w[6];
+#pragma unroll
+  for (int i = 0; i < 6; ++i) {
+    const int q = i - j;   // word q of D
+    w[i] = q < 0 ? 0u : q == 0 ? d0 : q == 1 ? d1 : q == 2 ? d2 : sx;
+  }
+  return fx::I192{((uint64_t)w[1] << 32) | w[0], ((uint64_t)w[3] << 32) | w[2], ((uint64_t)w[5] << 32) | w[4]};
 }
 
 // The value of the thread's cells, which are then cleared: the sum of the
-// rounded values deposited since the last call.  Per word position the two
-// signs' cells subtract to a 64-bit d_w (a P cell sums at most 16 values
-// below 2^54 between calls), and the four d_w combine at their 32-bit
-// offsets.
-__device__ __forceinline__ fx::I192 ct_take(uint64_t* A) {
-  int64_t d[4];
+// rounded values deposited since the last call, in units of g_f.  Per
+// position c the two signs' pairs subtract to a signed 96-bit D_c (each pair
+// holds less than 2^90), and T = sum_c D_c 2^(32 (c - 2)): A at position 0
+// and the low word of A at position 1 stay zero, so D_0 and D_1 shift down
+// exactly.
+__device__ __forceinline__ fx::I192 ct_take(uint64_t* A, uint32_t* B) {
+  fx::I192 t{0, 0, 0};
 #pragma unroll
-  for (int w = 2; w < 6; ++w) {
-    uint64_t pos = A[(w + 1) * C3_BLOCK], neg = A[(w + 8) * C3_BLOCK];   // P cells
-    A[(w + 1) * C3_BLOCK] = 0;
-    A[(w + 8) * C3_BLOCK] = 0;
-    if (w <= 4) {   // A cells
-      pos += A[(w - 2) * C3_BLOCK];
-      neg += A[(w + 5) * C3_BLOCK];
-      A[(w - 2) * C3_BLOCK] = 0;
-      A[(w + 5) * C3_BLOCK] = 0;
-    }
-    d[w - 2] = (int64_t)(pos - neg);
+  for (int c = 0; c < 5; ++c) {
+    const uint64_t ap = A[c * C3_BLOCK], an = A[(c + 5) * C3_BLOCK];
+    const uint32_t bp = B[c * C3_BLOCK], bn = B[(c + 5) * C3_BLOCK];
+    A[c * C3_BLOCK] = 0;
+    A[(c + 5) * C3_BLOCK] = 0;
+    B[c * C3_BLOCK] = 0;
+    B[(c + 5) * C3_BLOCK] = 0;
+    uint32_t d0, d1, d2;
+    asm("sub.cc.u32 %0, %3, %4;\n\tsubc.cc.u32 %1, %5, %6;\n\tsubc.u32 %2, %7, %8;"
+        : "=r"(d0), "=r"(d1), "=r"(d2)
+        : "r"((uint32_t)ap), "r"((uint32_t)an), "r"((uint32_t)(ap >> 32)), "r"((uint32_t)(an >> 32)), "r"(bp),
+          "r"(bn));
+    t = fx::i192_add(t, ct_s96(d0, d1, d2, c - 2));
   }
-  const uint64_t x0 = (uint64_t)(d[0] >> 63), x1 = (uint64_t)(d[1] >> 63), x2 = (uint64_t)(d[2] >> 63);
-  fx::I192 t{(uint64_t)d[0], x0, x0};
-  t = fx::i192_add(t, fx::I192{(uint64_t)d[1] << 32, (uint64_t)(d[1] >> 32), x1});
-  t = fx::i192_add(t, fx::I192{0, (uint64_t)d[2], x2});
-  t = fx::i192_add(t, fx::I192{0, (uint64_t)d[3] << 32, (uint64_t)(d[3] >> 32)});
   return t;
 }
 
@@ -1017,10 +1028,14 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
     if (L < facc.I) facc.raise(L);
   }
   uint64_t* A = (uint64_t*)ct_smem + threadIdx.x;   // double: this thread's cells
-  const uint32_t c7 = 7u * one;
+  uint32_t* Bc = (uint32_t*)((uint64_t*)ct_smem + CT_PAIRS * C3_BLOCK) + threadIdx.x;
+  const uint32_t c5 = 5u * one;
   if constexpr (sizeof(T) == 8) {
 #pragma unroll
-    for (int k = 0; k < CT_CELLS; ++k) A[k * C3_BLOCK] = 0;
+    for (int k = 0; k < CT_PAIRS; ++k) {
+      A[k * C3_BLOCK] = 0;
+      Bc[k * C3_BLOCK] = 0;
+    }
   }
   const int64_t gw = (int64_t)blockIdx.x * CF_WARPS + warp, GW = (int64_t)gridDim.x * CF_WARPS;
   for (int64_t ch = gw; ch < nch; ch += GW) {
@@ -1060,8 +1075,8 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
       // padding elements are zero and deposit nothing
 #pragma unroll
       for (int i = 0; i < 16; ++i)
-        ct_deposit((uint32_t)__double2hiint(v[i]), (uint32_t)__double2loint(v[i]), kc, c7, A);
-      const fx::I192 own = ct_take(A);
+        ct_deposit((uint32_t)__double2hiint(v[i]), (uint32_t)__double2loint(v[i]), kc, c5, A, Bc);
+      const fx::I192 own = ct_take(A, Bc);
       const fx::I192 exc = i192_warp_exclusive(own, &tot);
       const size_t plane = (size_t)nch * 32;
       uint64_t* lp = (uint64_t*)lanep;
