@@ -566,6 +566,18 @@ __device__ __forceinline__ bool c3_gated_off(const unsigned* gate) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   return *gate == 0u;
 }
+// The same for the later kernels of the fallback chain.  The gate is set by
+// the fast path's scan, which completed before the fast path's last kernel
+// started; the chain's first kernel waits for that kernel, and a later
+// kernel's blocks start only after every block of the kernel before it has
+// exited.  So a later kernel reads a final gate without waiting, and only a
+// set gate waits (for the results of the kernel before it).
+__device__ __forceinline__ bool c3_gated_off_later(const unsigned* gate) {
+  if (!gate) return false;
+  if (*(volatile const unsigned*)gate == 0u) return true;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  return false;
+}
 
 // ------------------------------------------------------------------ A
 // Per-warp totals: warp w of a tile covers its elements [w * 512, w * 512 +
@@ -640,7 +652,7 @@ __global__ void __launch_bounds__(1024) c3_scan_tiles(const unsigned char* __res
                                                       int I0, unsigned char* __restrict__ tloc,
                                                       unsigned char* __restrict__ btot, const unsigned* gate) {
   __shared__ S3 sm[32];
-  if (c3_gated_off(gate)) return;
+  if (c3_gated_off_later(gate)) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   S3 tot = s3_zero(I0);
@@ -690,7 +702,7 @@ __global__ void __launch_bounds__(1024) c3_scan_blocks(unsigned char* __restrict
                                                        unsigned char* __restrict__ bpre, const unsigned* gate,
                                                        const unsigned char* __restrict__ carry) {
   __shared__ S3 sm[32];
-  if (c3_gated_off(gate)) return;
+  if (c3_gated_off_later(gate)) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // nb <= 1024 * per; thread t handles [t * per, ...)
   int64_t per = (nb + blockDim.x - 1) / blockDim.x;
@@ -772,7 +784,7 @@ __global__ void __launch_bounds__(C3_BLOCK) c3_replay(const T* in, T* out, int64
                                                       const unsigned* gate) {
   __shared__ T sm[C3_TILE + C3_TILE / C3_ITEMS];
   __shared__ S3 wsm[C3_WARPS];
-  if (c3_gated_off(gate)) return;
+  if (c3_gated_off_later(gate)) return;
   for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     S3 st = s3_load(bpre + (size_t)(tile / 1024) * C3_STATE);
     s3_merge(st, s3_load(tloc + (size_t)tile * C3_STATE));
@@ -1111,27 +1123,38 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
 }
 
 // Pass 2: exclusive scan of the chunk totals.  Block b scans chunks
-// [1024 b, 1024 b + 1024) into lpre; the last block to finish scans the
-// block totals into bpre and decides the path.  Prefix of chunk c:
-// bpre[c >> 10] + lpre[c].
-__global__ void __launch_bounds__(1024) cf_scan(const fx::I192* __restrict__ ctot, int64_t nch, CsCtl* ctl,
-                                                fx::I192* __restrict__ lpre, fx::I192* __restrict__ btot,
-                                                fx::I192* __restrict__ bpre) {
-  __shared__ fx::I192 sm[32];
+// [1024 b, 1024 b + 1024) into lpre (four consecutive chunks per thread);
+// the last block to finish scans the block totals into bpre and decides the
+// path.  Prefix of chunk c: bpre[c >> 10] + lpre[c].
+constexpr int CS_SCAN_THREADS = 256;
+__global__ void __launch_bounds__(CS_SCAN_THREADS) cf_scan(const fx::I192* __restrict__ ctot, int64_t nch, CsCtl* ctl,
+                                                           fx::I192* __restrict__ lpre, fx::I192* __restrict__ btot,
+                                                           fx::I192* __restrict__ bpre) {
+  constexpr int NW = CS_SCAN_THREADS / 32;
+  __shared__ fx::I192 sm[NW];
   __shared__ bool last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t ci = (int64_t)blockIdx.x * 1024 + threadIdx.x;
-  fx::I192 v = ci < nch ? ctot[ci] : fx::I192{0, 0, 0};
+  const int64_t c0 = (int64_t)blockIdx.x * 1024 + 4 * threadIdx.x;
+  fx::I192 v[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) v[j] = c0 + j < nch ? ctot[c0 + j] : fx::I192{0, 0, 0};
+  // inclusive prefixes of the thread's four chunks
+  const fx::I192 p1 = fx::i192_add(v[0], v[1]), p2 = fx::i192_add(p1, v[2]), p3 = fx::i192_add(p2, v[3]);
   fx::I192 wt;
-  fx::I192 exc = i192_warp_exclusive(v, &wt);
+  fx::I192 exc = i192_warp_exclusive(p3, &wt);
   if (lane == 0) sm[warp] = wt;
   __syncthreads();
   fx::I192 base{0, 0, 0}, all{0, 0, 0};
-  for (int w = 0; w < 32; ++w) {
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
     if (w < warp) base = fx::i192_add(base, sm[w]);
     all = fx::i192_add(all, sm[w]);
   }
-  if (ci < nch) lpre[ci] = fx::i192_add(base, exc);
+  exc = fx::i192_add(base, exc);
+  if (c0 < nch) lpre[c0] = exc;
+  if (c0 + 1 < nch) lpre[c0 + 1] = fx::i192_add(exc, v[0]);
+  if (c0 + 2 < nch) lpre[c0 + 2] = fx::i192_add(exc, p1);
+  if (c0 + 3 < nch) lpre[c0 + 3] = fx::i192_add(exc, p2);
   if (threadIdx.x == 0) {
     btot[blockIdx.x] = all;
     __threadfence();
@@ -1141,7 +1164,7 @@ __global__ void __launch_bounds__(1024) cf_scan(const fx::I192* __restrict__ cto
   if (!last) return;
   __threadfence();
   const int64_t nb = gridDim.x;
-  const int64_t per = (nb + 1023) / 1024;
+  const int64_t per = (nb + CS_SCAN_THREADS - 1) / CS_SCAN_THREADS;
   const int64_t b0 = (int64_t)threadIdx.x * per, b1 = min(nb, b0 + per);
   fx::I192 agg{0, 0, 0};
   for (int64_t i = b0; i < b1; ++i) {
@@ -1637,7 +1660,7 @@ cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, 
     const int64_t wb = (nc + CF_WARPS - 1) / CF_WARPS;   // blocks that have a chunk
     const int64_t gt = max((int64_t)1, min(wb, sms * max(bt, 1))), gr = max((int64_t)1, min(wb, sms * max(br, 1)));
     cf_totals<T><<<(unsigned)gt, C3_BLOCK, ct_cell_bytes<T>(), s>>>(in, n, nc, 1u, ctl, lanep, ctot);
-    cf_scan<<<(unsigned)ncb, 1024, 0, s>>>(ctot, nc, ctl, lpre, btot, bpre);
+    cf_scan<<<(unsigned)ncb, CS_SCAN_THREADS, 0, s>>>(ctot, nc, ctl, lpre, btot, bpre);
     cf_replay<T><<<(unsigned)gr, C3_BLOCK, 0, s>>>(in, out, n, nc, 1u, ctl, lanep, lpre, bpre);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     gate = &ctl->general;
