@@ -1001,6 +1001,16 @@ __device__ __forceinline__ fx::I192 ct_take(uint64_t* A, uint32_t* B) {
   return t;
 }
 
+// The lane prefix's top word (double: bits 128..191 of a value below 2^139
+// in magnitude; float: the whole prefix, below 2^47) carries the lane's
+// largest exponent field in its top 16 bits, which are otherwise copies of
+// the sign; the replay takes it from there instead of rereading the lane.
+__device__ __forceinline__ uint64_t lanep_pack(uint64_t w, uint32_t eb) {
+  return (w & 0x0000FFFFFFFFFFFFull) | ((uint64_t)eb << 48);
+}
+__device__ __forceinline__ uint64_t lanep_word(uint64_t w) { return (uint64_t)((int64_t)(w << 16) >> 16); }
+__device__ __forceinline__ uint32_t lanep_exp(uint64_t w) { return (uint32_t)(w >> 48); }
+
 // Pass 1.  Persistent blocks; each warp takes whole chunks: staged in shared
 // memory, lane l sums its 16 contiguous elements (double: one rounding each;
 // float: the binned sum's floating-point primaries at the fixed index, whose
@@ -1059,17 +1069,26 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
     cf_stage<T>(buf, in + c0, cnt, lane);
     __syncwarp();
     const int b = lane * 16, sb = b + lane;
-    T v[16];
+    T v[sizeof(T) == 8 ? 1 : 16];   // float: the lane's elements (double deposits each as it is read)
     uint32_t em = 0;   // largest magnitude bits (hi word shifted past the sign)
+    if constexpr (sizeof(T) == 8) {
+      // padding elements are zero and deposit nothing
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      v[i] = b + i < cnt ? buf[sb + i] : (T)0;
-      uint32_t hi;
-      if constexpr (sizeof(T) == 8) hi = (uint32_t)__double2hiint(v[i]);
-      else hi = __float_as_uint(v[i]);
-      em = max(em, hi << 1);
+      for (int i = 0; i < 16; ++i) {
+        const double x = b + i < cnt ? buf[sb + i] : 0.0;
+        const uint32_t hi = (uint32_t)__double2hiint(x);
+        em = max(em, hi << 1);
+        ct_deposit(hi, (uint32_t)__double2loint(x), kc, c5, A, Bc);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        v[i] = b + i < cnt ? buf[sb + i] : (T)0;
+        em = max(em, __float_as_uint(v[i]) << 1);
+      }
     }
-    ebmax = max(ebmax, (int)(em >> (sizeof(T) == 8 ? 21 : 24)));
+    const uint32_t eb_lane = em >> (sizeof(T) == 8 ? 21 : 24);   // the lane's largest exponent field
+    ebmax = max(ebmax, (int)eb_lane);
     if (look) {
 #pragma unroll 1
       for (int i = 0; i < 16 && b + i < cnt; ++i) {
@@ -1084,17 +1103,13 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
     }
     const size_t li = (size_t)ch * 32 + lane;
     if constexpr (sizeof(T) == 8) {
-      // padding elements are zero and deposit nothing
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        ct_deposit((uint32_t)__double2hiint(v[i]), (uint32_t)__double2loint(v[i]), kc, c5, A, Bc);
       const fx::I192 own = ct_take(A, Bc);
       const fx::I192 exc = i192_warp_exclusive(own, &tot);
       const size_t plane = (size_t)nch * 32;
       uint64_t* lp = (uint64_t*)lanep;
       lp[li] = exc.w0;
       lp[plane + li] = exc.w1;
-      lp[2 * plane + li] = exc.w2;
+      lp[2 * plane + li] = lanep_pack(exc.w2, eb_lane);
     } else {
       // float primaries at the fixed index (the binned sum's deposit); lane
       // sums and chunk totals stay below 2^47
@@ -1108,7 +1123,7 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
         const int64_t o = (int64_t)__shfl_up_sync(0xffffffffu, (long long)inc, d);
         if (lane >= d) inc += o;
       }
-      ((int64_t*)lanep)[li] = inc - own;
+      ((int64_t*)lanep)[li] = (int64_t)lanep_pack((uint64_t)(inc - own), eb_lane);
       tot = i192_from_i64((int64_t)__shfl_sync(0xffffffffu, (long long)inc, 31));
     }
     __syncwarp();
@@ -1204,21 +1219,6 @@ __global__ void __launch_bounds__(CS_SCAN_THREADS) cf_scan(const fx::I192* __res
 // window results' exponent range is checked once for the lane; lanes
 // outside it, or with c < 0, take the general loop.
 
-// The lane's largest exponent field, over its valid elements.
-template <typename T>
-__device__ __forceinline__ uint32_t lane_exp_max(const T* buf, int sb, int b, int cnt) {
-  uint32_t em = 0;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    uint32_t hi;
-    if constexpr (sizeof(T) == 8) hi = (uint32_t)__double2hiint(buf[sb + i]);
-    else hi = __float_as_uint(buf[sb + i]);
-    const uint32_t e = (hi << 1) >> (sizeof(T) == 8 ? 21 : 24);
-    if (b + i < cnt) em = max(em, e);
-  }
-  return em;
-}
-
 __device__ __forceinline__ uint32_t lop3_or(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t r;
   asm("lop3.b32 %0, %1, %2, %3, 0xFE;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
@@ -1233,8 +1233,8 @@ __device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t b, uint32_
 // Double lanes, 128-bit totals (t1:t0).  Returns false, writing nothing,
 // when the lane cannot take the window.
 __device__ __forceinline__ bool cf_lane_window_f64(double* buf, int sb, int b, int cnt, uint64_t t0, uint64_t t1,
-                                                   const fx::FxConst& kc, int bf) {
-  const int e = max((int)lane_exp_max<double>(buf, sb, b, cnt), 1) - 1023;   // |x| < 2^(e + 1)
+                                                   const fx::FxConst& kc, int bf, uint32_t eb_lane) {
+  const int e = max((int)eb_lane, 1) - 1023;   // |x| < 2^(e + 1)
   const int A = e + 1 - bf;                                                   // |R| <= 2^A
   const uint64_t sg = (uint64_t)((int64_t)t1 >> 63);
   const uint64_t a1 = t1 ^ sg, a0 = t0 ^ sg;
@@ -1324,8 +1324,8 @@ __device__ __forceinline__ bool cf_lane_window_f64(double* buf, int sb, int b, i
 // holds for nearly every lane, and a per-element check measured slower
 // than the rare lanes that take the general loop.
 __device__ __forceinline__ bool cf_lane_window_f32(float* buf, int sb, int b, int cnt, int64_t t,
-                                                   const fx::F32Const& fk, int bf) {
-  const int e = max((int)lane_exp_max<float>(buf, sb, b, cnt), 1) - 127;
+                                                   const fx::F32Const& fk, int bf, uint32_t eb_lane) {
+  const int e = max((int)eb_lane, 1) - 127;
   const int A = e + 1 - bf;
   const uint64_t a = (uint64_t)(t ^ (t >> 63));
   const int p0 = 63 - __clzll((long long)a);   // 2^p0 <= |t| <= 2^(p0 + 1)
@@ -1366,14 +1366,14 @@ __device__ __forceinline__ bool cf_lane_window_f32(float* buf, int sb, int b, in
 // kernel's code stalled on instruction fetch.
 template <typename T, bool FULL>
 __device__ __forceinline__ void cf_replay_lanes(T* buf, int sb, int b, int cnt, fx::I192 t, const fx::FxConst& kc,
-                                                const fx::F32Const& fk, int bf) {
+                                                const fx::F32Const& fk, int bf, uint32_t eb_lane) {
   if constexpr (sizeof(T) == 8) {
     // Each rounded value is below 2^120 grid units, so a lane starting
     // below 2^126 in magnitude keeps its running total in 128 bits (the
     // usual case); otherwise 192.
     const uint64_t sx = (uint64_t)((int64_t)t.w1 >> 63);
     if (t.w2 == sx && ((int64_t)t.w1 >> 62) == ((int64_t)t.w1 >> 63)) {
-      if (cf_lane_window_f64(buf, sb, b, FULL ? 512 : cnt, t.w0, t.w1, kc, bf)) return;
+      if (cf_lane_window_f64(buf, sb, b, FULL ? 512 : cnt, t.w0, t.w1, kc, bf, eb_lane)) return;
       uint64_t t0 = t.w0, t1 = t.w1;
 #pragma unroll 8
       for (int i = 0; i < 16; ++i) {
@@ -1424,7 +1424,7 @@ __device__ __forceinline__ void cf_replay_lanes(T* buf, int sb, int b, int cnt, 
     const int64_t a0 = (int64_t)t.w0;
     const uint64_t sx = (uint64_t)(a0 >> 63);
     if (t.w1 == sx && t.w2 == sx && (a0 >> 62) == (a0 >> 63)) {
-      if (cf_lane_window_f32(buf, sb, b, FULL ? 512 : cnt, a0, fk, bf)) return;
+      if (cf_lane_window_f32(buf, sb, b, FULL ? 512 : cnt, a0, fk, bf, eb_lane)) return;
       uint32_t lo = (uint32_t)t.w0, hi = (uint32_t)(t.w0 >> 32);
 #pragma unroll 8
       for (int i = 0; i < 16; ++i) {
@@ -1493,21 +1493,26 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_replay(const T* in, T* out, int64
     const size_t li = (size_t)ch * 32 + lane;
     fx::I192 t = fx::i192_add(bpre[ch >> 10], lpre[ch]);
     const int b = lane * 16, sb = b + lane;
+    uint32_t eb_lane;
     if constexpr (sizeof(T) == 8) {
       const size_t plane = (size_t)nch * 32;
       const uint64_t* lp = (const uint64_t*)lanep;
-      t = fx::i192_add(t, fx::I192{lp[li], lp[plane + li], lp[2 * plane + li]});
+      const uint64_t w2 = lp[2 * plane + li];
+      eb_lane = lanep_exp(w2);
+      t = fx::i192_add(t, fx::I192{lp[li], lp[plane + li], lanep_word(w2)});
     } else {
-      t = fx::i192_add(t, i192_from_i64(((const int64_t*)lanep)[li]));
+      const uint64_t w = ((const uint64_t*)lanep)[li];
+      eb_lane = lanep_exp(w);
+      t = fx::i192_add(t, i192_from_i64((int64_t)lanep_word(w)));
     }
     __syncwarp();
     // float: full chunks without the per-element bound (measured faster);
     // double: one predicated body (the specialised copy costs registers)
     if constexpr (sizeof(T) == 4) {
-      if (cnt == CF_CHUNK) cf_replay_lanes<T, true>(buf, sb, b, cnt, t, kc, fk, bf);
-      else cf_replay_lanes<T, false>(buf, sb, b, cnt, t, kc, fk, bf);
+      if (cnt == CF_CHUNK) cf_replay_lanes<T, true>(buf, sb, b, cnt, t, kc, fk, bf, eb_lane);
+      else cf_replay_lanes<T, false>(buf, sb, b, cnt, t, kc, fk, bf, eb_lane);
     } else {
-      cf_replay_lanes<T, false>(buf, sb, b, cnt, t, kc, fk, bf);
+      cf_replay_lanes<T, false>(buf, sb, b, cnt, t, kc, fk, bf, eb_lane);
     }
     __syncwarp();
     T* g = out + c0;
