@@ -99,7 +99,7 @@ __device__ __forceinline__ void fx_deposit(uint32_t hi, uint32_t lo, const FxCon
   uint32_t w0 = funnel_l(0u, lo2, u);
   uint32_t w1 = funnel_l(lo2, mh2, u);
   uint32_t w2 = funnel_l(mh2, 0u, u);
-  uint32_t f1 = min(c, 1u), f0 = min(c >> 1, 1u);              // word c kept iff c >= 2, c + 1 iff c >= 1
+  uint32_t f1 = mad32(c, k.one, 127u) >> 7, f0 = mad32(c, k.one, 126u) >> 7;   // c >= 1, c >= 2
   uint32_t off = mad32(mad32(hi >> 31, k.c7, c), NT, 0u);
   uint64_t* p = A + off;
   uint32_t* pb = B + off;

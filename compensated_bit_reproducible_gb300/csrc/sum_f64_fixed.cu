@@ -27,7 +27,7 @@ namespace {
 
 constexpr int FX_U = 4;           // 16-byte vectors per thread per step
 constexpr int FX_J = 4;           // steps per chunk
-constexpr int FX_FOLD_CHUNKS = 31;   // 31 chunks x 32 deposits < 1024
+constexpr int FX_FOLD_CHUNKS = 992 / (2 * FX_U * FX_J);   // chunks between folds: at most 992 deposits
 
 // Control words, zero at launch; the kernel leaves them zero except the
 // fallback flag, which the general kernel clears.  The block totals are summed by
