@@ -887,6 +887,14 @@ __device__ __forceinline__ fx::I192 i192_add_signed(fx::I192 t, uint64_t rl, uin
   return i192_add_x(t, rl ^ sgn, rh ^ sgn, sgn);
 }
 
+// Asks L2 for the warp's next chunk (one 128-byte line per lane) while the
+// current one is processed.
+template <typename T>
+__device__ __forceinline__ void cf_prefetch_next(const T* in, int64_t n, int64_t ch_next, int lane) {
+  const int64_t i = ch_next * CF_CHUNK + (int64_t)lane * (128 / (int)sizeof(T));
+  if (i < n) asm volatile("prefetch.global.L2 [%0];" ::"l"(in + i));
+}
+
 // Coalesced copy of a chunk (cnt elements at g) into the warp's padded buffer.
 template <typename T>
 __device__ __forceinline__ void cf_stage(T* buf, const T* g, int cnt, int lane) {
@@ -1064,6 +1072,7 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
     const int64_t c0 = ch * CF_CHUNK;
     const int cnt = (int)min((int64_t)CF_CHUNK, n - c0);
     const bool look = c0 < C3_TILE;   // warp-uniform
+    cf_prefetch_next<T>(in, n, ch + GW, lane);
     fx::I192 tot;
     T* buf = sm + warp * CF_PAD;
     cf_stage<T>(buf, in + c0, cnt, lane);
@@ -1489,6 +1498,7 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_replay(const T* in, T* out, int64
   for (; ch < nch; ch += GW) {
     const int64_t c0 = ch * CF_CHUNK;
     const int cnt = (int)min((int64_t)CF_CHUNK, n - c0);
+    cf_prefetch_next<T>(in, n, ch + GW, lane);
     cf_stage<T>(buf, in + c0, cnt, lane);
     const size_t li = (size_t)ch * 32 + lane;
     fx::I192 t = fx::i192_add(bpre[ch >> 10], lpre[ch]);
