@@ -175,6 +175,22 @@ __device__ __forceinline__ I320 cx_take(uint64_t* A) {
   return t;
 }
 
+// Asks L2 for the warp's next chunk (one 128-byte line per lane) while the
+// current one is processed.
+__device__ __forceinline__ void cx_prefetch_next(const double* in, int64_t n, int64_t ch_next, int lane) {
+  const int64_t i = ch_next * CX_CHUNK + (int64_t)lane * 16;
+  if (i < n) asm volatile("prefetch.global.L2 [%0];" ::"l"(in + i));
+}
+
+// The lane prefix's top word (bits 256..319 of a value below 2^250 in
+// magnitude: copies of the sign) carries the lane's largest exponent field
+// in its top 16 bits; the replay takes it from there instead of rereading
+// the lane.
+__device__ __forceinline__ uint64_t cx_pack(uint64_t w, uint32_t eb) {
+  return (w & 0x0000FFFFFFFFFFFFull) | ((uint64_t)eb << 48);
+}
+__device__ __forceinline__ uint64_t cx_word(uint64_t w) { return (uint64_t)((int64_t)(w << 16) >> 16); }
+
 // Coalesced copy of a chunk (cnt elements at g) into the warp's padded buffer.
 __device__ __forceinline__ void cx_stage(double* buf, const double* g, int cnt, int lane) {
   if (cnt == CX_CHUNK && ((((uintptr_t)g) & 15) == 0)) {
@@ -231,15 +247,18 @@ __global__ void __launch_bounds__(CX_BLOCK) cx_totals(const double* __restrict__
     const int64_t c0 = ch * CX_CHUNK;
     const int cnt = (int)min((int64_t)CX_CHUNK, n - c0);
     double* buf = sm + warp * CX_PAD;
+    cx_prefetch_next(in, n, ch + GW, lane);
     cx_stage(buf, in + c0, cnt, lane);
     __syncwarp();
     const int b = lane * 16, sb = b + lane;
-    double v[16];
     uint32_t em = 0;
+    // each element deposited as it is read (padding elements are zero)
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      v[i] = b + i < cnt ? buf[sb + i] : 0.0;
-      em = max(em, (uint32_t)__double2hiint(v[i]) << 1);
+      const double x = b + i < cnt ? buf[sb + i] : 0.0;
+      const uint32_t hi = (uint32_t)__double2hiint(x);
+      em = max(em, hi << 1);
+      cx_deposit<STR>(hi, (uint32_t)__double2loint(x), kc, A);
     }
     ebmax = max(ebmax, (int)(em >> 21));
     if (c0 < CX_TILE) {
@@ -251,15 +270,13 @@ __global__ void __launch_bounds__(CX_BLOCK) cx_totals(const double* __restrict__
         }
       }
     }
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      cx_deposit<STR>((uint32_t)__double2hiint(v[i]), (uint32_t)__double2loint(v[i]), kc, A);
     const I320 own = cx_take<STR>(A);
     I320 tot;
     const I320 exc = i320_warp_exclusive(own, &tot);
     const size_t li = (size_t)ch * 32 + lane;
 #pragma unroll
-    for (int i = 0; i < 5; ++i) lanep[i * plane + li] = exc.w[i];
+    for (int i = 0; i < 4; ++i) lanep[i * plane + li] = exc.w[i];
+    lanep[4 * plane + li] = cx_pack(exc.w[4], em >> 21);
     __syncwarp();
     if (lane == 0) ctot[ch] = tot;
   }
@@ -272,27 +289,38 @@ __global__ void __launch_bounds__(CX_BLOCK) cx_totals(const double* __restrict__
 }
 
 // Pass 2: exclusive scan of the chunk totals.  Block b scans chunks
-// [1024 b, 1024 b + 1024) into lpre; the last block to finish scans the
-// block totals into bpre and decides the path.  Prefix of chunk c:
-// bpre[c >> 10] + lpre[c].
-__global__ void __launch_bounds__(1024) cx_scan(const I320* __restrict__ ctot, int64_t nch, CxCtl* ctl,
-                                                I320* __restrict__ lpre, I320* __restrict__ btot,
-                                                I320* __restrict__ bpre) {
-  __shared__ I320 sm[32];
+// [1024 b, 1024 b + 1024) into lpre (four consecutive chunks per thread);
+// the last block to finish scans the block totals into bpre and decides the
+// path.  Prefix of chunk c: bpre[c >> 10] + lpre[c].
+constexpr int CX_SCAN_THREADS = 256;
+__global__ void __launch_bounds__(CX_SCAN_THREADS) cx_scan(const I320* __restrict__ ctot, int64_t nch, CxCtl* ctl,
+                                                           I320* __restrict__ lpre, I320* __restrict__ btot,
+                                                           I320* __restrict__ bpre) {
+  constexpr int NW = CX_SCAN_THREADS / 32;
+  __shared__ I320 sm[NW];
   __shared__ bool last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t ci = (int64_t)blockIdx.x * 1024 + threadIdx.x;
-  const I320 v = ci < nch ? ctot[ci] : i320_zero();
+  const int64_t c0 = (int64_t)blockIdx.x * 1024 + 4 * threadIdx.x;
+  I320 v[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) v[j] = c0 + j < nch ? ctot[c0 + j] : i320_zero();
+  // inclusive prefixes of the thread's four chunks
+  const I320 p1 = fx::i320_add(v[0], v[1]), p2 = fx::i320_add(p1, v[2]), p3 = fx::i320_add(p2, v[3]);
   I320 wt;
-  const I320 exc = i320_warp_exclusive(v, &wt);
+  I320 exc = i320_warp_exclusive(p3, &wt);
   if (lane == 0) sm[warp] = wt;
   __syncthreads();
   I320 base = i320_zero(), all = i320_zero();
-  for (int w = 0; w < 32; ++w) {
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
     if (w < warp) base = fx::i320_add(base, sm[w]);
     all = fx::i320_add(all, sm[w]);
   }
-  if (ci < nch) lpre[ci] = fx::i320_add(base, exc);
+  exc = fx::i320_add(base, exc);
+  if (c0 < nch) lpre[c0] = exc;
+  if (c0 + 1 < nch) lpre[c0 + 1] = fx::i320_add(exc, v[0]);
+  if (c0 + 2 < nch) lpre[c0 + 2] = fx::i320_add(exc, p1);
+  if (c0 + 3 < nch) lpre[c0 + 3] = fx::i320_add(exc, p2);
   if (threadIdx.x == 0) {
     btot[blockIdx.x] = all;
     __threadfence();
@@ -302,7 +330,7 @@ __global__ void __launch_bounds__(1024) cx_scan(const I320* __restrict__ ctot, i
   if (!last) return;
   __threadfence();
   const int64_t nb = gridDim.x;
-  const int64_t per = (nb + 1023) / 1024;
+  const int64_t per = (nb + CX_SCAN_THREADS - 1) / CX_SCAN_THREADS;
   const int64_t b0 = (int64_t)threadIdx.x * per, b1 = min(nb, b0 + per);
   I320 agg = i320_zero();
   for (int64_t i = b0; i < b1; ++i) agg = fx::i320_add(agg, i320_ldcg(btot + i));
@@ -343,18 +371,14 @@ __device__ __forceinline__ int i320_lead(const uint32_t* x) {
 // over the staged inputs.
 template <int K>
 __device__ __forceinline__ void cx_replay_lane(double* buf, int sb, int b, int cnt, const I320& t,
-                                               const fx::FxConst& kc, int bf) {
+                                               const fx::FxConst& kc, int bf, uint32_t em) {
   uint32_t x[10];
 #pragma unroll
   for (int i = 0; i < 5; ++i) {
     x[2 * i] = (uint32_t)t.w[i];
     x[2 * i + 1] = (uint32_t)(t.w[i] >> 32);
   }
-  // lane bound: |R| <= 2^A for its elements
-  uint32_t em = 0;
-#pragma unroll
-  for (int i = 0; i < 16; ++i)
-    if (b + i < cnt) em = max(em, ((uint32_t)__double2hiint(buf[sb + i]) << 1) >> 21);
+  // lane bound: |R| <= 2^A for its elements (em: their largest exponent field)
   const int A = max((int)em, 1) - 1023 + 1 - bf;
   const int p0 = i320_lead(x);                   // |t| <= 2^(p0 + 1)
   const int pu = max(p0 + 1, A + 4) + 1;          // every prefix of the lane is below 2^pu
@@ -477,15 +501,18 @@ __global__ void __launch_bounds__(CX_BLOCK) cx_replay(const double* in, double* 
   for (; ch < nch; ch += GW) {
     const int64_t c0 = ch * CX_CHUNK;
     const int cnt = (int)min((int64_t)CX_CHUNK, n - c0);
+    cx_prefetch_next(in, n, ch + GW, lane);
     cx_stage(buf, in + c0, cnt, lane);
     const size_t li = (size_t)ch * 32 + lane;
     I320 t = fx::i320_add(bpre[ch >> 10], lpre[ch]);
     I320 lp;
 #pragma unroll
-    for (int i = 0; i < 5; ++i) lp.w[i] = lanep[i * plane + li];
+    for (int i = 0; i < 4; ++i) lp.w[i] = lanep[i * plane + li];
+    const uint64_t top = lanep[4 * plane + li];
+    lp.w[4] = cx_word(top);
     t = fx::i320_add(t, lp);
     __syncwarp();
-    cx_replay_lane<K>(buf, lane * 17, lane * 16, cnt, t, kc, bf);
+    cx_replay_lane<K>(buf, lane * 17, lane * 16, cnt, t, kc, bf, (uint32_t)(top >> 48));
     __syncwarp();
     double* g = out + c0;
     if (cnt == CX_CHUNK && ((((uintptr_t)g) & 15) == 0)) {
@@ -562,7 +589,7 @@ cudaError_t launch_fx_k(const double* in, double* out, int64_t n, unsigned char*
   const int64_t wb = (nc + CX_WARPS - 1) / CX_WARPS;   // blocks that have a chunk
   const int64_t gt = max((int64_t)1, min(wb, sms * max(bt, 1))), gr = max((int64_t)1, min(wb, sms * max(br, 1)));
   cx_totals<K><<<(unsigned)gt, CX_BLOCK, cx_cell_bytes<K>(), s>>>(in, n, nc, 1u, ctl, lanep, ctot);
-  cx_scan<<<(unsigned)ncb, 1024, 0, s>>>(ctot, nc, ctl, lpre, btot, bpre);
+  cx_scan<<<(unsigned)ncb, CX_SCAN_THREADS, 0, s>>>(ctot, nc, ctl, lpre, btot, bpre);
   cx_replay<K><<<(unsigned)gr, CX_BLOCK, 0, s>>>(in, out, n, nc, 1u, ctl, lanep, lpre, bpre);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // the first tile per fold when the index settles inside it (reads only its
