@@ -737,17 +737,16 @@ static cudaError_t launch_cumsum_generic(const T* in, T* out, int64_t n, int K, 
 }
 
 template <typename T>
-cudaError_t launch_cumsum(const T* in, T* out, int64_t n, int K, unsigned char* ws, int block, cudaStream_t s,
+cudaError_t launch_cumsum(const T* in, T* out, int64_t n, int K, unsigned char* ws, unsigned char* zc, cudaStream_t s,
                           const unsigned char* carry) {
-  (void)block;
   switch (K) {
     case 2: return launch_cumsum_k<T, 2>(in, out, n, K, ws, s, nullptr, carry);
-    case 3: return launch_cumsum_k3<T>(in, out, n, ws, s, carry);
+    case 3: return launch_cumsum_k3<T>(in, out, n, ws, zc, s, carry);
     case 4:
     case 5:
     case 6:
       if constexpr (sizeof(T) == 8) {
-        if (!carry) return launch_cumsum_fx(in, out, n, K, ws, s);
+        if (!carry) return launch_cumsum_fx(in, out, n, K, ws, zc, s);
       }
       if (K == 4) return launch_cumsum_k<T, 4>(in, out, n, K, ws, s, nullptr, carry);
       if (K == 5) return launch_cumsum_k<T, 5>(in, out, n, K, ws, s, nullptr, carry);
@@ -770,9 +769,9 @@ template size_t cumsum_carry_workspace_bytes<double>(int64_t, int);
 
 template size_t cumsum_workspace_bytes<float>(int64_t, int);
 template size_t cumsum_workspace_bytes<double>(int64_t, int);
-template cudaError_t launch_cumsum<float>(const float*, float*, int64_t, int, unsigned char*, int, cudaStream_t,
-                                          const unsigned char*);
-template cudaError_t launch_cumsum<double>(const double*, double*, int64_t, int, unsigned char*, int,
+template cudaError_t launch_cumsum<float>(const float*, float*, int64_t, int, unsigned char*, unsigned char*,
+                                          cudaStream_t, const unsigned char*);
+template cudaError_t launch_cumsum<double>(const double*, double*, int64_t, int, unsigned char*, unsigned char*,
                                            cudaStream_t, const unsigned char*);
 
 }  // namespace repro

@@ -89,6 +89,7 @@ cudaError_t ws_alloc(void** p, size_t bytes, cudaStream_t stream) {
 constexpr size_t CTL_PAGE_BYTES = 4096;
 constexpr size_t CTL_SUM_TICKET = 0;      // general sum kernel's ticket
 constexpr size_t CTL_SUM_FIXED = 256;     // double fixed-index sum's control words
+constexpr size_t CTL_CUMSUM = 2048;       // cumulative sums' control words (256 bytes)
 
 cudaError_t ctl_page(cudaStream_t stream, unsigned char** out) {
   static std::mutex mu;
@@ -375,7 +376,9 @@ repro_status cumsum_impl(const T* in, T* out, size_t n, int K, cudaStream_t stre
   ws.s = stream;
   const size_t wsb = cumsum_workspace_bytes<T>((int64_t)n, K);
   if (wsb) CK(ws_alloc(&ws.p, wsb, stream));   // none for a single tile
-  CK(launch_cumsum<T>(din, dout, (int64_t)n, K, (unsigned char*)ws.p, l ? l->block : 0, stream));
+  unsigned char* page = nullptr;
+  CK(ctl_page(stream, &page));
+  CK(launch_cumsum<T>(din, dout, (int64_t)n, K, (unsigned char*)ws.p, page + CTL_CUMSUM, stream));
   if (hout) {
     CK(cudaMemcpyAsync(out, dout, n * sizeof(T), cudaMemcpyDeviceToHost, stream));
     CK(cudaStreamSynchronize(stream));
@@ -402,7 +405,10 @@ repro_status cumsum_from_state_impl(const T* in, T* out, size_t n, int K, const 
   ws.s = stream;
   const size_t wsb = cumsum_carry_workspace_bytes<T>((int64_t)n, K);
   if (wsb) CK(ws_alloc(&ws.p, wsb, stream));
-  CK(launch_cumsum<T>(in, out, (int64_t)n, K, (unsigned char*)ws.p, 0, stream, (const unsigned char*)state));
+  unsigned char* page = nullptr;
+  CK(ctl_page(stream, &page));
+  CK(launch_cumsum<T>(in, out, (int64_t)n, K, (unsigned char*)ws.p, page + CTL_CUMSUM, stream,
+                      (const unsigned char*)state));
   return REPRO_OK;
 }
 

@@ -48,7 +48,9 @@ constexpr int CX_PAD = CX_CHUNK + CX_CHUNK / 16;   // staged chunk with one pad 
 constexpr int CX_TILE = 4096;                      // first tile: recomputed per fold when 0 < i* < 4096
 constexpr int64_t CX_MIN_N = 1 << 17;              // below: the general kernels alone
 
-struct CxCtl {                 // in the zeroed workspace header
+struct CxCtl {                 // in the stream's control page: zero at the call, and fail,
+                               // istar and ticket left zero by the scan; the other words
+                               // are written before they are read
   unsigned fail;               // guess failed / Inf, NaN / index too fine
   unsigned general;            // set by the scan: the general kernels compute everything
   int L;                       // the guessed index (written by block 0)
@@ -351,6 +353,11 @@ __global__ void __launch_bounds__(CX_SCAN_THREADS) cx_scan(const I320* __restric
     const bool general = ctl->fail != 0u || istar >= (int64_t)CX_TILE;
     ctl->general = general ? 1u : 0u;
     ctl->tile0 = (!general && istar > 0) ? 1u : 0u;
+    // every block has taken its ticket and the totals pass has ended: the
+    // accumulated words are left zero for the next call on the stream
+    ctl->fail = 0u;
+    ctl->istar = 0ull;
+    ctl->ticket = 0u;
   }
 }
 
@@ -557,10 +564,11 @@ size_t cx_fast_bytes(int64_t n) {
 }
 
 template <int K>
-cudaError_t launch_fx_k(const double* in, double* out, int64_t n, unsigned char* ws, cudaStream_t s) {
+cudaError_t launch_fx_k(const double* in, double* out, int64_t n, unsigned char* ws, unsigned char* zc,
+                        cudaStream_t s) {
   const size_t gb = (cumsum_general_bytes(n, K) + 255) & ~(size_t)255;
   unsigned char* f = ws + gb;
-  CxCtl* ctl = (CxCtl*)f;
+  CxCtl* ctl = (CxCtl*)zc;
   const int64_t nc = (n + CX_CHUNK - 1) / CX_CHUNK;
   const int64_t ncb = (nc + 1023) / 1024;
   uint64_t* lanep = (uint64_t*)(f + 256);
@@ -569,7 +577,6 @@ cudaError_t launch_fx_k(const double* in, double* out, int64_t n, unsigned char*
   I320* btot = lpre + nc;
   I320* bpre = btot + ncb;
   cudaError_t e;
-  if ((e = cudaMemsetAsync(ctl, 0, 256, s)) != cudaSuccess) return e;
   static bool attr_set[64] = {};
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -607,12 +614,13 @@ size_t cumsum_fx_workspace_bytes(int64_t n, int K) {
   return n >= CX_MIN_N ? gb + cx_fast_bytes(n) : cumsum_general_bytes(n, K);
 }
 
-cudaError_t launch_cumsum_fx(const double* in, double* out, int64_t n, int K, unsigned char* ws, cudaStream_t s) {
+cudaError_t launch_cumsum_fx(const double* in, double* out, int64_t n, int K, unsigned char* ws, unsigned char* zc,
+                             cudaStream_t s) {
   if (n < CX_MIN_N) return launch_cumsum_general<double>(in, out, n, K, ws, s, nullptr);
   switch (K) {
-    case 4: return launch_fx_k<4>(in, out, n, ws, s);
-    case 5: return launch_fx_k<5>(in, out, n, ws, s);
-    case 6: return launch_fx_k<6>(in, out, n, ws, s);
+    case 4: return launch_fx_k<4>(in, out, n, ws, zc, s);
+    case 5: return launch_fx_k<5>(in, out, n, ws, zc, s);
+    case 6: return launch_fx_k<6>(in, out, n, ws, zc, s);
     default: return cudaErrorInvalidValue;
   }
 }

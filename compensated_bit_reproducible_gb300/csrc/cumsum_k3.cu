@@ -809,7 +809,9 @@ __global__ void __launch_bounds__(C3_BLOCK) c3_replay(const T* in, T* out, int64
 // the tile totals; pass 3 (replay) starts each thread from tile prefix +
 // thread prefix and converts after every element.
 
-struct CsCtl {                 // in the zeroed workspace header
+struct CsCtl {                 // in the stream's control page: zero at the call, and fail,
+                               // istar and ticket left zero by the scan; the other words
+                               // are written before they are read
   unsigned fail;               // guess failed / Inf, NaN / index too fine
   unsigned general;            // set by the scan: the general path runs
   int L;                       // the guessed index (written by block 0)
@@ -993,10 +995,13 @@ __device__ __forceinline__ fx::I192 ct_take(uint64_t* A, uint32_t* B) {
   fx::I192 t{0, 0, 0};
 #pragma unroll
   for (int c = 0; c < 5; ++c) {
-    const uint64_t ap = A[c * C3_BLOCK], an = A[(c + 5) * C3_BLOCK];
+    // A at position 0 only ever receives zero words: not read, not cleared
+    const uint64_t ap = c ? A[c * C3_BLOCK] : 0ull, an = c ? A[(c + 5) * C3_BLOCK] : 0ull;
     const uint32_t bp = B[c * C3_BLOCK], bn = B[(c + 5) * C3_BLOCK];
-    A[c * C3_BLOCK] = 0;
-    A[(c + 5) * C3_BLOCK] = 0;
+    if (c) {
+      A[c * C3_BLOCK] = 0;
+      A[(c + 5) * C3_BLOCK] = 0;
+    }
     B[c * C3_BLOCK] = 0;
     B[(c + 5) * C3_BLOCK] = 0;
     uint32_t d0, d1, d2;
@@ -1212,6 +1217,11 @@ __global__ void __launch_bounds__(CS_SCAN_THREADS) cf_scan(const fx::I192* __res
     const int64_t istar = code ? (int64_t)(0x7FFFFFFFFFFFFFFFull - code) : INT64_MAX;
     ctl->general = (ctl->fail != 0u || istar >= (int64_t)C3_TILE) ? 1u : 0u;
     ctl->exact0 = (istar > 0) ? 1u : 0u;   // the first tile needs the per-fold replay
+    // every block has taken its ticket and the totals pass has ended: the
+    // accumulated words are left zero for the next call on the stream
+    ctl->fail = 0u;
+    ctl->istar = 0ull;
+    ctl->ticket = 0u;
   }
 }
 
@@ -1635,7 +1645,7 @@ size_t cumsum_k3_workspace_bytes(int64_t n) {
 }
 
 template <typename T>
-cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, cudaStream_t s,
+cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, unsigned char* zc, cudaStream_t s,
                              const unsigned char* carry) {
   if (n <= C3_TILE && !carry) {
     c3_single_tile<T><<<1, C3_BLOCK, 0, s>>>(in, out, n);
@@ -1654,7 +1664,7 @@ cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, 
   if (n >= CF_MIN_N && !carry) {
     // fixed-index fast path; the general kernels below become its gated fallback
     unsigned char* f = ws + c3_general_bytes<T>(n);
-    CsCtl* ctl = (CsCtl*)f;
+    CsCtl* ctl = (CsCtl*)zc;
     const int64_t nc = (n + CF_CHUNK - 1) / CF_CHUNK;
     const int64_t ncb = (nc + 1023) / 1024;
     unsigned char* lanep = f + 256;
@@ -1662,7 +1672,6 @@ cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, 
     fx::I192* lpre = ctot + nc;
     fx::I192* btot = lpre + nc;
     fx::I192* bpre = btot + ncb;
-    if ((e = cudaMemsetAsync(ctl, 0, 256, s)) != cudaSuccess) return e;
     if ((e = ct_prepare<T>()) != cudaSuccess) return e;
     int bt = 0, br = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bt, cf_totals<T>, C3_BLOCK, ct_cell_bytes<T>()) !=
@@ -1698,9 +1707,9 @@ cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, 
 
 template size_t cumsum_k3_workspace_bytes<float>(int64_t);
 template size_t cumsum_k3_workspace_bytes<double>(int64_t);
-template cudaError_t launch_cumsum_k3<float>(const float*, float*, int64_t, unsigned char*, cudaStream_t,
-                                             const unsigned char*);
-template cudaError_t launch_cumsum_k3<double>(const double*, double*, int64_t, unsigned char*, cudaStream_t,
-                                              const unsigned char*);
+template cudaError_t launch_cumsum_k3<float>(const float*, float*, int64_t, unsigned char*, unsigned char*,
+                                             cudaStream_t, const unsigned char*);
+template cudaError_t launch_cumsum_k3<double>(const double*, double*, int64_t, unsigned char*, unsigned char*,
+                                              cudaStream_t, const unsigned char*);
 
 }  // namespace repro

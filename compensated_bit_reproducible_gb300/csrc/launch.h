@@ -46,10 +46,12 @@ cudaError_t launch_segsum(const float* x, int64_t rows, int64_t cols, int axis, 
 // binned cumulative sum
 template <typename T>
 size_t cumsum_workspace_bytes(int64_t n, int K);
-// carry: null, or a device binned state (repro_state layout) that every
-// prefix includes; such calls take the general per-fold kernels.
+// zc: 256 bytes of control words, zero at the call and left zero (the
+// stream's control page).  carry: null, or a device binned state
+// (repro_state layout) that every prefix includes; such calls take the
+// general per-fold kernels.
 template <typename T>
-cudaError_t launch_cumsum(const T* in, T* out, int64_t n, int K, unsigned char* ws, int block, cudaStream_t s,
+cudaError_t launch_cumsum(const T* in, T* out, int64_t n, int K, unsigned char* ws, unsigned char* zc, cudaStream_t s,
                           const unsigned char* carry = nullptr);
 // The general per-fold kernels for K = 4..6 on doubles, optionally gated (see
 // adn_cumsum.cu), and their workspace.
@@ -60,7 +62,8 @@ size_t cumsum_general_bytes(int64_t n, int K);
 // Doubles with K = 4..6 (cumsum_fx.cu): the fixed-index path for long inputs,
 // the general kernels otherwise.
 size_t cumsum_fx_workspace_bytes(int64_t n, int K);
-cudaError_t launch_cumsum_fx(const double* in, double* out, int64_t n, int K, unsigned char* ws, cudaStream_t s);
+cudaError_t launch_cumsum_fx(const double* in, double* out, int64_t n, int K, unsigned char* ws, unsigned char* zc,
+                             cudaStream_t s);
 template <typename T>
 size_t cumsum_k3_workspace_bytes(int64_t n);
 template <typename T>
@@ -68,7 +71,7 @@ size_t cumsum_k3_general_bytes(int64_t n);
 template <typename T>
 size_t cumsum_carry_workspace_bytes(int64_t n, int K);
 template <typename T>
-cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, cudaStream_t s,
+cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, unsigned char* zc, cudaStream_t s,
                              const unsigned char* carry = nullptr);
 
 // variance

@@ -182,7 +182,9 @@ repro_status repro_cumsum_from_state_f64(const double* in, double* out, size_t n
    stream-ordered (returns once enqueued).  Plain host memory ("Pointer type
    handling"): a host input is copied to temporary device memory, a host
    output is computed there and copied back, and the call then returns only
-   when out holds the result. */
+   when out holds the result.  The *_ex forms check the launch shape (an
+   invalid one gives REPRO_ERR_INVALID_ARG) but the cumulative sums run
+   their own block sizes. */
 repro_status repro_cumsum_f32(const float* in, float* out, size_t n, int K, cudaStream_t stream);
 repro_status repro_cumsum_f64(const double* in, double* out, size_t n, int K, cudaStream_t stream);
 repro_status repro_cumsum_f32_ex(const float* in, float* out, size_t n, int K, cudaStream_t stream,
