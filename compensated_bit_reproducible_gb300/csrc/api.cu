@@ -267,34 +267,27 @@ repro_status sum_async_impl(const T* x, size_t n, int K, cudaStream_t stream, T*
       if (CTL_SUM_FIXED + sum_f64_fixed_ctl_bytes() > CTL_PAGE_BYTES) fgrid = 0;
     }
   }
-  // tickets and control words in the stream's page (zero between calls);
-  // the general kernel's partials in a workspace
+  // tickets and control words in the stream's page (zero between calls)
   unsigned char* page = nullptr;
   CK(ctl_page(stream, &page));
+  if constexpr (sizeof(T) == 8) {
+    if (fgrid > 0) {
+      // first pass at the sampled index, then the second pass: idle unless
+      // the first one missed (an element above the guessed bin, an index too
+      // fine for its shortcut, Inf or NaN); then it recomputes the sum at the
+      // index of the largest exponent, or finds which specials occur
+      unsigned* ctl = (unsigned*)(page + CTL_SUM_FIXED);
+      CK(launch_sum_f64_fixed((const double*)x, (int64_t)n, K, ctl, (double*)result_dev, fgrid, fblock, 0, stream));
+      CK(launch_sum_f64_fixed((const double*)x, (int64_t)n, K, ctl, (double*)result_dev, fgrid, fblock, 1, stream));
+      return REPRO_OK;
+    }
+  }
+  // the general one-pass kernel; its partials in a workspace
   unsigned* ticket = (unsigned*)(page + CTL_SUM_TICKET);
   Scratch ws;
   ws.s = stream;
   CK(ws_alloc(&ws.p, sum_workspace_bytes(K, grid), stream));
-  unsigned char* w = (unsigned char*)ws.p;
-  if constexpr (sizeof(T) == 8) {
-    if (fgrid > 0) {
-      unsigned* ctl = (unsigned*)(page + CTL_SUM_FIXED);
-      CK(launch_sum_f64_fixed((const double*)x, (int64_t)n, K, ctl, (double*)result_dev, fgrid, fblock, stream));
-      // the fallback runs when the guess misses: four blocks per SM keep its
-      // idle launch short and still fill the GPU when it runs (measured on a
-      // 1e8 sum with one value above the sampled bins: 1.06 ms with one block
-      // per SM, 0.60 with four, no faster with eight; the seeded sum the same
-      // in all three); also enough blocks for the per-thread limit of 2^23
-      int64_t need = ((int64_t)n + ((int64_t)block << 23) - 1) / ((int64_t)block << 23);
-      const int64_t fcap = 4 * (int64_t)sm_count();
-      int64_t fb = grid < fcap ? grid : fcap;
-      int fb_grid = (int)(fb > need ? fb : need);
-      if (l && l->grid > 0) fb_grid = grid;
-      CK(launch_sum<T>(x, (int64_t)n, K, ticket, w, result_dev, fb_grid, block, stream, ctl + 2));
-      return REPRO_OK;
-    }
-  }
-  CK(launch_sum<T>(x, (int64_t)n, K, ticket, w, result_dev, grid, block, stream));
+  CK(launch_sum<T>(x, (int64_t)n, K, ticket, (unsigned char*)ws.p, result_dev, grid, block, stream));
   return REPRO_OK;
 }
 

@@ -82,15 +82,26 @@ struct FxConst {
 // 2).  B takes at most 2^22 per deposit and is emptied by fx_fold every 992
 // deposits.  An element beyond the bin (flagged through umax) lands at
 // position STR - 2, in bounds.  k.c7 must be (STR - 1) k.one.
-template <int STR = STRIDE>
+// SUBN: subnormal inputs take their true significand (no hidden bit,
+// exponent field read as 1), for grids fine enough to see them; without it
+// the hidden bit is forced, which is exact whenever g_f / 2 lies above every
+// subnormal.
+template <int STR = STRIDE, bool SUBN = false>
 __device__ __forceinline__ void fx_deposit(uint32_t hi, uint32_t lo, const FxConst& k, uint64_t* A, uint32_t* B,
                                            uint32_t NT, int& umax) {
   uint32_t eb = mad32(hi, k.one + k.one, 0u) >> 21;          // biased exponent
+  uint32_t mh;
+  if constexpr (SUBN) {
+    const uint32_t nz = min(eb, 1u);                          // 0 for a subnormal or zero
+    mh = (hi & 0xFFFFFu) | mad32(nz, 0x100000u * k.one, 0u);
+    eb = max(eb, 1u);
+  } else {
+    mh = (hi & 0xFFFFFu) | 0x100000u;
+  }
   int us = (int)mad32(eb, k.one, k.Cp);                       // shift of M
   umax = max(umax, us);
   uint32_t u = (uint32_t)max(us, 0);   // tiny values: their words stay below position 2
   uint32_t c = min(u >> 5, (uint32_t)(STR - 2));
-  uint32_t mh = (hi & 0xFFFFFu) | 0x100000u;
   uint32_t hl = shl_clamp32(1u, (int)mad32(u, k.negone, k.c63));
   uint32_t hh = shl_clamp32(1u, (int)mad32(u, k.negone, k.c31));
   uint32_t b = min(mh & mad32(hl, k.c256, 0u), 1u);          // bit 103 of P': rounding bit of fold K-2
@@ -257,6 +268,17 @@ __device__ __forceinline__ TOT fx_thread_total(const uint64_t* A, const uint32_t
   return tot_add(t[0], tot_neg(t[1]));
 }
 
+// Bin index of a set whose largest biased exponent field is eb (0: all
+// zero or subnormal), capped at NB - K.
+template <typename T>
+__device__ __forceinline__ int index_of_exponent(int eb, int K) {
+  typedef Geom<T> G;
+  if (eb == 0) return G::NB - K;
+  int j = (G::B0 + G::W - 2 - (eb - G::BIAS)) / G::W;
+  j = min(j, G::NB - 1);
+  return min(j, G::NB - K);
+}
+
 // Index guess from the largest exponent field over SAMPLE evenly spaced
 // elements (every block computes the same value).  Returns the bin index;
 // *emax_out gets the largest biased exponent seen (all-ones: Inf/NaN).
@@ -283,10 +305,7 @@ __device__ __forceinline__ int guess_index(const T* __restrict__ x, int64_t n, i
   __syncthreads();
   const int eb = (int)(*s_emax >> ESH);
   *emax_out = eb;
-  if (eb == 0) return G::NB - K;
-  int j = (G::B0 + G::W - 2 - (eb - G::BIAS)) / G::W;
-  j = min(j, G::NB - 1);
-  return min(j, G::NB - K);
+  return index_of_exponent<T>(eb, K);
 }
 
 // Largest biased exponent inside bin I: |x| < 2^(beta_I + W - 1).

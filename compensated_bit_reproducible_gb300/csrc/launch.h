@@ -8,10 +8,10 @@ namespace repro {
 
 // binned sum.  ticket: a zero counter (zero again after the call); parts:
 // one partial state of 16 + 16 K bytes per block (sum_workspace_bytes(K,
-// grid) bytes suffice); gate: see adn_sum_kernel.
+// grid) bytes suffice); gate, gate_final: see adn_sum_kernel.
 template <typename T>
 cudaError_t launch_sum(const T* x, int64_t n, int K, unsigned* ticket, unsigned char* parts, T* result, int grid,
-                       int block, cudaStream_t s, unsigned* gate = nullptr);
+                       int block, cudaStream_t s, unsigned* gate = nullptr, int gate_final = 0);
 // One block, no workspace: the single-block sum for small inputs.
 template <typename T>
 cudaError_t launch_sum_single(const T* x, int64_t n, int K, T* result, int block, cudaStream_t s,
@@ -30,16 +30,20 @@ cudaError_t launch_state_op(int op, unsigned char* dst, const unsigned char* src
 size_t sum_workspace_bytes(int K, int grid);
 template <typename T>
 int sum_blocks_per_sm(int K, int block);
-// double sum at a sampled fixed index (K = 2..6): blocks per GPU for this
-// block size (0: not available), size of the control words, launch.  ctl
-// points at sum_f64_fixed_ctl_bytes() zero bytes (16-byte aligned), which
-// the kernel leaves zero except ctl[2]: it becomes nonzero when the general
-// kernel must compute the result (pass it as that kernel's gate, which that
-// kernel clears).
+// double sum at a fixed index (K = 2..6): blocks per GPU for this block
+// size (0: not available), size of the control words, launch.  The first
+// pass (second = 0) guesses the index from a sample; launched right after
+// it, the second pass (second = 1) runs only when an element lay above the
+// guessed bin, at the index of the largest exponent.  ctl points at
+// sum_f64_fixed_ctl_bytes() zero bytes (16-byte aligned), which the two
+// leave zero except ctl[2]: it becomes nonzero when neither can compute the
+// result and the general kernel must (pass it as that kernel's gate, read
+// without waiting: it is set before the second pass lets later kernels
+// start; that kernel clears it).
 int sum_f64_fixed_grid(int K, int block, int sms);
 size_t sum_f64_fixed_ctl_bytes();
 cudaError_t launch_sum_f64_fixed(const double* x, int64_t n, int K, unsigned* ctl, double* result, int grid,
-                                 int block, cudaStream_t s);
+                                 int block, int second, cudaStream_t s);
 cudaError_t launch_segsum(const float* x, int64_t rows, int64_t cols, int axis, int K, float* out, int grid,
                           int block, cudaStream_t s);
 

@@ -15,6 +15,7 @@
 // every 992 deposits.  K sets only how many positions there are (7 for
 // K <= 3, 10 for K = 6) and the width of the block total (192 or 320 bits):
 // an element's three words are the same for any K.
+#include <climits>
 #include "accum.cuh"
 #include "fixed_index.cuh"
 #include "launch.h"
@@ -37,10 +38,15 @@ constexpr int FX_FOLD_CHUNKS = 992 / (2 * FX_U * FX_J);   // chunks between fold
 constexpr int FX_DIGITS = 10;   // 320-bit totals
 constexpr int FX_DIG_STRIDE = 16;   // 64-bit words between two accumulators
 struct FixedCtl {
-  unsigned queue;    // next chunk of the dynamic queue (after the first gridDim.x)
-  unsigned ticket;   // finished blocks
-  unsigned fail;     // nonzero: the general pass computes the result
-  unsigned pad[29];
+  unsigned queue;     // next chunk of the dynamic queue (after the first gridDim.x)
+  unsigned ticket;    // finished blocks
+  unsigned general;   // unused by these kernels (the general kernel's gate when it follows them)
+  unsigned fail;      // some block of the first pass left the guessed bin
+  unsigned emax;      // largest biased exponent field the first pass deposited
+  unsigned run2;      // set by the first pass's last block: 1 the second pass deposits, 2 it scans for Inf/NaN
+  int I2;             // the second pass's index (from emax)
+  unsigned sflags;    // the second pass's Inf/NaN flags (emax all ones)
+  unsigned pad[24];
   unsigned long long dig[FX_DIGITS * FX_DIG_STRIDE];
 };
 
@@ -93,7 +99,7 @@ __device__ __forceinline__ void fx_folds(const I320& tot, W128* F) {
   F[0] = W128{lo, (int64_t)hi};
 }
 
-template <int K, int CNT>
+template <int K, int CNT, bool SECOND>
 __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
     sum_f64_fixed_kernel(const double* __restrict__ x, int64_t n, uint32_t one, FixedCtl* ctl,
                          double* __restrict__ result) {
@@ -105,9 +111,49 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
   uint32_t* B = (uint32_t*)(fx_smem + (size_t)Geo::CELLS * 8 * NT) + threadIdx.x;
   __shared__ unsigned s_emax;
 
-  // the gated fallback kernel may start launching now; it waits for this
-  // grid to complete before it reads the flag
-  asm volatile("griddepcontrol.launch_dependents;");
+  __shared__ bool last;
+  if constexpr (SECOND) {
+    // the second pass: launched as a programmatic dependent of the first, it
+    // waits for that grid and runs only if the first one asked for it
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const unsigned mode = __ldcg(&ctl->run2);
+    if (mode == 0u) return;
+    if (mode == 2u) {
+      // the largest exponent field is all ones: the result is Inf or NaN,
+      // set by which specials occur (one pass over the input, no deposits)
+      __shared__ unsigned s_fl;
+      if (threadIdx.x == 0) s_fl = 0u;
+      __syncthreads();
+      unsigned fl = 0u;
+      const int64_t G_ = (int64_t)gridDim.x * NT;
+      for (int64_t i = (int64_t)blockIdx.x * NT + threadIdx.x; i < n; i += G_) {
+        const double v = __ldcs(x + i);
+        if ((((uint32_t)__double2hiint(v)) & 0x7FF00000u) == 0x7FF00000u) fl |= (unsigned)special_flag<double>(v);
+      }
+      fl = __reduce_or_sync(0xffffffffu, fl);
+      if ((threadIdx.x & 31) == 0 && fl) atomicOr(&s_fl, fl);
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        if (s_fl) atomicOr(&ctl->sflags, s_fl);
+        __threadfence();
+        last = atomicAdd(&ctl->ticket, 1u) == gridDim.x - 1;
+      }
+      __syncthreads();
+      if (!last || threadIdx.x != 0) return;
+      __threadfence();
+      const int f = (int)__ldcg(&ctl->sflags);
+      ctl->sflags = 0u;
+      ctl->ticket = 0u;
+      ctl->run2 = 0u;
+      ctl->emax = 0u;
+      *result = from_flags<double>(f);
+      return;
+    }
+  } else {
+    // the second pass may start launching now; it waits for this grid to
+    // complete before it reads its flag
+    asm volatile("griddepcontrol.launch_dependents;");
+  }
   // Chunks of CV 16-byte vectors from the first 16-byte boundary on.  Block
   // b takes chunk b first and the rest from a dynamic queue; the first step
   // of chunk b is loaded before the index guess, so its latency overlaps
@@ -123,13 +169,16 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
 #pragma unroll
     for (int q = 0; q < FX_U; ++q) v0[q] = __ldcs(xv + (int64_t)blockIdx.x * CV + threadIdx.x + (int64_t)q * NT);
   }
-  // 1. Index guess from a sample.
-  int eb_max;
-  const int Ig = guess_index<double>(x, n, K, &s_emax, &eb_max);
+  // 1. Index: the first pass guesses it from a sample; the second takes the
+  // one the first pass's last block derived from the largest exponent.
+  int eb_max = 0;
+  const int Ig = SECOND ? __ldcg(&ctl->I2) : guess_index<double>(x, n, K, &s_emax, &eb_max);
   const int bf = beta<double>(Ig + K - 1);
-  // the shortcuts need g_f/2 above every subnormal and every x with a forced
-  // hidden bit below the grid: beta_f >= -1019; Inf/NaN in the sample fail too
-  const bool usable = (bf >= -1019) && (eb_max < 0x7FF);
+  // The first pass's shortcut (a forced hidden bit) needs g_f/2 above every
+  // subnormal: beta_f >= -1019; Inf/NaN in the sample fail it too (it then
+  // deposits nothing and only finds the largest exponent).  The second pass
+  // reads subnormals exactly and its index holds every element.
+  const bool usable = SECOND || ((bf >= -1019) && (eb_max < 0x7FF));
   const FxConst kc = make_const(bf, one, Geo::STR - 1);   // cell pairs per sign
   // largest valid shift: the top of bin Ig
   const int u_thr = bin_top_exponent<double>(Ig) + (int)kc.Cp;
@@ -140,7 +189,7 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
     A[w * NT] = 0;
     B[w * NT] = 0;
   }
-  int umax = -1;
+  int umax = INT_MIN / 2;   // largest shift seen
   const int64_t nchunks = usable ? nch_all : 0;
   int since = 0;
   // the next chunk number comes from the queue one chunk ahead, so the
@@ -151,8 +200,8 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
   if (ch < nchunks) {
 #pragma unroll
     for (int q = 0; q < FX_U; ++q) {
-      fx_deposit<Geo::STR>((uint32_t)__double2hiint(v0[q].x), (uint32_t)__double2loint(v0[q].x), kc, A, B, NT, umax);
-      fx_deposit<Geo::STR>((uint32_t)__double2hiint(v0[q].y), (uint32_t)__double2loint(v0[q].y), kc, A, B, NT, umax);
+      fx_deposit<Geo::STR, SECOND>((uint32_t)__double2hiint(v0[q].x), (uint32_t)__double2loint(v0[q].x), kc, A, B, NT, umax);
+      fx_deposit<Geo::STR, SECOND>((uint32_t)__double2hiint(v0[q].y), (uint32_t)__double2loint(v0[q].y), kc, A, B, NT, umax);
     }
   }
   for (int slot = 0; ch < nchunks; slot ^= 1) {
@@ -166,9 +215,9 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
       for (int q = 0; q < FX_U; ++q) v[q] = __ldcs(base + (int64_t)(j * FX_U + q) * NT);
 #pragma unroll
       for (int q = 0; q < FX_U; ++q) {
-        fx_deposit<Geo::STR>((uint32_t)__double2hiint(v[q].x), (uint32_t)__double2loint(v[q].x), kc, A, B, NT,
+        fx_deposit<Geo::STR, SECOND>((uint32_t)__double2hiint(v[q].x), (uint32_t)__double2loint(v[q].x), kc, A, B, NT,
                              umax);
-        fx_deposit<Geo::STR>((uint32_t)__double2hiint(v[q].y), (uint32_t)__double2loint(v[q].y), kc, A, B, NT,
+        fx_deposit<Geo::STR, SECOND>((uint32_t)__double2hiint(v[q].y), (uint32_t)__double2loint(v[q].y), kc, A, B, NT,
                              umax);
       }
     }
@@ -190,7 +239,7 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
     int cnt = 0;
     for (int64_t r = gt; r < R; r += G_) {
       double v = __ldg(x + (r < head ? r : tail0 + (r - head)));
-      fx_deposit<Geo::STR>((uint32_t)__double2hiint(v), (uint32_t)__double2loint(v), kc, A, B, NT, umax);
+      fx_deposit<Geo::STR, SECOND>((uint32_t)__double2hiint(v), (uint32_t)__double2loint(v), kc, A, B, NT, umax);
       if (++cnt == 992) {
         fx_fold<Geo::STR>(A, B, NT);
         cnt = 0;
@@ -198,19 +247,33 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
     }
     fx_fold<Geo::STR>(A, B, NT);
   }
+  if (!usable) {
+    // nothing deposited: the largest exponent field, for the second pass
+    const int64_t G_ = (int64_t)gridDim.x * NT;
+    for (int64_t i = (int64_t)blockIdx.x * NT + threadIdx.x; i < n; i += G_) {
+      const uint32_t eb = ((uint32_t)__double2hiint(__ldcs(x + i)) << 1) >> 21;
+      umax = max(umax, (int)eb + (int)kc.Cp);
+    }
+  }
   const int fail = __syncthreads_or(!usable || umax > u_thr);
+  // the largest exponent field deposited, for a second pass
+  __shared__ int s_umax;
+  if (threadIdx.x == 0) s_umax = INT_MIN / 2;
+  __syncthreads();
+  const int wmax = __reduce_max_sync(0xffffffffu, umax);
+  if ((threadIdx.x & 31) == 0) atomicMax(&s_umax, wmax);
 
   // 3. Block total into the digit accumulators; the last block converts.
   Tot t = fx_thread_total<Geo::STR, Tot>(A, B, NT);
 #pragma unroll
   for (int m = 16; m >= 1; m >>= 1) t = tot_add(t, tot_shfl_xor(t, m));
   __shared__ Tot s_wt[32];
-  __shared__ bool last;
   if ((threadIdx.x & 31) == 0) s_wt[threadIdx.x >> 5] = t;
   __syncthreads();
   if (threadIdx.x == 0) {
     Tot bt = s_wt[0];
     for (int w = 1; w < (int)(NT >> 5); ++w) bt = tot_add(bt, s_wt[w]);
+    if (!SECOND && s_umax > INT_MIN / 2) atomicMax(&ctl->emax, (unsigned)max(s_umax - (int)kc.Cp, 0));
     if (fail) {
       atomicOr(&ctl->fail, 1u);
     } else {
@@ -240,7 +303,27 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
   }
   ctl->queue = 0u;
   ctl->ticket = 0u;
-  if (__ldcg(&ctl->fail)) return;   // the general pass writes the result
+  if constexpr (SECOND) {
+    ctl->run2 = 0u;
+  } else {
+    const unsigned em = __ldcg(&ctl->emax);
+    ctl->emax = 0u;
+    if (__ldcg(&ctl->fail)) {
+      // Some element lies above the guessed bin, or the guess was not
+      // usable.  Every element was deposited, so em is the largest exponent
+      // field of the input: the second pass recomputes the sum at its index
+      // (no element can lie above that bin), or, when em is all ones, finds
+      // which of Inf and NaN occur.
+      ctl->fail = 0u;
+      if (em >= 0x7FFu) {
+        ctl->run2 = 2u;
+      } else {
+        ctl->I2 = index_of_exponent<double>((int)em, K);
+        ctl->run2 = 1u;
+      }
+      return;
+    }
+  }
   W128 F[K];
   fx_folds<K>(tot, F);
   *result = convert_fast<double, K>(Ig, 0, F);
@@ -266,14 +349,17 @@ int fixed_blocks_per_sm(int block) {
   if (*slot) return *slot;
   size_t smem = fx_smem_bytes<K>(block);
   if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(sum_f64_fixed_kernel<K, CNT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(sum_f64_fixed_kernel<K, CNT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(sum_f64_fixed_kernel<K, CNT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess) {
       cudaGetLastError();
       return 0;
     }
   }
+  // the grid is sized for the first pass (the second runs on the same grid)
   int nb = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, sum_f64_fixed_kernel<K, CNT>, block, smem) !=
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, sum_f64_fixed_kernel<K, CNT, false>, block, smem) !=
       cudaSuccess) {
     cudaGetLastError();
     return 0;
@@ -289,15 +375,30 @@ int blocks_per_sm_k(int block) {
   return fixed_blocks_per_sm<K, 0>(block);
 }
 
+template <int K, int CNT>
+cudaError_t launch_kc(const double* x, int64_t n, unsigned* ctl, double* result, int grid, int block, int second,
+                      cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = fx_smem_bytes<K>(block);
+  cfg.stream = s;
+  // the second pass overlaps its launch with the first one's tail
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = second ? 1 : 0;
+  if (second) return cudaLaunchKernelEx(&cfg, sum_f64_fixed_kernel<K, CNT, true>, x, n, 1u, (FixedCtl*)ctl, result);
+  return cudaLaunchKernelEx(&cfg, sum_f64_fixed_kernel<K, CNT, false>, x, n, 1u, (FixedCtl*)ctl, result);
+}
+
 template <int K>
-void launch_k(const double* x, int64_t n, unsigned* ctl, double* result, int grid, int block, cudaStream_t s) {
-  size_t smem = fx_smem_bytes<K>(block);
-  if (block == 128)
-    sum_f64_fixed_kernel<K, 128><<<grid, block, smem, s>>>(x, n, 1u, (FixedCtl*)ctl, result);
-  else if (block == 256)
-    sum_f64_fixed_kernel<K, 256><<<grid, block, smem, s>>>(x, n, 1u, (FixedCtl*)ctl, result);
-  else
-    sum_f64_fixed_kernel<K, 0><<<grid, block, smem, s>>>(x, n, 1u, (FixedCtl*)ctl, result);
+cudaError_t launch_k(const double* x, int64_t n, unsigned* ctl, double* result, int grid, int block, int second,
+                     cudaStream_t s) {
+  if (block == 128) return launch_kc<K, 128>(x, n, ctl, result, grid, block, second, s);
+  if (block == 256) return launch_kc<K, 256>(x, n, ctl, result, grid, block, second, s);
+  return launch_kc<K, 0>(x, n, ctl, result, grid, block, second, s);
 }
 }  // namespace
 
@@ -319,17 +420,16 @@ int sum_f64_fixed_grid(int K, int block, int sms) {
 size_t sum_f64_fixed_ctl_bytes() { return sizeof(FixedCtl); }
 
 cudaError_t launch_sum_f64_fixed(const double* x, int64_t n, int K, unsigned* ctl, double* result, int grid, int block,
-                                 cudaStream_t s) {
+                                 int second, cudaStream_t s) {
   // make sure the shared-memory attribute is set for this device and block size
   if (sum_f64_fixed_grid(K, block, 1) <= 0) return cudaErrorInvalidConfiguration;
   switch (K) {
-    case 2: launch_k<2>(x, n, ctl, result, grid, block, s); break;
-    case 3: launch_k<3>(x, n, ctl, result, grid, block, s); break;
-    case 4: launch_k<4>(x, n, ctl, result, grid, block, s); break;
-    case 5: launch_k<5>(x, n, ctl, result, grid, block, s); break;
-    default: launch_k<6>(x, n, ctl, result, grid, block, s); break;
+    case 2: return launch_k<2>(x, n, ctl, result, grid, block, second, s);
+    case 3: return launch_k<3>(x, n, ctl, result, grid, block, second, s);
+    case 4: return launch_k<4>(x, n, ctl, result, grid, block, second, s);
+    case 5: return launch_k<5>(x, n, ctl, result, grid, block, second, s);
+    default: return launch_k<6>(x, n, ctl, result, grid, block, second, s);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace repro

@@ -118,3 +118,24 @@ def test_threshold_sizes(n):
     check(x, 3)
     check(x, 2)
     check(x, 6)
+
+
+def test_paths_in_sequence():
+    """Calls on one stream that take the first pass, the second pass (an
+    element above the guessed bin) and the general kernel (specials, an
+    index too fine) in turn: each leaves the stream's control words as it
+    found them, so every result is the oracle's."""
+    dev()
+    base = inputs.wide_f64(N, seed=19)
+    out = base.copy()
+    out[4321] = -2.0e250
+    top = base.copy()
+    top[N // 3] = 1.7e308                                             # second pass at index 0
+    tiny = (np.arange(N) % 17 - 8).astype(F64) * 5e-324
+    nan = inputs.inject_specials(base, "nan", seed=5)
+    for K in (3, 6, 3):
+        for x in (base, out, base, top, tiny, out, base):
+            check(x, K)
+        assert np.isnan(lib_sum(nan, K))
+        check(out, K)
+        check(base, K)
