@@ -727,14 +727,12 @@ __global__ void __launch_bounds__(1024) c3_scan_blocks(unsigned char* __restrict
 
 // ------------------------------------------------------------------ C
 // Replay of one tile from its incoming state (prefix of everything before
-// the tile).  sm: C3_TILE + C3_TILE / C3_ITEMS elements, wsm: C3_WARPS states.
+// the tile), per fold.  sm: C3_TILE + C3_TILE / C3_ITEMS elements holding the
+// staged tile (element i at i + i / C3_ITEMS), wsm: C3_WARPS states.  The
+// results are written over the staged inputs.
 template <typename T>
-__device__ void c3_replay_tile(const T* in, T* out, int64_t n, int64_t tile, S3 st, T* sm, S3* wsm) {
+__device__ void c3_replay_staged(int cnt, S3 st, T* sm, S3* wsm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t base = tile * C3_TILE;
-  const int cnt = (int)min((int64_t)C3_TILE, n - base);
-  for (int i = threadIdx.x; i < cnt; i += blockDim.x) sm[i + i / C3_ITEMS] = in[base + i];
-  __syncthreads();
   const int b = threadIdx.x * C3_ITEMS;
   const int sb = b + threadIdx.x;
   const int I0 = Geom<T>::NB - 3;
@@ -763,6 +761,15 @@ __device__ void c3_replay_tile(const T* in, T* out, int64_t n, int64_t tile, S3 
       sm[sb + i] = r.value();
     }
   }
+}
+
+template <typename T>
+__device__ void c3_replay_tile(const T* in, T* out, int64_t n, int64_t tile, S3 st, T* sm, S3* wsm) {
+  const int64_t base = tile * C3_TILE;
+  const int cnt = (int)min((int64_t)C3_TILE, n - base);
+  for (int i = threadIdx.x; i < cnt; i += blockDim.x) sm[i + i / C3_ITEMS] = in[base + i];
+  __syncthreads();
+  c3_replay_staged<T>(cnt, st, sm, wsm);
   __syncthreads();
   for (int i = threadIdx.x; i < cnt; i += blockDim.x) out[base + i] = sm[i + i / C3_ITEMS];
   __syncthreads();
@@ -776,22 +783,6 @@ __global__ void __launch_bounds__(C3_BLOCK) c3_single_tile(const T* in, T* out, 
   __shared__ S3 wsm[C3_WARPS];
   c3_replay_tile<T>(in, out, n, 0, s3_zero(Geom<T>::NB - 3), sm, wsm);
 }
-
-template <typename T>
-__global__ void __launch_bounds__(C3_BLOCK) c3_replay(const T* in, T* out, int64_t n, int64_t ntiles,
-                                                      const unsigned char* __restrict__ tloc,
-                                                      const unsigned char* __restrict__ bpre,
-                                                      const unsigned* gate) {
-  __shared__ T sm[C3_TILE + C3_TILE / C3_ITEMS];
-  __shared__ S3 wsm[C3_WARPS];
-  if (c3_gated_off_later(gate)) return;
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    S3 st = s3_load(bpre + (size_t)(tile / 1024) * C3_STATE);
-    s3_merge(st, s3_load(tloc + (size_t)tile * C3_STATE));
-    c3_replay_tile<T>(in, out, n, tile, st, sm, wsm);
-  }
-}
-
 
 // ================================================ fixed-index fast path (K = 3)
 // See fixed_index.cuh: with the index L guessed from a sample and checked,
@@ -830,6 +821,14 @@ template <> struct CsTraits<double> {
 
 __device__ __forceinline__ fx::I192 i192_from_i64(int64_t v) {
   return fx::I192{(uint64_t)v, (uint64_t)(v >> 63), (uint64_t)(v >> 63)};
+}
+// v 2^s for a signed 128-bit v and 0 <= s < 128 (the bits beyond 192 dropped)
+__device__ __forceinline__ fx::I192 i192_shl_w128(W128 v, int s) {
+  const uint64_t x0 = v.lo, x1 = (uint64_t)v.hi, x2 = (uint64_t)(v.hi >> 63);
+  if (s == 0) return fx::I192{x0, x1, x2};
+  if (s < 64) return fx::I192{x0 << s, (x1 << s) | (x0 >> (64 - s)), (x2 << s) | (x1 >> (64 - s))};
+  if (s == 64) return fx::I192{0, x0, x1};
+  return fx::I192{0, x0 << (s - 64), (x1 << (s - 64)) | (x0 >> (128 - s))};
 }
 __device__ __forceinline__ fx::I192 i192_shfl_up(fx::I192 v, int d) {
   fx::I192 r;
@@ -1481,6 +1480,100 @@ __device__ __forceinline__ void cf_replay_lanes(T* buf, int sb, int b, int cnt, 
   }
 }
 
+// The general path's replay of one tile.  When the tile keeps the index of
+// its incoming state throughout (no element above that bin, no Inf/NaN, an
+// index the fixed-index shortcut can use), its prefixes are the correct
+// roundings of g_f times S + the sum of R_j, S the incoming folds as one
+// integer at the finest grid and R_j the single rounding of each element
+// there ("SyclReproSum", "How It Works": depositing at the final index gives
+// the same folds): the tile runs the fixed-index replay of the fast path,
+// with each thread's prefix from a block scan of its 16 rounded values.
+// Otherwise it replays per fold.  Both give the same bits.
+template <typename T>
+__device__ void c3_replay_tile_any(const T* in, T* out, int64_t n, int64_t tile, S3 st, T* sm, S3* wsm,
+                                   uint32_t one) {
+  typedef Geom<T> G;
+  __shared__ unsigned s_em;
+  __shared__ fx::I192 s_wt[C3_WARPS];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t base = tile * C3_TILE;
+  const int cnt = (int)min((int64_t)C3_TILE, n - base);
+  if (threadIdx.x == 0) s_em = 0u;
+  for (int i = threadIdx.x; i < cnt; i += blockDim.x) sm[i + i / C3_ITEMS] = in[base + i];
+  __syncthreads();
+  const int b = threadIdx.x * C3_ITEMS, sb = b + threadIdx.x;
+  constexpr int ESH = sizeof(T) == 8 ? 21 : 24;
+  uint32_t em = 0;   // this thread's largest exponent field
+#pragma unroll
+  for (int i = 0; i < C3_ITEMS; ++i) {
+    uint32_t hi;
+    if constexpr (sizeof(T) == 8) hi = (uint32_t)__double2hiint(sm[sb + i]);
+    else hi = __float_as_uint(sm[sb + i]);
+    if (b + i < cnt) em = max(em, (hi << 1) >> ESH);
+  }
+  const uint32_t wm = __reduce_max_sync(0xffffffffu, em);
+  if (lane == 0) atomicMax(&s_em, wm);
+  __syncthreads();
+  const int emt = (int)s_em;
+  const int L = st.I;
+  const int bf = beta<T>(L + 2);
+  const bool fixed = st.flags == 0 && emt < (sizeof(T) == 8 ? 0x7FF : 0xFF) &&
+                     fx::index_of_exponent<T>(emt, 3) >= L && bf >= CsTraits<T>::MAX_BETA_F;
+  if (!fixed) {
+    c3_replay_staged<T>(cnt, st, sm, wsm);
+  } else {
+    const fx::FxConst kc = fx::make_const(bf, one);
+    const fx::F32Const fk = fx::make_f32_const(-150 - bf + 24);
+    // the thread's 16 rounded values
+    fx::I192 own{0, 0, 0};
+#pragma unroll 4
+    for (int i = 0; i < C3_ITEMS; ++i) {
+      if (b + i < cnt) {
+        if constexpr (sizeof(T) == 8) {
+          const double v = sm[sb + i];
+          const uint32_t hi = (uint32_t)__double2hiint(v);
+          uint64_t rl, rh;
+          fx::round_f64(hi, (uint32_t)__double2loint(v), kc, rl, rh);
+          own = i192_add_signed(own, rl, rh, (uint64_t)((int64_t)(int32_t)hi >> 31));
+        } else {
+          const uint32_t bits = __float_as_uint(sm[sb + i]);
+          uint32_t rl, rh;
+          fx::round_f32w(bits, fk, rl, rh);
+          own = i192_add_signed(own, ((uint64_t)rh << 32) | rl, 0ull, (uint64_t)((int64_t)(int32_t)bits >> 31));
+        }
+      }
+    }
+    fx::I192 wt;
+    const fx::I192 exc = i192_warp_exclusive(own, &wt);
+    if (lane == 0) s_wt[warp] = wt;
+    __syncthreads();
+    // incoming folds as one integer at the finest grid: F0 2^(2W) + F1 2^W + F2
+    fx::I192 t = fx::i192_add(fx::i192_add(i192_shl_w128(st.F[0], 2 * G::W), i192_shl_w128(st.F[1], G::W)),
+                              i192_shl_w128(st.F[2], 0));
+    for (int w = 0; w < warp; ++w) t = fx::i192_add(t, s_wt[w]);
+    t = fx::i192_add(t, exc);
+    cf_replay_lanes<T, false>(sm, sb, b, cnt, t, kc, fk, bf, em);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < cnt; i += blockDim.x) out[base + i] = sm[i + i / C3_ITEMS];
+  __syncthreads();
+}
+
+template <typename T>
+__global__ void __launch_bounds__(C3_BLOCK) c3_replay(const T* in, T* out, int64_t n, int64_t ntiles,
+                                                      const unsigned char* __restrict__ tloc,
+                                                      const unsigned char* __restrict__ bpre,
+                                                      const unsigned* gate, uint32_t one) {
+  __shared__ T sm[C3_TILE + C3_TILE / C3_ITEMS];
+  __shared__ S3 wsm[C3_WARPS];
+  if (c3_gated_off_later(gate)) return;
+  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    S3 st = s3_load(bpre + (size_t)(tile / 1024) * C3_STATE);
+    s3_merge(st, s3_load(tloc + (size_t)tile * C3_STATE));
+    c3_replay_tile_any<T>(in, out, n, tile, st, sm, wsm, one);
+  }
+}
+
 // Pass 3.  Each warp replays whole chunks staged in shared memory (coalesced
 // global traffic); lane l starts from chunk prefix + its lane prefix and
 // converts after every one of its 16 elements.
@@ -1702,7 +1795,7 @@ cudaError_t launch_cumsum_k3(const T* in, T* out, int64_t n, unsigned char* ws, 
   if ((e = launch_gated(c3_scan_blocks<T>, 1, 1024, 0, s, pdl, btot, nb, I0, bpre, gate, carry)) != cudaSuccess)
     return e;
   return launch_gated(c3_replay<T>, ggrid, C3_BLOCK, 0, s, pdl, in, out, n, nt, (const unsigned char*)tloc,
-                      (const unsigned char*)bpre, gate);
+                      (const unsigned char*)bpre, gate, 1u);
 }
 
 template size_t cumsum_k3_workspace_bytes<float>(int64_t);
