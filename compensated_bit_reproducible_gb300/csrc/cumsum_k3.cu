@@ -809,6 +809,7 @@ struct CsCtl {                 // in the stream's control page: zero at the call
   unsigned exact0;             // set by the scan: the first tile is replayed per fold
   unsigned long long istar;    // max over elements of bin L of (2^63 - 1 - position)
   unsigned ticket;             // finished blocks of the scan
+  unsigned stop;               // the first tile holds no element of bin L: the totals pass stops
 };
 
 template <typename T> struct CsTraits;
@@ -1076,6 +1077,9 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
     const int64_t c0 = ch * CF_CHUNK;
     const int cnt = (int)min((int64_t)CF_CHUNK, n - c0);
     const bool look = c0 < C3_TILE;   // warp-uniform
+    // read now, tested after this chunk: block 0 sets it once the first tile
+    // turns out to hold no element of bin L
+    const unsigned stop = *(volatile const unsigned*)&ctl->stop;
     cf_prefetch_next<T>(in, n, ch + GW, lane);
     fx::I192 tot;
     T* buf = sm + warp * CF_PAD;
@@ -1141,6 +1145,21 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_totals(const T* __restrict__ in, 
     }
     __syncwarp();
     if (lane == 0) ctot[ch] = tot;
+    if (blockIdx.x == 0 && ch == gw) {
+      // Block 0's warps have just taken the first tile (chunks 0..7; every
+      // warp of the block has this first chunk).  Without an element of bin
+      // L (or above) in it, i* lies beyond the first tile or the guess is
+      // wrong: the general kernels compute everything, so the other blocks
+      // stop at their next chunk.
+      if (!__syncthreads_or(first != INT64_MAX)) {
+        if (threadIdx.x == 0) {
+          ctl->stop = 1u;
+          atomicOr(&ctl->fail, 1u);
+        }
+        return;
+      }
+    }
+    if (stop) break;
   }
   const int bad = __syncthreads_or(ebmax > eb_top);
   int64_t f = first;
@@ -1221,6 +1240,7 @@ __global__ void __launch_bounds__(CS_SCAN_THREADS) cf_scan(const fx::I192* __res
     ctl->fail = 0u;
     ctl->istar = 0ull;
     ctl->ticket = 0u;
+    ctl->stop = 0u;
   }
 }
 
@@ -1498,8 +1518,27 @@ __device__ void c3_replay_tile_any(const T* in, T* out, int64_t n, int64_t tile,
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t base = tile * C3_TILE;
   const int cnt = (int)min((int64_t)C3_TILE, n - base);
+  typedef typename std::conditional<sizeof(T) == 4, float4, double2>::type V;
+  constexpr int VW = 16 / sizeof(T);
+  const bool vec = cnt == C3_TILE && ((((uintptr_t)(in + base)) & 15) == 0) && ((((uintptr_t)(out + base)) & 15) == 0);
   if (threadIdx.x == 0) s_em = 0u;
-  for (int i = threadIdx.x; i < cnt; i += blockDim.x) sm[i + i / C3_ITEMS] = in[base + i];
+  {
+    // ask L2 for this block's next tile while this one is replayed
+    const int64_t nx = (tile + gridDim.x) * C3_TILE + (int64_t)threadIdx.x * (128 / (int)sizeof(T));
+    if (threadIdx.x < C3_TILE * (int)sizeof(T) / 128 && nx < n) asm volatile("prefetch.global.L2 [%0];" ::"l"(in + nx));
+  }
+  if (vec) {
+#pragma unroll
+    for (int k = 0; k < C3_TILE / VW / C3_BLOCK; ++k) {
+      const int i = (k * C3_BLOCK + (int)threadIdx.x) * VW;
+      const V v = __ldcs((const V*)(in + base) + k * C3_BLOCK + threadIdx.x);
+      const T* e = (const T*)&v;
+#pragma unroll
+      for (int q = 0; q < VW; ++q) sm[i + q + (i + q) / C3_ITEMS] = e[q];
+    }
+  } else {
+    for (int i = threadIdx.x; i < cnt; i += blockDim.x) sm[i + i / C3_ITEMS] = in[base + i];
+  }
   __syncthreads();
   const int b = threadIdx.x * C3_ITEMS, sb = b + threadIdx.x;
   constexpr int ESH = sizeof(T) == 8 ? 21 : 24;
@@ -1555,12 +1594,24 @@ __device__ void c3_replay_tile_any(const T* in, T* out, int64_t n, int64_t tile,
     cf_replay_lanes<T, false>(sm, sb, b, cnt, t, kc, fk, bf, em);
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < cnt; i += blockDim.x) out[base + i] = sm[i + i / C3_ITEMS];
+  if (vec) {
+#pragma unroll
+    for (int k = 0; k < C3_TILE / VW / C3_BLOCK; ++k) {
+      const int i = (k * C3_BLOCK + (int)threadIdx.x) * VW;
+      V v;
+      T* e = (T*)&v;
+#pragma unroll
+      for (int q = 0; q < VW; ++q) e[q] = sm[i + q + (i + q) / C3_ITEMS];
+      ((V*)(out + base))[k * C3_BLOCK + threadIdx.x] = v;
+    }
+  } else {
+    for (int i = threadIdx.x; i < cnt; i += blockDim.x) out[base + i] = sm[i + i / C3_ITEMS];
+  }
   __syncthreads();
 }
 
 template <typename T>
-__global__ void __launch_bounds__(C3_BLOCK) c3_replay(const T* in, T* out, int64_t n, int64_t ntiles,
+__global__ void __launch_bounds__(C3_BLOCK, 3) c3_replay(const T* in, T* out, int64_t n, int64_t ntiles,
                                                       const unsigned char* __restrict__ tloc,
                                                       const unsigned char* __restrict__ bpre,
                                                       const unsigned* gate, uint32_t one) {
