@@ -17,6 +17,18 @@
  *  - Streams: work is enqueued on `stream` (0 = legacy default stream).
  *    Calls documented "synchronous" wait for their own work; the others
  *    return once the work is enqueued.
+ *  - Control words: the sums and cumulative sums count and accumulate in a
+ *    4 KiB page of device memory per device and stream, allocated and
+ *    zeroed at a stream's first call, which every call leaves zero again
+ *    (so no call needs a memset).  Calls on one stream therefore run one
+ *    after another on it; calls on different streams use different pages.
+ *    Pages are kept until the process exits.  A CUDA graph captured from a
+ *    stream keeps that stream's page: its launches must not overlap one
+ *    another or calls made directly on that stream, and the stream's first
+ *    call must come before the capture (the page is allocated then).
+ *  - Device reset: the library keeps per-device state (its memory pool,
+ *    the control pages, cached device properties).  After cudaDeviceReset
+ *    the library's calls must not be used again in that process.
  *  - Errors: a non-zero repro_status.  Argument and capacity checks happen
  *    before any pointer is touched or any memory allocated; an error leaves
  *    outputs unwritten.  repro_strerror() gives a static message.
