@@ -1696,7 +1696,7 @@ __global__ void __launch_bounds__(C3_BLOCK) cf_replay(const T* in, T* out, int64
           v.z = buf[i + 2 + (i + 2) / 16];
           v.w = buf[i + 3 + (i + 3) / 16];
         }
-        ((V*)g)[k * 32 + lane] = v;
+        __stcs((V*)g + k * 32 + lane, v);   // streaming: the outputs are not read again here
       }
     } else {
       for (int i = lane; i < cnt; i += 32) g[i] = buf[i + i / 16];
