@@ -34,12 +34,10 @@ int sum_blocks_per_sm(int K, int block);
 // size (0: not available), size of the control words, launch.  The first
 // pass (second = 0) guesses the index from a sample; launched right after
 // it, the second pass (second = 1) runs only when an element lay above the
-// guessed bin, at the index of the largest exponent.  ctl points at
+// guessed bin (or the first pass could not be used), at the index of the
+// largest exponent, or to find which of Inf and NaN occur.  ctl points at
 // sum_f64_fixed_ctl_bytes() zero bytes (16-byte aligned), which the two
-// leave zero except ctl[2]: it becomes nonzero when neither can compute the
-// result and the general kernel must (pass it as that kernel's gate, read
-// without waiting: it is set before the second pass lets later kernels
-// start; that kernel clears it).
+// leave zero.
 int sum_f64_fixed_grid(int K, int block, int sms);
 size_t sum_f64_fixed_ctl_bytes();
 cudaError_t launch_sum_f64_fixed(const double* x, int64_t n, int K, unsigned* ctl, double* result, int grid,

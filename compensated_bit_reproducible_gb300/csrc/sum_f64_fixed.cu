@@ -1,9 +1,11 @@
 // Double binned sum (K = 2..6) at an index fixed before the deposit (see
-// fixed_index.cuh for the reading this rests on).  If any element lies
-// outside the guessed bin or is Inf/NaN, or the index is too fine for the
-// shortcuts, the kernel sets a flag and the general one-pass kernel
-// (launched right after, idle unless the flag is set) computes the sum.
-// Both paths give the same bits.
+// fixed_index.cuh for the reading this rests on).  The first pass guesses
+// the index from a sample.  If any element lies outside the guessed bin or
+// is Inf/NaN, or the index is too fine for its shortcut, it records the
+// largest exponent field of the input, and the second pass (launched right
+// after, idle otherwise) recomputes the sum at the index of that exponent,
+// reading subnormals exactly, or finds which of Inf and NaN occur.  Both
+// passes give the binned sum's bits.
 //
 // Accumulation.  M + h - b shifted by u & 31 is three 32-bit words w0, w1,
 // w2 that land at word positions c, c + 1, c + 2 of P'' (c = u >> 5); words
@@ -30,17 +32,18 @@ constexpr int FX_U = 4;           // 16-byte vectors per thread per step
 constexpr int FX_J = 4;           // steps per chunk
 constexpr int FX_FOLD_CHUNKS = 992 / (2 * FX_U * FX_J);   // chunks between folds: at most 992 deposits
 
-// Control words, zero at launch; the kernel leaves them zero except the
-// fallback flag, which the general kernel clears.  The block totals are summed by
-// atomics as 32-bit digits in 64-bit accumulators (2^32 blocks before one
-// could carry out), one accumulator per 128-byte line so that the blocks'
+// Control words, zero at launch and left zero by the two passes (the first
+// pass's last block clears what it accumulated and sets run2; the second
+// pass's last block clears that).  The block totals are summed by atomics
+// as 32-bit digits in 64-bit accumulators (2^32 blocks before one could
+// carry out), one accumulator per 128-byte line so that the blocks'
 // additions to different digits do not queue on one line.
 constexpr int FX_DIGITS = 10;   // 320-bit totals
 constexpr int FX_DIG_STRIDE = 16;   // 64-bit words between two accumulators
 struct FixedCtl {
   unsigned queue;     // next chunk of the dynamic queue (after the first gridDim.x)
   unsigned ticket;    // finished blocks
-  unsigned general;   // unused by these kernels (the general kernel's gate when it follows them)
+  unsigned spare;
   unsigned fail;      // some block of the first pass left the guessed bin
   unsigned emax;      // largest biased exponent field the first pass deposited
   unsigned run2;      // set by the first pass's last block: 1 the second pass deposits, 2 it scans for Inf/NaN
@@ -291,8 +294,7 @@ __global__ void __launch_bounds__(fx_max_threads(CNT), fx_min_blocks(CNT, K))
   if (!last || threadIdx.x != 0) return;
   __threadfence();
   // sum of the digits D_i 2^(32 i), modulo 2^(64 N) (the total fits); the
-  // control words are left zero for the next call, except the flag, which
-  // the general pass clears
+  // control words are left zero for the next call
   Tot tot{};
 #pragma unroll
   for (int i = 0; i < 2 * TotW<Tot>::N; ++i) {
