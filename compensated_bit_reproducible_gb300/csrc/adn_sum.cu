@@ -221,30 +221,13 @@ __global__ void state_finalize_kernel(const unsigned char* st, int K, uint64_t c
 }
 
 // ticket: a counter that is zero at launch, and zero again when the kernel
-// ends; parts: one partial state per block.  With a gate, the kernel runs
-// only if *gate is nonzero (it is the fallback of a faster path that decides
-// on the device), and clears it; gate_final says the gate was set before the
-// preceding grid let this one start.
+// ends; parts: one partial state per block.
 // With `state`, the merged result is added to that binned state (no
 // conversion; `result` unused).
 template <typename T, int KT, int U>
 __global__ void __launch_bounds__(1024) adn_sum_kernel(const T* __restrict__ x, int64_t n, int K,
                                                        unsigned* ticket, unsigned char* __restrict__ parts,
-                                                       T* __restrict__ result, unsigned* gate, int gate_final,
-                                                       unsigned char* __restrict__ state) {
-  if (gate) {
-    // launched as a programmatic dependent of the fast path.  A gate set
-    // before the preceding grid let this one start is read at once (and the
-    // grid is waited for only when it is set); otherwise wait until the
-    // preceding grid has completed and its writes are visible
-    if (gate_final) {
-      if (*(volatile const unsigned*)gate == 0u) return;
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-    } else {
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      if (*gate == 0u) return;
-    }
-  }
+                                                       T* __restrict__ result, unsigned char* __restrict__ state) {
   typedef typename AccOf<T, KT>::type Acc;
   constexpr int N = Acc::N;
   Acc acc;
@@ -269,9 +252,8 @@ __global__ void __launch_bounds__(1024) adn_sum_kernel(const T* __restrict__ x, 
     if (state) state_add<T>(state, K, st.I, st.flags, st.F, (uint64_t)n);
     else if constexpr (KT != 0) *result = convert_fast<T, KT>(st.I, st.flags, st.F);
     else *result = convert_state<T, N>(st, K);
-    // leave the control words zero for the next call
+    // leave the ticket zero for the next call
     *ticket = 0u;
-    if (gate) *gate = 0u;
   }
 }
 
@@ -391,40 +373,24 @@ __global__ void __launch_bounds__(256) segsum_cols_kernel(const float* __restric
 // ------------------------------------------------------------------ launch
 template <typename T, int KT>
 static cudaError_t launch_sum_k(const T* x, int64_t n, int K, unsigned* ticket, unsigned char* parts, T* result,
-                                int grid, int block, unsigned* gate, cudaStream_t s, unsigned char* state = nullptr,
-                                int gate_final = 0) {
+                                int grid, int block, cudaStream_t s, unsigned char* state = nullptr) {
   constexpr int U = 4;
-  if (!gate) {
-    adn_sum_kernel<T, KT, U><<<grid, block, 0, s>>>(x, n, K, ticket, parts, result, gate, 0, state);
-    return cudaGetLastError();
-  }
-  // gated fallback: programmatic dependent launch overlaps its launch with
-  // the tail of the preceding kernel on the stream
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3((unsigned)block);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, adn_sum_kernel<T, KT, U>, x, n, K, ticket, parts, result, gate, gate_final, state);
+  adn_sum_kernel<T, KT, U><<<grid, block, 0, s>>>(x, n, K, ticket, parts, result, state);
+  return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_sum(const T* x, int64_t n, int K, unsigned* ticket, unsigned char* parts, T* result, int grid,
-                       int block, cudaStream_t s, unsigned* gate, int gate_final) {
+                       int block, cudaStream_t s) {
   switch (K) {
-    case 2: return launch_sum_k<T, 2>(x, n, K, ticket, parts, result, grid, block, gate, s, nullptr, gate_final);
-    case 3: return launch_sum_k<T, 3>(x, n, K, ticket, parts, result, grid, block, gate, s, nullptr, gate_final);
-    case 4: return launch_sum_k<T, 4>(x, n, K, ticket, parts, result, grid, block, gate, s, nullptr, gate_final);
-    case 5: return launch_sum_k<T, 5>(x, n, K, ticket, parts, result, grid, block, gate, s, nullptr, gate_final);
-    case 6: return launch_sum_k<T, 6>(x, n, K, ticket, parts, result, grid, block, gate, s, nullptr, gate_final);
-    case 7: return launch_sum_k<T, 7>(x, n, K, ticket, parts, result, grid, block, gate, s, nullptr, gate_final);
-    case 8: return launch_sum_k<T, 8>(x, n, K, ticket, parts, result, grid, block, gate, s, nullptr, gate_final);
-    default: return launch_sum_k<T, 0>(x, n, K, ticket, parts, result, grid, block, gate, s, nullptr, gate_final);
+    case 2: return launch_sum_k<T, 2>(x, n, K, ticket, parts, result, grid, block, s);
+    case 3: return launch_sum_k<T, 3>(x, n, K, ticket, parts, result, grid, block, s);
+    case 4: return launch_sum_k<T, 4>(x, n, K, ticket, parts, result, grid, block, s);
+    case 5: return launch_sum_k<T, 5>(x, n, K, ticket, parts, result, grid, block, s);
+    case 6: return launch_sum_k<T, 6>(x, n, K, ticket, parts, result, grid, block, s);
+    case 7: return launch_sum_k<T, 7>(x, n, K, ticket, parts, result, grid, block, s);
+    case 8: return launch_sum_k<T, 8>(x, n, K, ticket, parts, result, grid, block, s);
+    default: return launch_sum_k<T, 0>(x, n, K, ticket, parts, result, grid, block, s);
   }
 }
 
@@ -457,14 +423,14 @@ cudaError_t launch_state_deposit(const T* x, int64_t n, int K, unsigned char* ws
   unsigned* tk = (unsigned*)ws;
   unsigned char* pp = ws + 256;
   switch (K) {
-    case 2: return launch_sum_k<T, 2>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
-    case 3: return launch_sum_k<T, 3>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
-    case 4: return launch_sum_k<T, 4>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
-    case 5: return launch_sum_k<T, 5>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
-    case 6: return launch_sum_k<T, 6>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
-    case 7: return launch_sum_k<T, 7>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
-    case 8: return launch_sum_k<T, 8>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
-    default: return launch_sum_k<T, 0>(x, n, K, tk, pp, nullptr, grid, block, nullptr, s, state);
+    case 2: return launch_sum_k<T, 2>(x, n, K, tk, pp, nullptr, grid, block, s, state);
+    case 3: return launch_sum_k<T, 3>(x, n, K, tk, pp, nullptr, grid, block, s, state);
+    case 4: return launch_sum_k<T, 4>(x, n, K, tk, pp, nullptr, grid, block, s, state);
+    case 5: return launch_sum_k<T, 5>(x, n, K, tk, pp, nullptr, grid, block, s, state);
+    case 6: return launch_sum_k<T, 6>(x, n, K, tk, pp, nullptr, grid, block, s, state);
+    case 7: return launch_sum_k<T, 7>(x, n, K, tk, pp, nullptr, grid, block, s, state);
+    case 8: return launch_sum_k<T, 8>(x, n, K, tk, pp, nullptr, grid, block, s, state);
+    default: return launch_sum_k<T, 0>(x, n, K, tk, pp, nullptr, grid, block, s, state);
   }
 }
 
@@ -487,9 +453,9 @@ template cudaError_t launch_state_op<double>(int, unsigned char*, const unsigned
                                              cudaStream_t);
 
 template cudaError_t launch_sum<float>(const float*, int64_t, int, unsigned*, unsigned char*, float*, int, int,
-                                       cudaStream_t, unsigned*, int);
+                                       cudaStream_t);
 template cudaError_t launch_sum<double>(const double*, int64_t, int, unsigned*, unsigned char*, double*, int, int,
-                                        cudaStream_t, unsigned*, int);
+                                        cudaStream_t);
 
 // Resident blocks per SM of the sum kernel for this K and block size (one
 // wave of blocks covers the GPU; more would leave a partial second wave).

@@ -8,10 +8,10 @@ namespace repro {
 
 // binned sum.  ticket: a zero counter (zero again after the call); parts:
 // one partial state of 16 + 16 K bytes per block (sum_workspace_bytes(K,
-// grid) bytes suffice); gate, gate_final: see adn_sum_kernel.
+// grid) bytes suffice).
 template <typename T>
 cudaError_t launch_sum(const T* x, int64_t n, int K, unsigned* ticket, unsigned char* parts, T* result, int grid,
-                       int block, cudaStream_t s, unsigned* gate = nullptr, int gate_final = 0);
+                       int block, cudaStream_t s);
 // One block, no workspace: the single-block sum for small inputs.
 template <typename T>
 cudaError_t launch_sum_single(const T* x, int64_t n, int K, T* result, int block, cudaStream_t s,
