@@ -155,9 +155,10 @@ def run_ours(args):
         "sum_f64_1e8": lambda: api.repro_sum_async(x64, s64, args.k),
         "cumsum_f64_1e8": lambda: api.repro_cumsum(x64, out=c64, K=args.k),
     }
-    # kernels per call: the double sum is the fixed-index kernel plus its
-    # gated fallback; a cumulative sum is totals, scan and replay plus four
-    # gated fallback kernels (the workspace memsets are not kernels)
+    # kernels per call: the double sum is the fixed-index first pass plus its
+    # second pass (idle unless the first missed); a cumulative sum is totals,
+    # scan and replay plus four gated fallback kernels (no call launches a
+    # memset)
     launches_per_row = {"var_f32_4096x4096": 1, "sum_f32_1e8": 1, "segsum_f32_4096x4096": 1,
                         "cumsum_f32_1e8": 7, "sum_f64_1e8": 2, "cumsum_f64_1e8": 7}
 
