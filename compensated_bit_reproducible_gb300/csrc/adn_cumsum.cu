@@ -14,112 +14,6 @@ constexpr int CS_BLOCK = 256;
 constexpr int CS_ITEMS = 16;
 constexpr int CS_TILE = CS_BLOCK * CS_ITEMS;
 
-template <int N> struct SState {
-  int I;
-  int flags;
-  W128 F[N];
-};
-
-template <int N>
-__device__ __forceinline__ void sstate_zero(SState<N>& s, int I0) {
-  s.I = I0;
-  s.flags = 0;
-#pragma unroll(N <= 8 ? N : 1)
-  for (int k = 0; k < N; ++k) s.F[k] = W128{0, 0};
-}
-
-// a <- merge(a, b): both re-expressed at the smaller index, folds added.
-template <int N>
-__device__ __forceinline__ void sstate_merge(SState<N>& a, const SState<N>& b, int K) {
-  int I = min(a.I, b.I);
-  int da = a.I - I, db = b.I - I;
-  W128 r[N];
-#pragma unroll(N <= 8 ? N : 1)
-  for (int k = 0; k < N; ++k) r[k] = w_add(fold_at<N, W128>(a.F, K, k - da), fold_at<N, W128>(b.F, K, k - db));
-#pragma unroll(N <= 8 ? N : 1)
-  for (int k = 0; k < N; ++k) a.F[k] = r[k];
-  a.I = I;
-  a.flags |= b.flags;
-}
-
-template <int N>
-__device__ __forceinline__ SState<N> sstate_shfl_up(const SState<N>& s, int d) {
-  SState<N> o;
-  o.I = __shfl_up_sync(0xffffffffu, s.I, d);
-  o.flags = __shfl_up_sync(0xffffffffu, s.flags, d);
-#pragma unroll(N <= 8 ? N : 1)
-  for (int k = 0; k < N; ++k) o.F[k] = shfl_up_w(s.F[k], d);
-  return o;
-}
-
-// Exclusive scan of one state per thread across the block.  Returns the
-// merge of the states of all lower threads (identity for thread 0) and, in
-// *total, the merge of all.  Uses `sm` (one SState per warp).
-template <int N>
-__device__ SState<N> block_exclusive_scan(const SState<N>& mine, int K, int I0, SState<N>* sm,
-                                          SState<N>* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  SState<N> inc = mine;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    SState<N> o = sstate_shfl_up(inc, d);
-    if (lane >= d) {
-      SState<N> t = o;
-      sstate_merge(t, inc, K);
-      inc = t;
-    }
-  }
-  SState<N> exc = sstate_shfl_up(inc, 1);
-  if (lane == 0) sstate_zero(exc, I0);
-  if (lane == 31) sm[warp] = inc;
-  __syncthreads();
-  SState<N> base;
-  sstate_zero(base, I0);
-  for (int w = 0; w < warp; ++w) sstate_merge(base, sm[w], K);
-  if (total) {
-    sstate_zero(*total, I0);
-    for (int w = 0; w < nw; ++w) sstate_merge(*total, sm[w], K);
-  }
-  sstate_merge(base, exc, K);
-  __syncthreads();
-  return base;
-}
-
-template <typename T, int N>
-__device__ __forceinline__ void sstate_deposit(SState<N>& s, T x, int K) {
-  uint64_t a = abs_bits<T>(x);
-  if (a >= (sizeof(T) == 4 ? 0x7F800000ull : 0x7FF0000000000000ull)) {
-    s.flags |= special_flag(x);
-    return;
-  }
-  if (x == (T)0) return;
-  int j = bin_index<T>(x);
-  if (j < s.I) {
-    int d = s.I - j;
-    W128 t[N];
-#pragma unroll(N <= 8 ? N : 1)
-    for (int k = 0; k < N; ++k) t[k] = fold_at<N, W128>(s.F, K, k - d);
-#pragma unroll(N <= 8 ? N : 1)
-    for (int k = 0; k < N; ++k) s.F[k] = t[k];
-    s.I = j;
-  }
-  int64_t dg[N];
-  chain_digits<T>(x, s.I, K, dg);
-#pragma unroll(N <= 8 ? N : 1)
-  for (int k = 0; k < N; ++k)
-    if (k < K) s.F[k] = w_add(s.F[k], w_from(dg[k]));
-}
-
-template <typename T, int N>
-__device__ __forceinline__ T sstate_value(const SState<N>& s, int K) {
-  State<N> st;
-  st.I = s.I;
-  st.flags = s.flags;
-#pragma unroll(N <= 8 ? N : 1)
-  for (int k = 0; k < N; ++k) st.F[k] = s.F[k];
-  return convert_state<T, N>(st, K);
-}
-
 // Tile staging: coalesced copy of the tile into shared memory, thread t then
 // owns elements [t * ITEMS, (t + 1) * ITEMS) of it.
 template <typename T>

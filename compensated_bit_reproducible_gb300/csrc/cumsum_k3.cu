@@ -98,41 +98,6 @@ __device__ __forceinline__ bool t192_to_double_normal(uint64_t t0, uint64_t t1, 
   return true;
 }
 
-// The same for a signed 128-bit T (t1:t0): one word level fewer.
-__device__ __forceinline__ bool t128_to_double_normal(uint64_t t0, uint64_t t1, int lsb, double* out) {
-  const uint32_t x0 = (uint32_t)t0, x1 = (uint32_t)(t0 >> 32), x2 = (uint32_t)t1, x3 = (uint32_t)(t1 >> 32);
-  const uint32_t s = (uint32_t)((int32_t)x3 >> 31);
-  const bool za = (x3 == s) & (x2 == s);
-  uint32_t W3 = za ? x1 : x3;
-  uint32_t W2 = za ? x0 : x2;
-  uint32_t W1 = za ? 0u : x1;
-  uint32_t W0 = za ? 0u : x0;
-  int e = za ? -64 : 0;
-  if (W3 == s) {
-    W3 = W2;
-    W2 = W1;
-    W1 = W0;
-    W0 = 0u;
-    e -= 32;
-  }
-  const uint32_t lz = (uint32_t)__clz((int)(W3 ^ s));   // 32 only for T = 0 or -1
-  const int E = e + 127 - (int)lz + lsb;
-  if (lz == 32u || (unsigned)(E + 1022) > 2045u) return false;
-  const uint32_t h = fx::funnel_l(W2, W3, lz);
-  const uint32_t l = fx::funnel_l(W1, W2, lz);
-  const uint32_t below = fx::shl_clamp32(W1, (int)lz) | W0;
-  const uint32_t st = ((l & 0x3FFu) | below) != 0u ? 1u : 0u;
-  const uint32_t odd = (l >> 11) & 1u;
-  const uint64_t w = (((uint64_t)h) << 32) | ((l & ~0x3FFu) | st);
-  const uint64_t v = w + 0x3FFu + odd;
-  const uint64_t q = (v >> 11) | ((uint64_t)(v < w) << 53);
-  const uint64_t S = (uint64_t)(int64_t)(int32_t)s;
-  const uint64_t m = (q ^ S) + (S & ((1ull << 53) + 1));
-  *out = __longlong_as_double(
-      (long long)((S & 0x8000000000000000ull) + ((uint64_t)(E + 1022) << 52) + m));
-  return true;
-}
-
 // Conversions through the hardware's integer-to-floating-point rounding.
 // A value S rounds alike directly and through its round-to-odd window: with
 // S = W 2^k + r (0 <= r < 2^k, W = floor(S / 2^k)), W' = W | [r != 0] is
@@ -837,12 +802,6 @@ __device__ __forceinline__ fx::I192 i192_shfl_up(fx::I192 v, int d) {
   r.w1 = __shfl_up_sync(0xffffffffu, v.w1, d);
   r.w2 = __shfl_up_sync(0xffffffffu, v.w2, d);
   return r;
-}
-// Warp sums of signed 192-bit values (every lane gets the total).
-__device__ __forceinline__ fx::I192 i192_warp_sum(fx::I192 v) {
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) v = fx::i192_add(v, fx::i192_shfl_xor(v, m));
-  return v;
 }
 // Exclusive warp scan; *total gets the warp sum.
 __device__ __forceinline__ fx::I192 i192_warp_exclusive(fx::I192 v, fx::I192* total) {

@@ -437,28 +437,6 @@ __device__ __forceinline__ bool i96_to_float_normal(I96 a, int lsb, uint32_t* ou
   return true;
 }
 
-// The same for a signed 64-bit a (one word level instead of two).
-__device__ __forceinline__ bool i64_to_float_normal(int64_t a, int lsb, uint32_t* out) {
-  const uint32_t lo = (uint32_t)(uint64_t)a, hi = (uint32_t)((uint64_t)a >> 32);
-  const uint32_t s = (uint32_t)((int32_t)hi >> 31);
-  const bool z1 = hi == s;
-  const uint32_t top = z1 ? lo : hi, nxt = z1 ? 0u : lo;
-  const int e = z1 ? -32 : 0;                             // bit position of nxt
-  const uint32_t lz = (uint32_t)__clz((int)(top ^ s));    // 32 only for a = 0 or -1
-  const int E = e + 63 - (int)lz + lsb;                   // exponent of bit p
-  if (lz == 32u || (unsigned)(E + 126) > 253u) return false;
-  const uint32_t v = funnel_l(nxt, top, lz);              // bits p .. p - 31
-  const uint32_t below = shl_clamp32(nxt, (int)lz);
-  const uint32_t st = ((v & 0x7Fu) | below) != 0u ? 1u : 0u;
-  const uint32_t odd = (v >> 8) & 1u;
-  const uint32_t w = (v & ~0x7Fu) | st;
-  const uint32_t u = w + 0x7Fu + odd;
-  const uint32_t q = (u >> 8) | ((uint32_t)(u < w) << 24);
-  const uint32_t m = (q ^ s) + (s & ((1u << 24) + 1u));
-  *out = (s & 0x80000000u) + ((uint32_t)(E + 126) << 23) + m;
-  return true;
-}
-
 // Correct rounding of a * 2^lsb to float for |a| * 2^lsb >= 2^-126 or a = 0
 // (the fast path's grids guarantee it); overflow gives +-Inf.
 __device__ __forceinline__ float i96_to_float(I96 a, int lsb) {
