@@ -15,6 +15,7 @@ the CPU oracle's rate are reported on the same JSON line.
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -270,11 +271,19 @@ def load_traffic(kernel_row: str):
 def run_e2e(args, api, torch, h32, h64, hA, dev, stream):
     """Same step through the C ABI from pinned host buffers: every input is
     copied host->device once and every result device->host inside the timed
-    region.  Input copies run on one stream, in the order the rows use them,
-    and result copies on another, each after an event on the compute stream,
-    so copies in both directions overlap the rows' kernels.  The host link
-    (about 208 GB/s in, 191 GB/s out, measured with pinned copies) bounds
-    this number, not the kernels."""
+    region.  Each 1e8-element vector goes over the link in chunks (the
+    library's binned states carry the sums across them):
+    - chunk 0's cumulative sum is a plain call, chunk j's continues from the
+      state of chunks 0..j-1 (repro_cumsum_from_state), and the chunk is
+      then deposited into that state; the state's value is the vector's sum.
+      Binned states merge exactly, so every output has the bits of the
+      one-call cumulative sum and sum (checked below, outside the timed
+      region);
+    - input copies run on one stream, in the order the calls use them, and
+      result copies on another, each after an event on the compute stream,
+      so a chunk's results go back while later chunks come in.
+    The host link (about 210 GB/s in, 190 GB/s out, measured with pinned
+    copies) bounds this number, not the kernels."""
     p32 = torch.from_numpy(h32).pin_memory()
     p64 = torch.from_numpy(h64).pin_memory()
     pA = torch.from_numpy(hA).pin_memory()
@@ -293,55 +302,92 @@ def run_e2e(args, api, torch, h32, h64, hA, dev, stream):
     s32 = torch.empty(1, dtype=torch.float32, device=dev)
     s64 = torch.empty(1, dtype=torch.float64, device=dev)
     seg = torch.empty(ROWS, dtype=torch.float32, device=dev)
+    var = torch.empty(ROWS, dtype=torch.float32, device=dev)
+    mean = torch.empty(ROWS, dtype=torch.float32, device=dev)
+    st32 = api.state_new(torch.float32, 3, device=dev, stream=stream)
+    st64 = api.state_new(torch.float64, 3, device=dev, stream=stream)
     copy_stream = torch.cuda.Stream(device=dev)
     h2d_stream = torch.cuda.Stream(device=dev)
+    # chunk bounds: multiples of 64 elements, so every chunk starts 256-byte aligned
+    nch = max(1, args.e2e_chunks)
+    step = -(-N_SUM // nch)
+    step = -(-step // 64) * 64
+    bounds = [(a, min(N_SUM, a + step)) for a in range(0, N_SUM, step)]
+
+    # events made once (each is recorded at most once per step, and a step
+    # ends with a device synchronisation)
+    ev_pool = [torch.cuda.Event() for _ in range(4 * len(bounds) + 8)]
+    ev_next = [0]
+
+    def event():
+        ev = ev_pool[ev_next[0]]
+        ev_next[0] += 1
+        return ev
 
     def back(dst, src):
         # device->host on the copy stream once `src` is complete
-        ev = torch.cuda.Event()
+        ev = event()
         ev.record(stream)
         copy_stream.wait_event(ev)
         with torch.cuda.stream(copy_stream):
             dst.copy_(src, non_blocking=True)
 
-    def one():
-        # inputs host->device on their own stream, in the order the rows use
-        # them: the double array first, so that its 800 MB cumulative sum
-        # goes back over the link while the other inputs still come in
-        evs = []
+    def send(dst, src):
         with torch.cuda.stream(h2d_stream):
-            for dst, src in ((d64, p64), (dA, pA), (d32, p32)):
-                dst.copy_(src, non_blocking=True)
-                ev = torch.cuda.Event()
-                ev.record(h2d_stream)
-                evs.append(ev)
+            dst.copy_(src, non_blocking=True)
+            ev = event()
+            ev.record(h2d_stream)
+        return ev
+
+    def vector(d, c, oc, st, s, so, evs):
+        # on the compute stream: every chunk's cumulative sum, then the sum
+        api.state_init(st, d.dtype, 3)
+        for j, (a, b) in enumerate(bounds):
+            stream.wait_event(evs[j])
+            if j == 0:
+                api.repro_cumsum(d[a:b], out=c[a:b], K=3)
+            else:
+                api.repro_cumsum_from_state(d[a:b], st, K=3, out=c[a:b])
+            back(oc[a:b], c[a:b])
+            api.state_deposit(st, d[a:b], K=3)
+        api.state_finalize(st, d.dtype, 3, out=s)
+        back(so, s)
+
+    def one():
+        # inputs in the order the calls use them: the double vector first, so
+        # that its 800 MB of cumulative sums go back while the rest comes in
+        ev_next[0] = 0
+        e64 = [send(d64[a:b], p64[a:b]) for a, b in bounds]
+        eA = send(dA, pA)
+        e32 = [send(d32[a:b], p32[a:b]) for a, b in bounds]
         with torch.cuda.stream(stream):
-            stream.wait_event(evs[0])
-            api.repro_sum_async(d64, s64, 3)
-            back(os64, s64)
-            api.repro_cumsum(d64, out=c64, K=3)
-            back(oc64, c64)
-            stream.wait_event(evs[1])
-            v, m = api.stable_var(dA, axis=1, ddof=1)
-            back(ov, v)
-            back(om, m)
+            vector(d64, c64, oc64, st64, s64, os64, e64)
+            stream.wait_event(eA)
+            api.stable_var(dA, axis=1, ddof=1, out=var, mean_out=mean)
+            back(ov, var)
+            back(om, mean)
             api.repro_segsum(dA, axis=1, K=3, out=seg)
             back(oseg, seg)
-            stream.wait_event(evs[2])
-            api.repro_sum_async(d32, s32, 3)
-            back(os32, s32)
-            api.repro_cumsum(d32, out=c32, K=3)
-            back(oc32, c32)
+            vector(d32, c32, oc32, st32, s32, os32, e32)
         torch.cuda.synchronize()
 
     one()
     n = max(1, args.e2e_steps)
     times = []
-    for _ in range(n):
-        t = time.perf_counter()
-        one()
-        times.append(time.perf_counter() - t)
+    # no garbage collection inside the timed steps (as timeit does)
+    gc.collect()
+    gc_on = gc.isenabled()
+    gc.disable()
+    try:
+        for _ in range(n):
+            t = time.perf_counter()
+            one()
+            times.append(time.perf_counter() - t)
+    finally:
+        if gc_on:
+            gc.enable()
     dt = sum(times) / n
+    check_e2e(api, torch, dev, stream, (d32, d64, dA), (oc32, oc64, os32, os64, ov, om, oseg))
     elems = sum(nn for _, nn, _ in ROWS_SPEC)
     h2d = 4 * N_SUM + 8 * N_SUM + 4 * ROWS * COLS
     d2h = 4 * N_SUM + 8 * N_SUM + 4 + 8 + 3 * 4 * ROWS
@@ -349,10 +395,36 @@ def run_e2e(args, api, torch, h32, h64, hA, dev, stream):
     link = measure_link(torch, dev)
     return {"value": round(elems / dt / 1e9, 3), "unit": "GElements/s", "ms_per_step": round(dt * 1e3, 3),
             "ms_per_step_min": round(min(times) * 1e3, 3), "ms_per_step_max": round(max(times) * 1e3, 3),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "ms_per_step_median": round(sorted(times)[len(times) // 2] * 1e3, 3),
+            "ms_steps": [round(t * 1e3, 3) for t in times],
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n, "chunks": len(bounds),
+            "bits_equal_to_resident_calls": True,
             "link_gbs": link,
             "link_bound_ms": round(max(h2d / link["h2d"], d2h / link["d2h"]) / 1e6, 3),
             "host_api": run_host_api(api, torch, h32, h64)}
+
+
+def check_e2e(api, torch, dev, stream, inputs, outs):
+    """The end-to-end leg's host results against the one-call device results
+    on the same (device-resident) inputs, bit for bit; raises on any
+    difference."""
+    d32, d64, dA = inputs
+    oc32, oc64, os32, os64, ov, om, oseg = outs
+    with torch.cuda.stream(stream):
+        want = {
+            "cumsum_f32": (oc32, api.repro_cumsum(d32, K=3)),
+            "cumsum_f64": (oc64, api.repro_cumsum(d64, K=3)),
+            "sum_f32": (os32, api.repro_sum_async(d32, torch.empty(1, dtype=torch.float32, device=dev), 3)),
+            "sum_f64": (os64, api.repro_sum_async(d64, torch.empty(1, dtype=torch.float64, device=dev), 3)),
+            "segsum": (oseg, api.repro_segsum(dA, axis=1, K=3)),
+        }
+        v, m = api.stable_var(dA, axis=1, ddof=1)
+        want["var"], want["mean"] = (ov, v), (om, m)
+    torch.cuda.synchronize()
+    for name, (got, ref) in want.items():
+        it = torch.int64 if got.dtype == torch.float64 else torch.int32
+        if not torch.equal(got.view(it), ref.cpu().view(it)):
+            raise RuntimeError("end-to-end %s differs from the one-call device result" % name)
 
 
 def measure_link(torch, dev):
@@ -663,6 +735,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-chunks", type=int, default=8,
+                    help="chunks per 1e8-element vector in the end-to-end leg")
     ap.add_argument("--k", type=int, default=3,
                     help="fold count of the sum and cumulative-sum rows (for profiling other K; the metric is "
                          "quoted at K = 3)")

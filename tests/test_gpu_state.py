@@ -174,6 +174,34 @@ def test_cumsum_from_state_continues_the_whole_scan(dt, K):
 
 
 @pytest.mark.parametrize("dt", [F32, F64])
+def test_chunked_pipeline_equals_one_call(dt):
+    """The chunked form of a long input (as the benchmark's end-to-end leg
+    streams it over the host link): chunk 0 by the plain cumulative sum
+    (fixed-index path), chunk j from the state of chunks 0..j-1, each chunk
+    then deposited; the outputs and the state's value are the oracle's
+    cumulative sum and sum of the whole input."""
+    dev()
+    n = 2_000_003
+    x = data(dt, n, 71)
+    want = oracle.adn_cumsum(x, 3)
+    t = to_dev(x)
+    out = torch.empty_like(t)
+    st = api.state_new(t.dtype, 3)
+    step = -(-n // 8)
+    step = -(-step // 64) * 64
+    for j, a in enumerate(range(0, n, step)):
+        b = min(n, a + step)
+        if j == 0:
+            api.repro_cumsum(t[a:b], out=out[a:b], K=3)
+        else:
+            api.repro_cumsum_from_state(t[a:b], st, 3, out=out[a:b])
+        api.state_deposit(st, t[a:b], 3)
+    got = out.cpu().numpy()
+    assert same_bits(got, want), np.flatnonzero(got.view(np.uint8) != want.view(np.uint8))[:3]
+    assert same_bits(final(st, dt, 3), np.array([oracle.adn_sum(x, 3, "fp")], dt)[0])
+
+
+@pytest.mark.parametrize("dt", [F32, F64])
 def test_cumsum_from_state_specials_and_mismatch(dt):
     dev()
     x = data(dt, 5000, 71)
