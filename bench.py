@@ -401,6 +401,7 @@ def run_e2e(args, api, torch, h32, h64, hA, dev, stream):
             "bits_equal_to_resident_calls": True,
             "link_gbs": link,
             "link_bound_ms": round(max(h2d / link["h2d"], d2h / link["d2h"]) / 1e6, 3),
+            "link_bound_ms_duplex": round(max(h2d / link["h2d_duplex"], d2h / link["d2h_duplex"]) / 1e6, 3),
             "host_api": run_host_api(api, torch, h32, h64)}
 
 
@@ -428,7 +429,8 @@ def check_e2e(api, torch, dev, stream, inputs, outs):
 
 
 def measure_link(torch, dev):
-    """Pinned host<->device copy rates (GB/s) of 1 GiB, best of three."""
+    """Pinned host<->device copy rates (GB/s) of 1 GiB, best of three: each
+    direction alone, and both at once."""
     nb = 1 << 30
     h = torch.empty(nb, dtype=torch.uint8).pin_memory()
     d = torch.empty(nb, dtype=torch.uint8, device=dev)
@@ -444,7 +446,32 @@ def measure_link(torch, dev):
             torch.cuda.synchronize()
             best = min(best, a.elapsed_time(b) * 1e-3)
         out[name] = round(nb / best / 1e9, 1)
-    del h, d
+    # both directions at once, each on its own stream (the end-to-end leg's
+    # copies overlap like this)
+    h2 = torch.empty(nb, dtype=torch.uint8).pin_memory()
+    d2 = torch.empty(nb, dtype=torch.uint8, device=dev)
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    best_in = best_out = 1e9
+    for _ in range(3):
+        torch.cuda.synchronize()
+        go = torch.cuda.Event()
+        go.record()
+        evs = []
+        for st, dst, src in ((s_in, d, h), (s_out, h2, d2)):
+            st.wait_event(go)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            with torch.cuda.stream(st):
+                dst.copy_(src, non_blocking=True)
+            b.record(st)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        best_in = min(best_in, evs[0][0].elapsed_time(evs[0][1]) * 1e-3)
+        best_out = min(best_out, evs[1][0].elapsed_time(evs[1][1]) * 1e-3)
+    out["h2d_duplex"] = round(nb / best_in / 1e9, 1)
+    out["d2h_duplex"] = round(nb / best_out / 1e9, 1)
+    del h, d, h2, d2
     return out
 
 
