@@ -308,11 +308,7 @@ def run_e2e(args, api, torch, h32, h64, hA, dev, stream):
     st64 = api.state_new(torch.float64, 3, device=dev, stream=stream)
     copy_stream = torch.cuda.Stream(device=dev)
     h2d_stream = torch.cuda.Stream(device=dev)
-    # chunk bounds: multiples of 64 elements, so every chunk starts 256-byte aligned
-    nch = max(1, args.e2e_chunks)
-    step = -(-N_SUM // nch)
-    step = -(-step // 64) * 64
-    bounds = [(a, min(N_SUM, a + step)) for a in range(0, N_SUM, step)]
+    bounds = chunk_bounds(N_SUM, max(1, args.e2e_chunks))
 
     # events made once (each is recorded at most once per step, and a step
     # ends with a device synchronisation)
@@ -403,6 +399,14 @@ def run_e2e(args, api, torch, h32, h64, hA, dev, stream):
             "link_bound_ms": round(max(h2d / link["h2d"], d2h / link["d2h"]) / 1e6, 3),
             "link_bound_ms_duplex": round(max(h2d / link["h2d_duplex"], d2h / link["d2h_duplex"]) / 1e6, 3),
             "host_api": run_host_api(api, torch, h32, h64)}
+
+
+def chunk_bounds(n: int, nch: int):
+    """[start, end) of nch nearly equal chunks of an n-element vector:
+    multiples of 64 elements, so every chunk starts 256-byte aligned."""
+    step = -(-n // nch)
+    step = -(-step // 64) * 64
+    return [(a, min(n, a + step)) for a in range(0, n, step)]
 
 
 def check_e2e(api, torch, dev, stream, inputs, outs):
