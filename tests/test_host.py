@@ -118,3 +118,17 @@ def test_forced_environment_failure(monkeypatch):
     assert lib.repro_sum_kahan_f32(p, ctypes.c_size_t(64), q, None) == ENV
     assert not out.any()
     monkeypatch.delenv("REPRO_FORCE_ENV_FAIL")
+
+
+@pytest.mark.parametrize("n,nch", [(100_000_000, 8), (100_000_000, 1), (40_000_000, 12), (1000, 8), (100, 8),
+                                   (64, 3), (1, 4)])
+def test_end_to_end_chunk_bounds(n, nch):
+    """The end-to-end leg's chunks tile [0, n) in order, start on 64-element
+    boundaries (256-byte aligned for both element types) and number at most
+    nch."""
+    import bench
+    b = bench.chunk_bounds(n, nch)
+    assert 1 <= len(b) <= nch
+    assert b[0][0] == 0 and b[-1][1] == n
+    assert all(x[1] == y[0] for x, y in zip(b, b[1:]))
+    assert all(e > s and s % 64 == 0 for s, e in b)
