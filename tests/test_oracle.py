@@ -361,6 +361,27 @@ def test_empty_and_zero_inputs(orc):
         assert same_bits(orc.adn_sum(np.array([1.0, -1.0], dt), 3), dt(0.0))
 
 
+def test_segmented_sums_are_per_slice_sums(orc):
+    """A segmented sum is one ADN sum per slice of a row-major array: each
+    row (axis 1) or column (axis 0) against the sequential primary form of
+    that slice alone, a different route from the closed form the segmented
+    oracle uses, and, on integer data, the exact sums."""
+    rng = np.random.default_rng(21)
+    a = (rng.standard_normal((37, 53)) * np.exp2(rng.integers(-30, 30, (37, 1)))).astype(F32)
+    a[5, 7] = F32(3e30)                     # one slice with a far higher index
+    for K in (2, 3, 5):
+        rows = orc.segsum(a, 1, K)
+        cols = orc.segsum(a, 0, K)
+        assert rows.shape == (37,) and cols.shape == (53,)
+        for r in range(37):
+            assert same_bits(rows[r], F32(orc.adn_sum(np.ascontiguousarray(a[r]), K, "fp")))
+        for c in range(53):
+            assert same_bits(cols[c], F32(orc.adn_sum(np.ascontiguousarray(a[:, c]), K, "fp")))
+    z = rng.integers(-1000, 1000, (19, 23)).astype(F32)
+    assert np.array_equal(orc.segsum(z, 1, 3), z.astype(np.int64).sum(axis=1).astype(F32))
+    assert np.array_equal(orc.segsum(z, 0, 3), z.astype(np.int64).sum(axis=0).astype(F32))
+
+
 # ------------------------------------------------------ comparison modes
 def test_comparison_modes(orc):
     # the controlled case the reductions page alludes to: Neumaier keeps the
