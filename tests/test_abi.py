@@ -103,6 +103,17 @@ def test_state_calls_check_arguments_first(L):
         assert fin(odd, 3, good, None) == 1
     assert L.repro_state_init_f32(good, 22, None) == 1     # float folds: K <= 21
     assert L.repro_state_init_f64(good, 53, None) == 1
+    # cumulative sums from a state: K, capacity, state, then the arrays
+    for t, cap, esz in (("f32", 4294966785, 4), ("f64", 9223372036854773761, 8)):
+        cs = getattr(L, "repro_cumsum_from_state_" + t)
+        assert cs(good, good, 10, 1, good, None) == 1
+        assert cs(None, None, cap, 3, good, None) == 2
+        assert cs(good, good, 10, 3, None, None) == 1
+        assert cs(good, good, 10, 3, odd, None) == 1
+        assert cs(None, None, 0, 3, good, None) == 0          # empty: nothing is touched
+        assert cs(None, good, 10, 3, good, None) == 1
+        assert cs(P(0x1002), good, 10, 3, good, None) == 1   # misaligned input
+        assert cs(P(0x100000), P(0x100000 + esz), 16, 3, good, None) == 3   # partial overlap
 
 
 def test_strerror(L):
