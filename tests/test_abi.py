@@ -116,6 +116,26 @@ def test_state_calls_check_arguments_first(L):
         assert cs(P(0x100000), P(0x100000 + esz), 16, 3, good, None) == 3   # partial overlap
 
 
+class Launch(ctypes.Structure):
+    _fields_ = [("block", ctypes.c_int), ("grid", ctypes.c_int)]
+
+
+def test_launch_shapes_are_checked_first(L):
+    """The *_ex and *_async calls reject a block size off [32, 1024] or not
+    a multiple of 32, and a negative grid, before any pointer is touched."""
+    P = ctypes.c_void_p
+    good = P(0x100)
+    bad = [Launch(16, 0), Launch(33, 0), Launch(2048, 0), Launch(256, -1)]
+    for t in ("f32", "f64"):
+        sa = getattr(L, "repro_sum_%s_async" % t)
+        cx = getattr(L, "repro_cumsum_%s_ex" % t)
+        for b in bad:
+            assert sa(good, 1000, 3, None, good, ctypes.byref(b)) == 1, (t, b.block, b.grid)
+            assert cx(good, good, 1000, 3, None, ctypes.byref(b)) == 1, (t, b.block, b.grid)
+        assert sa(good, 1000, 3, None, None, None) == 1        # no result pointer
+        assert sa(good, 1000, 3, None, P(0x101), None) == 1    # misaligned result pointer
+
+
 def test_strerror(L):
     for s in range(7):
         assert L.repro_strerror(s)
