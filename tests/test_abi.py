@@ -136,6 +136,19 @@ def test_launch_shapes_are_checked_first(L):
         assert sa(good, 1000, 3, None, P(0x101), None) == 1    # misaligned result pointer
 
 
+def test_comparison_sums_check_arguments_first(L):
+    P = ctypes.c_void_p
+    good = P(0x100)
+    for m in ("naive", "pairwise", "kahan", "neumaier"):
+        for t, esz in (("f32", 4), ("f64", 8)):
+            f = getattr(L, "repro_sum_%s_%s" % (m, t))
+            assert f(None, 10, good, None) == 1                 # null input
+            assert f(P(0x100 + esz // 2), 10, good, None) == 1  # misaligned input
+            assert f(good, 10, None, None) == 1                 # null result
+            assert f(good, 10, P(0x100 + esz // 2), None) == 1  # misaligned result
+            assert f(good, (1 << 40) + 1, good, None) == 2      # above the supported length
+
+
 def test_strerror(L):
     for s in range(7):
         assert L.repro_strerror(s)
