@@ -149,6 +149,39 @@ def test_comparison_sums_check_arguments_first(L):
             assert f(good, (1 << 40) + 1, good, None) == 2      # above the supported length
 
 
+def test_variance_and_noalloc_calls_check_arguments_first(L):
+    P = ctypes.c_void_p
+    good = P(0x100)
+    i64 = ctypes.c_int64
+    # float64 kernel: shape, ddof and alignment
+    v64 = L.stable_var_f64
+    assert v64(good, i64(4), i64(4), 2, 0, good, None, None) == 1
+    assert v64(good, i64(4), i64(4), 1, 4, good, None, None) == 1
+    assert v64(good, i64(0), i64(4), 1, 0, good, None, None) == 1
+    assert v64(P(0x104), i64(4), i64(4), 1, 0, good, None, None) == 1
+    assert v64(good, i64(4), i64(4), 1, 0, None, None, None) == 1
+    assert v64(good, i64(4), i64(4), 1, 0, good, P(0x104), None) == 1
+    # complex64: 8-byte pairs
+    vc = L.stable_var_c64
+    assert vc(P(0x104), i64(4), i64(4), 1, 0, good, None, None) == 1
+    assert vc(good, i64(4), i64(4), 1, 0, good, P(0x104), None) == 1
+    assert vc(good, i64(4), i64(4), 0, 4, good, None, None) == 1
+    # variants 0..6 only
+    vv = L.stable_var_f32_variant
+    for variant in (-1, 7):
+        assert vv(good, i64(4), i64(4), 1, 0, variant, good, None, None) == 1
+    assert L.twoterm_var_f32(good, i64(4), i64(4), 3, 0, good, None) == 1
+    # allocation-free sum: K, capacity, pointers
+    na = L.repro_sum_f32_noalloc
+    for K in (1, 22):
+        assert na(good, 10, K, None, good) == 1
+    assert na(None, 4294966785, 3, None, good) == 2
+    assert na(None, 10, 3, None, good) == 1
+    assert na(P(0x102), 10, 3, None, good) == 1
+    assert na(good, 10, 3, None, None) == 1
+    assert na(good, 10, 3, None, P(0x102)) == 1
+
+
 def test_strerror(L):
     for s in range(7):
         assert L.repro_strerror(s)
